@@ -1,0 +1,244 @@
+"""The five synthetic paged-attention workloads, as plain data.
+
+Every workload is seeded (seed = 2630 + its number) and describes only the
+*inputs*: sequence lengths, query-chunk lengths, the order in which physical
+blocks are handed out by the pool, the shared prefix, the copy-on-write fork,
+and the counter-based value streams for Q, K and V.  Building block tables,
+writing the cache and computing attention are left to the two sides (the CUDA
+library and the oracle), each with its own code.
+
+Recipes (the shapes follow Llama-3 layers; "1K" = 1,024 tokens):
+
+1. ``tiny``      4 sequences of 300/2,000/600/4,400 tokens; Hq 8, Hkv 2; pool of
+                 512 blocks handed out in a seeded random order; bf16.
+2. ``llama8b``   64 sequences, length uniform in [512, 4096]; Hq 32, Hkv 8;
+                 pool of 65,536 blocks in random order; bf16.
+3. ``llama70b_prefix``  128 sequences sharing one 2,000-token prefix (125 blocks,
+                 ref-counted), then a private tail of floor(exp(U[ln 1K, ln 32K]))
+                 tokens; Hq 64, Hkv 8; each sequence forks logical block 124 with
+                 copy-on-write before its tail is written; bf16.
+4. ``mixed_prefill``  one 1,024-token query chunk over 100,000 cached tokens
+                 (context 101,024) plus 255 decode sequences of length uniform in
+                 [1K, 8K]; Hq 64, Hkv 8; bf16.
+5. ``split_fp8`` 8 sequences of 131,072 tokens; Hq 64, Hkv 8; fp8-e4m3 cache with
+                 per-head scales; 16 split-KV partitions.
+
+For every sequence the step's "new" tokens (the last ``q_len`` positions) are
+the ones appended by the cache write in the step; all earlier positions are
+written while the workload is set up.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+from . import IH4_MAX_ABS, normal_bf16, stream_key
+
+__all__ = ["Workload", "make_workload", "WORKLOADS", "small_workload"]
+
+Q_STREAM, K_STREAM, V_STREAM = 0, 1, 2
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    num_q_heads: int
+    num_kv_heads: int
+    num_blocks: int
+    kv_dtype: str                    # "bf16" or "fp8"
+    context_lens: np.ndarray         # int32 [B]; includes the step's new tokens
+    q_lens: np.ndarray               # int32 [B]; 1 for decode rows
+    free_order: np.ndarray           # int32 [num_blocks]; first entry is handed out first
+    prefix_tokens: int = 0           # tokens of one prefix shared by every sequence
+    cow_block: int = -1              # logical block forked by copy-on-write (-1: none)
+    num_splits: int = 0              # split-KV partitions per sequence (0: library picks)
+    head_dim: int = 128
+    block_size: int = 16
+    description: str = ""
+    _tail_base: np.ndarray = field(default=None, repr=False)
+
+    def __post_init__(self):
+        self.context_lens = np.asarray(self.context_lens, dtype=np.int32)
+        self.q_lens = np.asarray(self.q_lens, dtype=np.int32)
+        self.free_order = np.asarray(self.free_order, dtype=np.int32)
+        tails = (self.context_lens.astype(np.int64) - self.prefix_tokens)
+        base = np.zeros(len(tails), dtype=np.int64)
+        if len(tails) > 1:
+            base[1:] = np.cumsum(tails)[:-1]
+        self._tail_base = base + self.prefix_tokens
+
+    # ------------------------------------------------------------------ sizes
+    @property
+    def num_seqs(self) -> int:
+        return int(len(self.context_lens))
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def total_q(self) -> int:
+        return int(self.q_lens.sum())
+
+    @property
+    def cu_q_lens(self) -> np.ndarray:
+        cu = np.zeros(self.num_seqs + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(self.q_lens)
+        return cu
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(-(-int(self.context_lens.max()) // self.block_size))
+
+    @property
+    def is_decode(self) -> bool:
+        return bool((self.q_lens == 1).all())
+
+    @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.kv_dtype == "fp8" else 2
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    # ------------------------------------------------------------ value keys
+    def token_keys(self, s: int, t0: int, t1: int) -> np.ndarray:
+        """Value-stream keys of tokens t0..t1-1 of sequence s (prefix tokens are
+        the same logical tokens in every sequence)."""
+        t = np.arange(t0, t1, dtype=np.int64)
+        key = self._tail_base[s] + (t - self.prefix_tokens)
+        if self.prefix_tokens:
+            key = np.where(t < self.prefix_tokens, t, key)
+        return key
+
+    def kv_values(self, which: str, keys, device="cpu") -> torch.Tensor:
+        """bf16 [len(keys)][Hkv][D] K or V rows for the given token keys."""
+        sid = K_STREAM if which == "k" else V_STREAM
+        keys = torch.as_tensor(np.asarray(keys, dtype=np.int64), device=device)
+        hd = self.num_kv_heads * self.head_dim
+        ctr = keys[:, None] * hd + torch.arange(hd, device=device, dtype=torch.int64)[None, :]
+        out = normal_bf16(stream_key(self.seed, sid), ctr)
+        return out.view(len(keys), self.num_kv_heads, self.head_dim)
+
+    def seq_kv(self, which: str, s: int, t0: int = 0, t1: int | None = None, device="cpu"):
+        if t1 is None:
+            t1 = int(self.context_lens[s])
+        return self.kv_values(which, self.token_keys(s, t0, t1), device)
+
+    def q_values(self, rows=None, device="cpu") -> torch.Tensor:
+        """bf16 [rows][Hq][D] query rows (global row index over all sequences)."""
+        if rows is None:
+            rows = np.arange(self.total_q, dtype=np.int64)
+        rows = torch.as_tensor(np.asarray(rows, dtype=np.int64), device=device)
+        hd = self.num_q_heads * self.head_dim
+        ctr = rows[:, None] * hd + torch.arange(hd, device=device, dtype=torch.int64)[None, :]
+        out = normal_bf16(stream_key(self.seed, Q_STREAM), ctr)
+        return out.view(len(rows), self.num_q_heads, self.head_dim)
+
+    def fp8_scales(self):
+        """Per-KV-head fp32 scales for K and V.  The generator's values are bounded
+        by IH4_MAX_ABS, so amax/448 with that bound maps every value into the
+        finite e4m3 range without saturation."""
+        s = np.float32(np.float32(IH4_MAX_ABS) / np.float32(448.0))
+        ks = np.full(self.num_kv_heads, s, dtype=np.float32)
+        return ks, ks.copy()
+
+    # ------------------------------------------------------------ bytes
+    def kv_bytes_per_token(self) -> int:
+        return 2 * self.num_kv_heads * self.head_dim * self.kv_elem_bytes
+
+    def summary(self) -> dict:
+        return {
+            "workload": self.name, "num_seqs": self.num_seqs, "num_q_heads": self.num_q_heads,
+            "num_kv_heads": self.num_kv_heads, "head_dim": self.head_dim,
+            "block_size": self.block_size, "kv_dtype": self.kv_dtype,
+            "num_blocks": self.num_blocks, "total_context_tokens": int(self.context_lens.sum()),
+            "total_q_tokens": self.total_q, "prefix_tokens": self.prefix_tokens,
+            "num_splits": self.num_splits,
+        }
+
+
+def _blocks(n, bs=16):
+    return -(-int(n) // bs)
+
+
+def _pool_to_fit(lens, prefix, cow, bs=16, slack=1.02):
+    need = 0
+    pb = _blocks(prefix, bs) if prefix else 0
+    for L in lens:
+        need += _blocks(L, bs) - pb
+    need += pb
+    if cow >= 0:
+        need += len(lens)
+    return int(math.ceil(need * slack / 1024.0) * 1024)
+
+
+def make_workload(name: str) -> Workload:
+    if name in ("tiny", "cfg1", "1"):
+        seed = 2631
+        rng = np.random.Generator(np.random.PCG64(seed))
+        lens = np.array([300, 2000, 600, 4400], dtype=np.int32)
+        pool = 512
+        return Workload("tiny", seed, 8, 2, pool, "bf16", lens, np.ones(4, np.int32),
+                        rng.permutation(pool), description="tiny paged decode, GQA 4")
+    if name in ("llama8b", "cfg2", "2"):
+        seed = 2632
+        rng = np.random.Generator(np.random.PCG64(seed))
+        lens = rng.integers(512, 4096, size=64, endpoint=True).astype(np.int32)
+        pool = 65536
+        return Workload("llama8b", seed, 32, 8, pool, "bf16", lens, np.ones(64, np.int32),
+                        rng.permutation(pool), description="Llama-3-8B layer-shape decode, batch 64")
+    if name in ("llama70b_prefix", "cfg3", "3"):
+        seed = 2633
+        rng = np.random.Generator(np.random.PCG64(seed))
+        u = rng.uniform(math.log(1024), math.log(32768), size=128)
+        tails = np.floor(np.exp(u)).astype(np.int64)
+        lens = (2000 + tails).astype(np.int32)
+        pool = _pool_to_fit(lens, 2000, 124)
+        return Workload("llama70b_prefix", seed, 64, 8, pool, "bf16", lens,
+                        np.ones(128, np.int32), rng.permutation(pool), prefix_tokens=2000,
+                        cow_block=124,
+                        description="Llama-3-70B layer-shape decode, batch 128, shared 2,000-token prefix")
+    if name in ("mixed_prefill", "cfg4", "4"):
+        seed = 2634
+        rng = np.random.Generator(np.random.PCG64(seed))
+        dec = rng.integers(1024, 8192, size=255, endpoint=True).astype(np.int32)
+        lens = np.concatenate([[101024], dec]).astype(np.int32)
+        qlens = np.concatenate([[1024], np.ones(255, np.int64)]).astype(np.int32)
+        pool = _pool_to_fit(lens, 0, -1)
+        return Workload("mixed_prefill", seed, 64, 8, pool, "bf16", lens, qlens,
+                        rng.permutation(pool),
+                        description="chunked-prefill mix: 1,024-token chunk over 100,000 cached tokens + 255 decodes")
+    if name in ("split_fp8", "cfg5", "5"):
+        seed = 2635
+        rng = np.random.Generator(np.random.PCG64(seed))
+        lens = np.full(8, 131072, dtype=np.int32)
+        pool = 65536
+        return Workload("split_fp8", seed, 64, 8, pool, "fp8", lens, np.ones(8, np.int32),
+                        rng.permutation(pool), num_splits=16,
+                        description="long-context split-KV decode, fp8-e4m3 cache, 16 partitions")
+    raise KeyError(name)
+
+
+WORKLOADS = ("tiny", "llama8b", "llama70b_prefix", "mixed_prefill", "split_fp8")
+
+
+def small_workload(seed: int, lens, q_lens=None, hq=8, hkv=2, kv_dtype="bf16", num_blocks=None,
+                   prefix_tokens=0, cow_block=-1, num_splits=0, head_dim=128, block_size=16,
+                   name="small") -> Workload:
+    """A small workload for parity tests: same recipe, caller-chosen sizes."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens = np.asarray(lens, dtype=np.int32)
+    if q_lens is None:
+        q_lens = np.ones(len(lens), np.int32)
+    if num_blocks is None:
+        num_blocks = _pool_to_fit(lens, prefix_tokens, cow_block, block_size, 1.5)
+    return Workload(name, seed, hq, hkv, num_blocks, kv_dtype, lens, q_lens,
+                    rng.permutation(num_blocks), prefix_tokens=prefix_tokens,
+                    cow_block=cow_block, num_splits=num_splits, head_dim=head_dim,
+                    block_size=block_size)

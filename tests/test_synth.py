@@ -1,0 +1,71 @@
+"""The seeded input generator: bit-exact to its published definition, and the
+workload recipes have the stated shapes."""
+import math
+
+import numpy as np
+import torch
+
+from synth import GAMMA, IH4_MAX_ABS, MASK64, mix13_t, normal_bf16, splitmix64_py, stream_key
+from synth.workloads import WORKLOADS, make_workload
+
+
+def test_splitmix64_reference_values():
+    # first outputs of SplitMix64 seeded with 0 (state advanced by GAMMA before mixing)
+    expect = [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+    got = [splitmix64_py((i + 1) * GAMMA & MASK64) for i in range(3)]
+    assert got == expect
+
+
+def test_torch_mix_matches_python_bigints():
+    rng = np.random.default_rng(1)
+    vals = [int(x) for x in rng.integers(0, 1 << 63, size=2000, dtype=np.int64)]
+    vals += [0, 1, (1 << 63) - 1]
+    t = torch.tensor(vals, dtype=torch.int64)
+    got = mix13_t(t).numpy().astype(np.uint64)
+    ref = np.array([splitmix64_py(v) for v in vals], dtype=np.uint64)
+    assert np.array_equal(got, ref)
+
+
+def test_normal_moments_and_bound():
+    key = stream_key(2630, 1)
+    x = normal_bf16(key, torch.arange(1 << 20)).float()
+    assert abs(x.mean().item()) < 0.01
+    assert abs(x.var().item() - 1.0) < 0.01
+    assert x.abs().max().item() <= IH4_MAX_ABS * (1 + 2 ** -8)
+    assert abs(IH4_MAX_ABS - 131070 * math.sqrt(3) / 65536) < 1e-6
+
+
+def test_counter_based_values_are_position_independent():
+    key = stream_key(5, 2)
+    full = normal_bf16(key, torch.arange(1000))
+    part = normal_bf16(key, torch.arange(500, 700))
+    assert torch.equal(full[500:700], part)
+
+
+def test_workload_recipes():
+    for name in WORKLOADS:
+        wl = make_workload(name)
+        assert wl.num_q_heads % wl.num_kv_heads == 0
+        assert sorted(wl.free_order.tolist()) == list(range(wl.num_blocks))
+    wl = make_workload("tiny")
+    assert wl.context_lens.tolist() == [300, 2000, 600, 4400] and wl.num_blocks == 512
+    wl = make_workload("llama8b")
+    assert len(wl.context_lens) == 64 and wl.context_lens.min() >= 512 and wl.context_lens.max() <= 4096
+    assert (wl.num_q_heads, wl.num_kv_heads, wl.num_blocks) == (32, 8, 65536)
+    wl = make_workload("llama70b_prefix")
+    tails = wl.context_lens - 2000
+    assert len(tails) == 128 and tails.min() >= 1024 and tails.max() <= 32768
+    need = 125 + 128 + sum(-(-int(t) // 16) for t in tails)
+    assert wl.num_blocks >= need
+    wl = make_workload("mixed_prefill")
+    assert wl.q_lens[0] == 1024 and wl.context_lens[0] == 101024 and (wl.q_lens[1:] == 1).all()
+    assert wl.context_lens[1:].min() >= 1024 and wl.context_lens[1:].max() <= 8192
+    wl = make_workload("split_fp8")
+    assert (wl.context_lens == 131072).all() and wl.kv_dtype == "fp8" and wl.num_splits == 16
+
+
+def test_prefix_tokens_share_keys():
+    wl = make_workload("llama70b_prefix")
+    a = wl.token_keys(0, 0, 2010)
+    b = wl.token_keys(5, 0, 2010)
+    assert np.array_equal(a[:2000], b[:2000]) and not np.array_equal(a[2000:], b[2000:])
