@@ -1,0 +1,251 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache attention library.
+ *
+ * The library implements the data-parallel hot path of PagedAttention: a KV
+ * cache held in fixed 16-token physical blocks, reached through a
+ * per-sequence block table, with GQA head groups, ref-counted shared-prefix
+ * blocks with copy-on-write, chunked-prefill query chunks mixed with decode
+ * queries, split-KV partitions merged by a log-sum-exp reduction, and an
+ * fp8-e4m3 cache.
+ *
+ * Sources (web pages; cited by title and section):
+ *  [P1] "PagedAttention, chunked prefill, and the launch that cascades"
+ *       (deepnotes.pages.dev), sections "PagedAttention: an OS idea, not an ML
+ *       one", "Serving systems: the layer that survives real traffic",
+ *       "FlashAttention: why the mechanism this whole layer runs on isn't
+ *       compute-bound", "Kernel engineering: the layer underneath everything
+ *       else here".
+ *  [P2] "Waste, and three ways to reclaim it" (runbooks.in, Document 10 - Quick
+ *       learn), sections "PagedAttention - operating-system virtual memory,
+ *       applied to attention", "Sharing, and what makes a prefix reusable",
+ *       "Quantising the cache".
+ *  [P3] "M.65 Inference serving" (systemdesigntutorial.com), paragraphs on the
+ *       KV-cache memory math, PagedAttention block management (a)-(h),
+ *       prefill vs decode (a)-(f), and quantisation (a)-(f).
+ *
+ * Conventions for every call:
+ *  - Fixed geometry: head_dim D = 128 and block size BS = 16 tokens ([P3] block
+ *    management (a): fixed at compile time, 16 tokens).  Other values are not
+ *    representable in the ABI.
+ *  - Cache layout (chosen here; the pages give none): k_cache and v_cache are
+ *    each [num_blocks][num_kv_heads][16][128] elements of the cache dtype, so one
+ *    (block, kv head) tile is contiguous: 4 KiB in bf16, 2 KiB in fp8.
+ *  - Query/output layout: q is [rows][num_q_heads][128] bf16; out is
+ *    [rows][num_q_heads][128] fp32.  Query head h reads KV head h / G, with
+ *    G = num_q_heads / num_kv_heads (the repeat_interleave grouping of [P1]
+ *    "Kernel engineering"); G must be 1, 2, 4, 8 or 16.
+ *  - Block ids are int32.  Unused block-table entries may hold any value; only
+ *    the first ceil(context_len / 16) entries of a row are read.
+ *  - Ownership: every device buffer (caches, q, out, tables, lengths, slot
+ *    mapping, scales, workspace) belongs to the caller; the attention and
+ *    cache-write calls allocate no device memory.  A kv_pool is a host object
+ *    owned by the library between kv_pool_create and kv_pool_destroy.
+ *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Device
+ *    work is enqueued asynchronously; the calls return once it is launched.
+ *  - Errors: every call returns a kv_status; nothing is thrown across the ABI.
+ *    Host-visible argument errors are reported before anything is launched
+ *    (KV_ERR_INVALID / KV_ERR_UNSUPPORTED); launch failures as KV_ERR_CUDA.
+ *    Errors that only device data can show (a block id outside the pool, a slot
+ *    outside the pool, a context length outside [1, max_blocks_per_seq*16], a
+ *    query chunk longer than its context, a pipeline wait that timed out) never
+ *    fault: the kernel skips the offending access, sets a sticky device status
+ *    word and continues; kv_last_device_status() reports and clears it.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PAGEDKV_API __attribute__((visibility("default")))
+#else
+#define PAGEDKV_API
+#endif
+
+#define PAGEDKV_HEAD_DIM 128
+#define PAGEDKV_BLOCK_SIZE 16
+
+typedef enum {
+    KV_OK = 0,
+    KV_ERR_INVALID = 1,        /* bad argument, double free, sharing a free block */
+    KV_ERR_OUT_OF_BLOCKS = 2,  /* pool exhausted; the pool is left unchanged */
+    KV_ERR_UNSUPPORTED = 3,    /* shape or dtype this build does not handle */
+    KV_ERR_CUDA = 4,           /* a CUDA runtime/driver call or launch failed */
+    KV_ERR_DEVICE_BOUNDS = 5   /* device data was out of range (see above) */
+} kv_status;
+
+typedef enum { KV_BF16 = 0, KV_FP8_E4M3 = 1 } kv_dtype;
+
+typedef struct kv_pool kv_pool; /* opaque, host-only */
+
+typedef struct {
+    int32_t num_blocks;      /* pool size */
+    int32_t free_blocks;     /* blocks on the free list */
+    int32_t live_blocks;     /* blocks with refcount >= 1 */
+    int32_t shared_blocks;   /* blocks with refcount >= 2 */
+    int64_t cow_copies;      /* copy-on-write forks that copied a block */
+    int64_t alloc_failures;  /* allocations refused for lack of blocks */
+} kv_pool_stats_t;
+
+/* Human-readable name of a status code (static storage). */
+PAGEDKV_API const char *kv_status_string(kv_status s);
+
+/* ------------------------------------------------------------------------
+ * Host block manager: free-list pool, block ids, refcounts, copy-on-write.
+ * [P3] block management (b) per-request block table, (c) O(1) allocation from
+ * a free list and return of all blocks on completion, (e) reference-counted
+ * prefix sharing, (g) copy-on-write; [P2] "Sharing, and what makes a prefix
+ * reusable" (one physical copy, many block tables; copy on write).
+ * Free-list order is deterministic: a LIFO stack whose first hand-out is
+ * initial_free_order[0] (ascending ids when NULL); a freed block is the next
+ * one handed out.  All calls on one pool are serialised by a mutex.
+ * ---------------------------------------------------------------------- */
+
+/* Creates a pool of num_blocks (>= 1) blocks.  initial_free_order, if not NULL,
+ * must be a permutation of 0..num_blocks-1 (KV_ERR_INVALID otherwise). */
+PAGEDKV_API kv_status kv_pool_create(int32_t num_blocks, const int32_t *initial_free_order, kv_pool **out);
+PAGEDKV_API void kv_pool_destroy(kv_pool *pool);
+
+/* Allocates n (>= 0) blocks into out_ids[0..n) with refcount 1.  All-or-nothing:
+ * on KV_ERR_OUT_OF_BLOCKS nothing changes except stats.alloc_failures. */
+PAGEDKV_API kv_status kv_block_alloc(kv_pool *pool, int32_t n, int32_t *out_ids);
+
+/* Drops one reference per listed id (an id may repeat, once per reference it
+ * drops); a block reaching refcount 0 returns to the free list, in list order.
+ * Validated first: any id not holding enough references -> KV_ERR_INVALID and
+ * nothing changes. */
+PAGEDKV_API kv_status kv_block_free(kv_pool *pool, const int32_t *ids, int32_t n);
+
+/* Adds one reference per listed id; every id must be live (refcount >= 1),
+ * else KV_ERR_INVALID and nothing changes. */
+PAGEDKV_API kv_status kv_block_share(kv_pool *pool, const int32_t *ids, int32_t n);
+
+/* Copy-on-write of block `id` before a write into it.
+ *  refcount == 1: *out_id = id; nothing is copied.
+ *  refcount >= 2: one new block is allocated (KV_ERR_OUT_OF_BLOCKS if none, pool
+ *    unchanged), the caller's reference moves to it (old refcount - 1), and --
+ *    if k_cache and v_cache are not NULL -- all num_kv_heads tiles of K and V of
+ *    `id` are copied to the new block by a kernel on `stream`.  With both cache
+ *    pointers NULL only the bookkeeping is done and the caller copies.
+ *  The caches must hold the pool's num_blocks blocks in the layout above. */
+PAGEDKV_API kv_status kv_copy_on_write(kv_pool *pool, int32_t id, int32_t *out_id, void *k_cache,
+                           void *v_cache, int32_t num_kv_heads, kv_dtype dtype, void *stream);
+
+/* Current refcount of block id (0 = free). */
+PAGEDKV_API kv_status kv_block_refcount(const kv_pool *pool, int32_t id, int32_t *out);
+
+PAGEDKV_API kv_status kv_pool_stats(const kv_pool *pool, kv_pool_stats_t *out);
+
+/* Host fault injection: the k-th kv_block_alloc call from now (k >= 1),
+ * including the allocation inside kv_copy_on_write, fails with
+ * KV_ERR_OUT_OF_BLOCKS exactly as if the pool were empty; k <= 0 disarms. */
+PAGEDKV_API kv_status kv_pool_fail_alloc_after(kv_pool *pool, int32_t k);
+
+/* ------------------------------------------------------------------------
+ * Cache write ("blocks allocated on demand as a sequence grows" [P1]
+ * "PagedAttention: an OS idea"; [P3] block management (c)).
+ *  k, v          device, bf16 [num_tokens][num_kv_heads][128]
+ *  slot_mapping  device, int64 [num_tokens]; token t goes to block slot/16,
+ *                offset slot%16; a negative slot skips the token (padding)
+ *  k_cache/v_cache  device, layout above, num_blocks blocks
+ *  dtype KV_BF16: the bytes are copied.  KV_FP8_E4M3: each element is stored as
+ *    e4m3(round-to-nearest-even, saturating at +-448)(fp32(x) / scale[h]) with
+ *    the IEEE fp32 division and per-KV-head k_scale/v_scale (device fp32
+ *    [num_kv_heads]); [P2] "Quantising the cache", [P3] quantisation (b),(d).
+ *  A slot >= num_blocks*16 is skipped and flagged (KV_ERR_DEVICE_BOUNDS).
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API kv_status reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                            const int64_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                            int32_t num_blocks, kv_dtype dtype, const float *k_scale,
+                            const float *v_scale, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Paged attention, decode: one query token per sequence at position
+ * context_len-1, attending keys 0..context_len-1 read through the block table
+ * ([P2] "PagedAttention", "a matching attention kernel that knows how to read
+ * from scattered blocks"; [P3] block management (d)).  Softmax is computed
+ * online, block by block ([P1] "FlashAttention": running max and normaliser).
+ * Long contexts are cut into split-KV partitions of whole logical blocks;
+ * partitions are merged with a log-sum-exp reduction (the running max and
+ * normaliser of two partitions combine exactly).  Split points depend only on
+ * logical positions, and no atomics touch the arithmetic, so the output is
+ * bitwise identical under any physical placement of the blocks.
+ *
+ *  out            device fp32 [num_seqs][num_q_heads][128]
+ *  q              device bf16 [num_seqs][num_q_heads][128]
+ *  block_tables   device int32 [num_seqs][max_blocks_per_seq]
+ *  context_lens   device int32 [num_seqs], 1 <= len <= max_blocks_per_seq*16
+ *  scale          softmax scale (1/sqrt(128) for the standard head)
+ *  dtype          cache element type; for KV_FP8_E4M3 k_scale/v_scale are the
+ *                 device fp32 [num_kv_heads] dequantisation scales
+ *  num_splits     maximum partitions per sequence; partition length is
+ *                 ceil(max_blocks_per_seq / num_splits) blocks.  0 = choose.
+ *  workspace      device scratch of at least paged_attention_workspace_size()
+ *                 bytes (256-byte aligned), or NULL when that size is 0.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t max_blocks_per_seq, int32_t num_splits);
+
+PAGEDKV_API kv_status paged_attention_decode(float *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                 int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t num_blocks, float scale, kv_dtype dtype,
+                                 const float *k_scale, const float *v_scale, int32_t num_splits,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Paged attention over a mixed batch of chunked-prefill and decode queries
+ * ([P1] "Serving systems": long prompts split into ~1K-token chunks interleaved
+ * with decode; [P3] prefill vs decode (e)).  Sequence s owns query rows
+ * cu_q_lens[s] .. cu_q_lens[s+1]-1; its n_s rows sit at positions
+ * context_len-n_s .. context_len-1, row i attends keys 0 .. context_len-n_s+i
+ * (causal inside the chunk, everything before it visible).  Rows with n_s = 1
+ * are decode rows and take the decode kernel; chunks (n_s >= 2) take the
+ * tensor-core (tcgen05) kernel.
+ *
+ *  out, q          device [total_q_tokens][num_q_heads][128] (fp32 / bf16)
+ *  cu_q_lens       device int32 [num_seqs+1], cu_q_lens[0] = 0, non-decreasing,
+ *                  cu_q_lens[num_seqs] = total_q_tokens
+ *  context_lens    device int32 [num_seqs]; includes the chunk; n_s <= len
+ *  max_q_len       host int: an upper bound on every n_s (sizes the grid)
+ *  other arguments as for paged_attention_decode; workspace must be at least
+ *  paged_attention_chunked_prefill_workspace_size() bytes.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API size_t paged_attention_chunked_prefill_workspace_size(int32_t num_seqs, int32_t total_q_tokens,
+                                                      int32_t max_q_len, int32_t num_q_heads,
+                                                      int32_t num_kv_heads,
+                                                      int32_t max_blocks_per_seq,
+                                                      int32_t num_splits);
+
+PAGEDKV_API kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32_t *cu_q_lens,
+                                          const int32_t *context_lens, int32_t num_seqs,
+                                          int32_t total_q_tokens, int32_t max_q_len,
+                                          const void *k_cache, const void *v_cache,
+                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                          int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t num_blocks, float scale, kv_dtype dtype,
+                                          const float *k_scale, const float *v_scale,
+                                          int32_t num_splits, void *workspace,
+                                          size_t workspace_bytes, void *stream);
+
+/* Waits for `stream`, then returns and clears the sticky device status word
+ * set by earlier calls (KV_OK or KV_ERR_DEVICE_BOUNDS); KV_ERR_CUDA if the
+ * stream itself reports an error. */
+PAGEDKV_API kv_status kv_last_device_status(void *stream);
+
+/* Bit flags of the last non-OK device status (0 if none), for diagnostics:
+ * 1 block id outside the pool, 2 slot outside the pool, 4 bad context length
+ * or chunk, 8 a pipeline wait timed out.  Read together with
+ * kv_last_device_status (which clears them). */
+PAGEDKV_API uint32_t kv_last_device_status_flags(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

@@ -1,0 +1,294 @@
+"""GB300-native paged KV-cache attention: Python binding of libpagedkv.so.
+
+The binding only marshals arguments: every step runs in the library (host
+block manager in C++, kernels in CUDA for sm_103a).  Functions carry the
+C-ABI names of ``include/pagedkv.h``; torch tensors supply device memory and
+the current CUDA stream.  There is no fallback: if the library is missing or
+a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "KVError", "lib", "KVPool", "kv_status_string", "reshape_and_cache",
+    "paged_attention_workspace_size", "paged_attention_decode",
+    "paged_attention_chunked_prefill_workspace_size", "paged_attention_chunked_prefill",
+    "kv_last_device_status", "kv_last_device_status_flags", "KV_BF16", "KV_FP8_E4M3",
+    "HEAD_DIM", "BLOCK_SIZE", "library_path",
+]
+
+HEAD_DIM = 128
+BLOCK_SIZE = 16
+KV_BF16, KV_FP8_E4M3 = 0, 1
+_STATUS = {0: "ok", 1: "invalid argument", 2: "out of blocks", 3: "unsupported",
+           4: "CUDA error", 5: "device data out of range"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libpagedkv.so")
+_lib = None
+
+
+class KVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {_STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+class _Stats(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("free_blocks", ctypes.c_int32),
+                ("live_blocks", ctypes.c_int32), ("shared_blocks", ctypes.c_int32),
+                ("cow_copies", ctypes.c_int64), ("alloc_failures", ctypes.c_int64)]
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"{library_path} is not built (run __graft_entry__.build())")
+        L = ctypes.CDLL(library_path)
+        c = ctypes
+        P, I, I64, F, SZ = c.c_void_p, c.c_int32, c.c_int64, c.c_float, c.c_size_t
+        sig = {
+            "kv_status_string": (c.c_char_p, [c.c_int]),
+            "kv_pool_create": (c.c_int, [I, P, c.POINTER(P)]),
+            "kv_pool_destroy": (None, [P]),
+            "kv_block_alloc": (c.c_int, [P, I, P]),
+            "kv_block_free": (c.c_int, [P, P, I]),
+            "kv_block_share": (c.c_int, [P, P, I]),
+            "kv_copy_on_write": (c.c_int, [P, I, c.POINTER(I), P, P, I, c.c_int, P]),
+            "kv_block_refcount": (c.c_int, [P, I, c.POINTER(I)]),
+            "kv_pool_stats": (c.c_int, [P, c.POINTER(_Stats)]),
+            "kv_pool_fail_alloc_after": (c.c_int, [P, I]),
+            "reshape_and_cache": (c.c_int, [P, P, P, P, P, I, I, I, c.c_int, P, P, P]),
+            "paged_attention_workspace_size": (SZ, [I, I, I, I]),
+            "paged_attention_decode": (c.c_int, [P, P, P, P, P, I, P, I, I, I, I, F, c.c_int, P, P,
+                                                 I, P, SZ, P]),
+            "paged_attention_chunked_prefill_workspace_size": (SZ, [I, I, I, I, I, I, I]),
+            "paged_attention_chunked_prefill": (c.c_int, [P, P, P, P, I, I, I, P, P, P, I, I, I, I,
+                                                          F, c.c_int, P, P, I, P, SZ, P]),
+            "kv_last_device_status": (c.c_int, [P]),
+            "kv_last_device_status_flags": (c.c_uint32, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise KVError(st, where)
+
+
+def kv_status_string(st: int) -> str:
+    return lib().kv_status_string(st).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dt(kv_dtype) -> int:
+    if kv_dtype in (KV_BF16, "bf16", torch.bfloat16):
+        return KV_BF16
+    if kv_dtype in (KV_FP8_E4M3, "fp8", "fp8_e4m3", torch.float8_e4m3fn, torch.uint8):
+        return KV_FP8_E4M3
+    raise ValueError(f"unsupported kv dtype {kv_dtype}")
+
+
+def _need(t, name, dtype=None, dev=True, contig=True):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if dev and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if contig and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _cache_dtype(k_cache):
+    return KV_BF16 if k_cache.dtype == torch.bfloat16 else KV_FP8_E4M3
+
+
+# ------------------------------------------------------------------- pool
+class KVPool:
+    """Host block manager (free list, refcounts, copy-on-write)."""
+
+    def __init__(self, num_blocks: int, initial_free_order=None):
+        L = lib()
+        self._p = ctypes.c_void_p()
+        order = None
+        if initial_free_order is not None:
+            import numpy as np
+            order = np.ascontiguousarray(initial_free_order, dtype=np.int32)
+            if order.shape != (num_blocks,):
+                raise ValueError("initial_free_order must have num_blocks entries")
+        _check(L.kv_pool_create(int(num_blocks), None if order is None else order.ctypes.data_as(ctypes.c_void_p),
+                                ctypes.byref(self._p)), "kv_pool_create")
+        self.num_blocks = int(num_blocks)
+
+    def close(self):
+        if self._p:
+            lib().kv_pool_destroy(self._p)
+            self._p = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self, n: int):
+        import numpy as np
+        out = np.empty(max(int(n), 0), dtype=np.int32)
+        _check(lib().kv_block_alloc(self._p, int(n), out.ctypes.data_as(ctypes.c_void_p)), "kv_block_alloc")
+        return out
+
+    def free(self, ids):
+        import numpy as np
+        a = np.ascontiguousarray(ids, dtype=np.int32)
+        _check(lib().kv_block_free(self._p, a.ctypes.data_as(ctypes.c_void_p), a.size), "kv_block_free")
+
+    def share(self, ids):
+        import numpy as np
+        a = np.ascontiguousarray(ids, dtype=np.int32)
+        _check(lib().kv_block_share(self._p, a.ctypes.data_as(ctypes.c_void_p), a.size), "kv_block_share")
+
+    def copy_on_write(self, block_id: int, k_cache=None, v_cache=None, stream=None) -> int:
+        """Returns the block to write into; copies K/V on the device if caches are given."""
+        out = ctypes.c_int32()
+        if k_cache is None:
+            st = lib().kv_copy_on_write(self._p, int(block_id), ctypes.byref(out), None, None, 0, 0, None)
+        else:
+            _need(k_cache, "k_cache")
+            _need(v_cache, "v_cache")
+            st = lib().kv_copy_on_write(self._p, int(block_id), ctypes.byref(out), _ptr(k_cache),
+                                        _ptr(v_cache), int(k_cache.shape[1]), _cache_dtype(k_cache),
+                                        _stream(stream))
+        _check(st, "kv_copy_on_write")
+        return int(out.value)
+
+    def refcount(self, block_id: int) -> int:
+        out = ctypes.c_int32()
+        _check(lib().kv_block_refcount(self._p, int(block_id), ctypes.byref(out)), "kv_block_refcount")
+        return int(out.value)
+
+    def stats(self) -> dict:
+        s = _Stats()
+        _check(lib().kv_pool_stats(self._p, ctypes.byref(s)), "kv_pool_stats")
+        return {"num_blocks": s.num_blocks, "free": s.free_blocks, "live": s.live_blocks,
+                "shared": s.shared_blocks, "cow_copies": s.cow_copies, "alloc_failures": s.alloc_failures}
+
+    def fail_alloc_after(self, k: int):
+        _check(lib().kv_pool_fail_alloc_after(self._p, int(k)), "kv_pool_fail_alloc_after")
+
+
+# ------------------------------------------------------------------ kernels
+def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None, stream=None):
+    """Scatter K/V rows [T][Hkv][128] (bf16) into the paged caches at slot_mapping."""
+    _need(k, "k", torch.bfloat16)
+    _need(v, "v", torch.bfloat16)
+    _need(k_cache, "k_cache", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn))
+    _need(v_cache, "v_cache", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn))
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    T, hkv, d = k.shape
+    if d != HEAD_DIM or tuple(v.shape) != (T, hkv, d) or k_cache.shape[1:] != (hkv, BLOCK_SIZE, HEAD_DIM):
+        raise ValueError("shape mismatch")
+    dt = _cache_dtype(k_cache)
+    _check(lib().reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+                                   T, hkv, k_cache.shape[0], dt, _ptr(k_scale), _ptr(v_scale),
+                                   _stream(stream)), "reshape_and_cache")
+
+
+def paged_attention_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq, num_splits=0) -> int:
+    return int(lib().paged_attention_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq, num_splits))
+
+
+def paged_attention_chunked_prefill_workspace_size(num_seqs, total_q_tokens, max_q_len, num_q_heads,
+                                                   num_kv_heads, max_blocks_per_seq, num_splits=0) -> int:
+    return int(lib().paged_attention_chunked_prefill_workspace_size(
+        num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq, num_splits))
+
+
+def _workspace(nbytes, device):
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale=None,
+                           k_scale=None, v_scale=None, num_splits=0, workspace=None, stream=None):
+    """Decode attention: out[B][Hq][128] fp32 from q[B][Hq][128] bf16 over the paged cache."""
+    _need(out, "out", torch.float32)
+    _need(q, "q", torch.bfloat16)
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache")
+    _need(block_tables, "block_tables", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    B, hq, d = q.shape
+    nb, hkv = k_cache.shape[0], k_cache.shape[1]
+    mb = block_tables.shape[1]
+    if scale is None:
+        scale = HEAD_DIM ** -0.5
+    need = paged_attention_workspace_size(B, hq, mb, num_splits)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().paged_attention_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                        mb, _ptr(context_lens), B, hq, hkv, nb, float(scale),
+                                        _cache_dtype(k_cache), _ptr(k_scale), _ptr(v_scale), int(num_splits),
+                                        _ptr(workspace), ws_bytes, _stream(stream)), "paged_attention_decode")
+    return out
+
+
+def paged_attention_chunked_prefill(out, q, cu_q_lens, context_lens, max_q_len, k_cache, v_cache,
+                                    block_tables, scale=None, k_scale=None, v_scale=None, num_splits=0,
+                                    workspace=None, stream=None):
+    """Mixed chunked-prefill / decode attention over the paged cache."""
+    _need(out, "out", torch.float32)
+    _need(q, "q", torch.bfloat16)
+    _need(cu_q_lens, "cu_q_lens", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    _need(block_tables, "block_tables", torch.int32)
+    R, hq, d = q.shape
+    B = context_lens.shape[0]
+    nb, hkv = k_cache.shape[0], k_cache.shape[1]
+    mb = block_tables.shape[1]
+    if scale is None:
+        scale = HEAD_DIM ** -0.5
+    need = paged_attention_chunked_prefill_workspace_size(B, R, int(max_q_len), hq, hkv, mb, num_splits)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().paged_attention_chunked_prefill(
+        _ptr(out), _ptr(q), _ptr(cu_q_lens), _ptr(context_lens), B, R, int(max_q_len), _ptr(k_cache),
+        _ptr(v_cache), _ptr(block_tables), mb, hq, hkv, nb, float(scale), _cache_dtype(k_cache),
+        _ptr(k_scale), _ptr(v_scale), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)),
+        "paged_attention_chunked_prefill")
+    return out
+
+
+def kv_last_device_status(stream=None) -> int:
+    """Synchronises the stream; returns 0 or 5 (device data out of range), clearing it."""
+    st = lib().kv_last_device_status(_stream(stream))
+    if st not in (0, 5):
+        raise KVError(st, "kv_last_device_status")
+    return st
+
+
+def kv_last_device_status_flags() -> int:
+    return int(lib().kv_last_device_status_flags())
