@@ -1,0 +1,388 @@
+"""Benchmark of one paged-attention layer step on GB300.
+
+Default workload: Llama-3-8B layer-shape decode (64 sequences, 32 query / 8 KV
+heads, head_dim 128, contexts uniform in [512, 4096], bf16 cache in a
+65,536-block pool, one new token per sequence appended with reshape_and_cache
+through a slot mapping).  A step is the whole hot path for that batch: the
+cache write of the new tokens, then paged decode attention (split-KV
+partitions merged by the log-sum-exp kernel).
+
+Reported metric: achieved HBM GB/s of the step -- algorithmic bytes (every
+K/V element of every sequence read once, Q read, O written, block-table rows
+and lengths read, new K/V written) divided by the measured step time -- and
+microseconds per layer step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+With --gpus N > 1 (launched by torchrun), every rank runs its own batch of the
+same recipe (weak scaling, no collective on the data path); the timed region
+is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of peak) and µs per layer step"
+UNIT = "GB/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x across the ranks of the default process group (the
+    timing rule: the slowest rank's time); x itself when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(bytes_per_rank_step: float, world_size: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank processes its own batch of the same size, so
+    the units of all ranks are divided by the slowest rank's step time."""
+    return world_size * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for ln in f:
+                p = [x.strip() for x in ln.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.remove(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _traffic(kernel_src):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
+    if that summary was taken on the current kernel source; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_llama8b_traffic.json")) as f:
+            d = json.load(f)
+        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+        return int(d["traffic_bytes_per_launch"]) if d.get("kernel_source_sha256") == sha else None
+    except Exception:
+        return None
+
+
+# -------------------------------------------------------------- CPU oracle
+class OracleSample:
+    """The fp64 oracle (as it stands) on the first ``m`` sequences of the
+    workload: block tables from the oracle's allocator model, a compact pool
+    holding only those sequences' blocks, the oracle's own scatter; ``run()``
+    is one call of the paged oracle on that sample."""
+
+    def __init__(self, wl, m):
+        import numpy as np
+        import torch
+
+        import oracle
+        from oracle import model as omodel
+        from synth.workloads import Workload
+
+        self.oracle = oracle
+        m = max(1, min(int(m), wl.num_seqs))
+        sub = Workload(wl.name + "_sample", wl.seed, wl.num_q_heads, wl.num_kv_heads, 0, wl.kv_dtype,
+                       wl.context_lens[:m], wl.q_lens[:m], np.zeros(0, np.int32), wl.prefix_tokens,
+                       wl.cow_block, wl.num_splits)
+        nblk = int(sum(-(-int(L) // 16) for L in sub.context_lens))
+        sub.num_blocks = nblk + (m if sub.cow_block >= 0 else 0)
+        sub.free_order = np.arange(sub.num_blocks, dtype=np.int32)
+        self.tb = omodel.build_tables(sub)
+        self.kc, self.vc = omodel.build_cache(sub, self.tb)
+        self.q = sub.q_values().contiguous().view(torch.int16).numpy().view(np.uint16)
+        self.code = oracle.FP8 if sub.kv_dtype == "fp8" else oracle.BF16
+        self.ks, self.vs = sub.fp8_scales() if self.code == oracle.FP8 else (None, None)
+        self.cu = None if sub.is_decode else sub.cu_q_lens
+        self.sub, self.m, self.wl = sub, m, wl
+        eb = sub.kv_elem_bytes
+        kv_bytes = 2 * nblk * sub.num_kv_heads * 16 * 128 * eb
+        self.algo_bytes = kv_bytes + sub.total_q * sub.num_q_heads * 128 * (2 + 4)
+
+    def run(self):
+        self.oracle.paged_attention(self.q, self.kc, self.vc, self.tb.tables, self.sub.context_lens, self.cu,
+                                    dtype=self.code, k_scale=self.ks, v_scale=self.vs, scale=self.sub.scale)
+
+    def describe(self):
+        return (f"first {self.m} of {self.wl.num_seqs} sequences ({int(self.sub.context_lens.sum())} "
+                f"context tokens) of the same workload, fp64 paged oracle")
+
+
+def cpu_oracle_baseline(wl, budget_s=10.0, max_seqs=16):
+    smp = OracleSample(wl, max_seqs)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        smp.run()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    per = el / reps
+    return {"value": smp.algo_bytes / per / 1e9, "unit": UNIT, "cores": smp.oracle.max_threads(),
+            "kind": "oracle", "sample": f"{smp.describe()}, {reps} calls in {el:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is one oracle call on a sample
+    of the workload sized so that W + K steps take about two minutes."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from synth.workloads import make_workload
+    wl = make_workload(args.workload)
+    probe = OracleSample(wl, 1)
+    t0 = time.perf_counter()
+    probe.run()
+    per_seq = max(time.perf_counter() - t0, 1e-6)
+    budget = args.ref_budget / max(1, args.steps + args.warmup)
+    smp = OracleSample(wl, min(args.ref_seqs, max(1, int(budget / per_seq))))
+    for _ in range(args.warmup):
+        smp.run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        smp.run()
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    v = smp.algo_bytes * len(times) / total / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "sample": smp.describe(), "device": "host cores"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": smp.oracle.max_threads(), "kind": "oracle",
+                             "sample": smp.describe()},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args):
+    import torch
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import paged_kv_cache_263_gb300 as pkv
+    from paged_kv_cache_263_gb300 import build as pkv_build
+    from paged_kv_cache_263_gb300.workload import DeviceWorkload
+    from synth.workloads import make_workload
+
+    pkv_build.build()
+    wl = make_workload(args.workload)
+    dw = DeviceWorkload(wl, device=dev)
+    ab = dw.algorithmic_bytes()
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    dw.step()
+    st = pkv.kv_last_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {pkv.kv_last_device_status_flags()}")
+
+    # ---- device-resident timed region: K steps, per-call events on the launching stream
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = Clocks(local)
+    clocks.start()                      # sampling covers the warm-up and the timed steps
+    for _ in range(args.warmup):
+        dw.step()
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        dw.write_new_tokens()
+        ev[i][1].record(stream)
+        dw.attention()
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    barrier()
+    ck = clocks.stop()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
+    ms_per_step = total_ms / K
+    attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    write_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    st = pkv.kv_last_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after timing")
+
+    # ---- end to end through the public API with pinned host buffers
+    h_q = dw.q.cpu().pin_memory()
+    h_k = dw.new_k.cpu().pin_memory()
+    h_v = dw.new_v.cpu().pin_memory()
+    h_slots = dw.slot_mapping.cpu().pin_memory()
+    h_tab = dw.block_tables.cpu().pin_memory()
+    h_len = dw.context_lens.cpu().pin_memory()
+    h_out = torch.empty(dw.out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_tab, h_len))
+    d2h = h_out.numel() * h_out.element_size()
+    E = max(3, min(K, 200))
+
+    def e2e_step():
+        dw.q.copy_(h_q, non_blocking=True)
+        dw.new_k.copy_(h_k, non_blocking=True)
+        dw.new_v.copy_(h_v, non_blocking=True)
+        dw.slot_mapping.copy_(h_slots, non_blocking=True)
+        dw.block_tables.copy_(h_tab, non_blocking=True)
+        dw.context_lens.copy_(h_len, non_blocking=True)
+        dw.step()
+        h_out.copy_(dw.out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, dev)
+
+    peak, peak_kind = _peaks()
+    step_bytes = ab["total"]
+    value = weak_scaling_value(step_bytes, ws, ms_per_step)
+    attn_bytes = ab["kv_unique"] + ab["q"] + ab["o"] + ab["meta"]
+    attn_avg = statistics.mean(attn_ms)
+    achieved = attn_bytes / (attn_avg * 1e-3) / 1e9
+    splits_used = pkv.paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, wl.max_blocks_per_seq,
+                                                     wl.num_splits) > 0
+    launches_per_step = 1 + 1 + (1 if splits_used else 0)
+    kv_bytes = ab["kv_unique"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "us_per_layer_step": ms_per_step * 1e3,
+        "pct_of_peak": 100.0 * value / ws / peak, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.kv_dtype == "bf16" else "fp8-e4m3 cache, f16 math",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+                   "num_kv_heads": wl.num_kv_heads, "head_dim": 128, "block_size": 16,
+                   "kv_dtype": wl.kv_dtype, "num_blocks": wl.num_blocks,
+                   "context_tokens": int(wl.context_lens.sum()), "new_tokens_per_step": wl.total_q,
+                   "kv_bytes_per_step": kv_bytes, "algorithmic_bytes_per_step": step_bytes,
+                   "l2": f"no flush: every step reads {kv_bytes / 1e6:.0f} MB of KV, "
+                         f"{kv_bytes / L2_BYTES:.1f}x the 129 MB L2",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "paged_attention_decode (decode kernel + LSE reduce)",
+                     "bytes_per_launch": attn_bytes, "avg_launch_ms": attn_avg,
+                     "traffic": _traffic(os.path.join(ROOT, "paged_kv_cache_263_gb300", "csrc", "decode.cu"))},
+        "cache_write_avg_ms": statistics.mean(write_ms),
+        "e2e": {"value": weak_scaling_value(step_bytes, ws, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "clocks": ck,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_baseline(wl, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-seqs", type=int, default=16)
+    ap.add_argument("--ref-budget", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
