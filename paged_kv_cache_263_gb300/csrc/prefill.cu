@@ -1,10 +1,468 @@
-// prefill.cu -- paged attention over mixed chunked-prefill / decode batches.
-// (work in progress: decode rows only)
+// prefill.cu -- paged attention over a mixed batch of chunked-prefill query
+// chunks and decode queries (sm_103a, 5th-generation tensor cores).
+//
+// A sequence with n >= 2 query rows is a prefill chunk: its rows sit at
+// positions L-n .. L-1 and row i attends keys 0 .. L-n+i (causal inside the
+// chunk, all earlier context visible) -- "PagedAttention, chunked prefill,
+// and the launch that cascades", section "Serving systems" (long prompts split
+// into ~1K-token chunks interleaved with decode); "M.65 Inference serving",
+// prefill vs decode (a) prefill is a dense O(N^2) contraction, (e) chunked
+// prefill.  Rows with n = 1 are decode rows and go to the decode kernel.
+//
+// Tensor-core kernel, one CTA per (128-row query tile, KV head, KV partition):
+//  * A query tile packs 128/G chunk tokens x the G query heads of one KV head
+//    (row = token * G + head), so every K/V tile is shared by the whole GQA
+//    group.  Q (3-D TMA box) stays in shared memory for the CTA's life.
+//  * K/V tiles of 128 keys = 8 physical blocks, gathered through the block
+//    table by 2-D TMA loads (128-byte swizzle), double-buffered.
+//  * S = Q K^T and O += P V run as tcgen05.mma (M=128, N=128, K=16 steps) issued
+//    by one thread, accumulators in tensor memory (S: 128 columns, O: 128).
+//    K is the K-major B operand of the first product; V is the MN-major B
+//    operand of the second, straight from the same swizzled tiles.
+//  * Four softmax warps own one TMEM lane (= one query row) per thread: they
+//    read S with tcgen05.ld, apply the causal mask on diagonal tiles, keep the
+//    online max / normaliser ("FlashAttention" section: running max and
+//    normaliser per block), write P in bf16 to shared memory in the operand
+//    layout, and rescale O in tensor memory only when the running max grew by
+//    more than 2^8 (otherwise the stale max is kept; exact in the end).
+//  * Long contexts are cut into partitions of whole 128-key tiles; partitions
+//    are merged by a fixed-order log-sum-exp kernel (no atomics).
 #include "common.cuh"
 
+#include <algorithm>
+
 namespace {
+
 __device__ uint32_t g_status;
+
+using namespace pkv;
+
+constexpr int BM = 128, BN = 128;
+constexpr int THREADS = 192;                    // warps 0-3 softmax, 4 TMA producer, 5 MMA issuer
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float RESCALE_LOG2 = 8.0f;
+constexpr uint32_t SQ = 0, SK0 = 32768, SV0 = 98304, SP = 163840, SBAR = 196608;
+constexpr int SMEM_BYTES = 196608 + 256 + 1024;
+enum { B_Q = 0, B_KVF0 = 1, B_KVF1 = 2, B_KVE0 = 3, B_KVE1 = 4, B_S = 5, B_P = 6, B_PV = 7, B_DRAIN = 8, NBAR = 9 };
+
+// instruction descriptors, kind::f16: fp32 accumulate, bf16 A and B, M=128, N=128
+constexpr uint32_t IDESC_KMAJ = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t IDESC_BMN = IDESC_KMAJ | (1u << 16);   // B operand MN-major (V)
+
+struct PrefillParams {
+    float *out;
+    const int32_t *cu_q_lens;
+    const int32_t *context_lens;
+    const int32_t *block_tables;
+    int32_t *tile_off;   // [num_seqs + 1] query tiles per sequence, prefix sums
+    float *part_o;       // [rows][Hq][max_splits][128]
+    float *part_ml;      // [rows][Hq][max_splits][2]
+    int max_blocks, num_seqs, hq, hkv, group, num_blocks, total_rows;
+    int tiles_per_split, max_splits;
+    float scale_log2;
+};
+
+__device__ __forceinline__ void flag(uint32_t bits) { atomicOr(&g_status, bits); }
+
+// bounded wait that also gives up as soon as another role has aborted
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                flag(ST_TIMEOUT);
+                return false;
+            }
+        }
+    }
 }
+
+// per-sequence query-tile counts -> prefix sums; validates chunk metadata
+__global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
+{
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t carry;
+    const int tpt = BM / p.group;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < p.num_seqs; base += blockDim.x) {
+        const int s = base + threadIdx.x;
+        int tiles = 0;
+        if (s < p.num_seqs) {
+            const int a = p.cu_q_lens[s], b = p.cu_q_lens[s + 1];
+            const int n = b - a, L = p.context_lens[s];
+            if (n >= 2) {
+                if (a < 0 || b > p.total_rows || L < n || L > p.max_blocks * BS) flag(ST_BAD_LEN);
+                else tiles = (n + tpt - 1) / tpt;
+            } else if (n < 0) {
+                flag(ST_BAD_LEN);
+            }
+        }
+        // block-wide inclusive scan
+        int v = tiles;
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int t = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += t;
+        }
+        if (lane == 31) warp_sums[w] = v;
+        __syncthreads();
+        if (w == 0) {
+            int x = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int t = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += t;
+            }
+            warp_sums[lane] = x;
+        }
+        __syncthreads();
+        const int incl = v + (w > 0 ? warp_sums[w - 1] : 0) + carry;
+        if (s < p.num_seqs) p.tile_off[s + 1] = incl;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = incl;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) p.tile_off[0] = 0;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SBAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    auto bar = [&](int i) -> uint32_t { return smem_u32(bars + i); };
+    // warp-uniform wait: every role below runs warp-collective instructions
+    // (ballots, tcgen05.ld/st), so a warp leaves a loop only as a whole
+    auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait_bar(b, parity, abort_flag));
+    };
+
+    // ---- which query tile / KV head / partition
+    const int x = blockIdx.x, g = blockIdx.y, split = blockIdx.z;
+    if (x >= p.tile_off[p.num_seqs]) return;
+    int lo = 0, hi = p.num_seqs;                 // tile_off[lo] <= x < tile_off[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.tile_off[mid] <= x) lo = mid;
+        else hi = mid;
+    }
+    const int s = lo, mt = x - p.tile_off[s];
+    const int row0 = p.cu_q_lens[s], n = p.cu_q_lens[s + 1] - row0, L = p.context_lens[s];
+    const int G = p.group, tpt = BM / G;
+    const int i0 = mt * tpt, i1 = min(n, i0 + tpt);
+    const int kmax = L - n + i1;                 // keys visible to the tile's last row
+    const int KT = (kmax + BN - 1) / BN;
+    const int j0 = split * p.tiles_per_split;
+    if (j0 >= KT) return;
+    const int j1 = min(KT, j0 + p.tiles_per_split);
+    const int T = j1 - j0;
+    const int nsplit = (KT + p.tiles_per_split - 1) / p.tiles_per_split;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B_Q), 1);
+        mbar_init(bar(B_KVF0), 1);
+        mbar_init(bar(B_KVF1), 1);
+        mbar_init(bar(B_KVE0), 1);
+        mbar_init(bar(B_KVE1), 1);
+        mbar_init(bar(B_S), 1);
+        mbar_init(bar(B_P), 128);
+        mbar_init(bar(B_PV), 1);
+        mbar_init(bar(B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tO = tmem + 128;
+
+    if (warp == 4) {
+        // ======================= TMA producer
+        const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks;
+        const int nblk = (L + BS - 1) / BS;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(B_Q), 2 * 16384);
+            tma_load_3d(sbase + SQ, &qmap, 0, g * G, row0 + i0, bar(B_Q));
+            tma_load_3d(sbase + SQ + 16384, &qmap, 64, g * G, row0 + i0, bar(B_Q));
+        }
+        int issued = 0;
+        for (int jj = 0; jj < T; ++jj) {
+            const int st = jj & 1;
+            if (jj >= 2 && !wait_w(bar(B_KVE0 + st), ((jj - 2) >> 1) & 1)) break;
+            const int j = j0 + jj;
+            const int b = j * 8 + (lane & 7);
+            int32_t id = -1;
+            if (lane < 8 && b < nblk) id = __ldg(bt + b);
+            const bool valid = lane < 8 && b < nblk && id >= 0 && id < p.num_blocks;
+            if (lane < 8 && b < nblk && !valid) flag(ST_BAD_BLOCK);
+            const unsigned vm = __ballot_sync(0xffffffffu, valid);
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar(B_KVF0 + st), __popc(vm) * 4 * 2048);
+            }
+            __syncwarp();
+            if (valid) {
+                const int y = (id * p.hkv + g) * BS;
+                const uint32_t kd = sbase + SK0 + st * 32768 + lane * 2048;
+                const uint32_t vd = sbase + SV0 + st * 32768 + lane * 2048;
+                tma_load_2d(kd, &kmap, 0, y, bar(B_KVF0 + st));
+                tma_load_2d(kd + 16384, &kmap, 64, y, bar(B_KVF0 + st));
+                tma_load_2d(vd, &vmap, 0, y, bar(B_KVF0 + st));
+                tma_load_2d(vd + 16384, &vmap, 64, y, bar(B_KVF0 + st));
+            }
+            issued = jj + 1;
+        }
+        if (*abort_flag) {
+            // let loads already in flight land before the CTA exits
+            for (int jj = max(0, issued - 2); jj < issued; ++jj)
+                (void)mbar_wait_bounded(bar(B_KVF0 + (jj & 1)), (jj >> 1) & 1);
+        }
+    } else if (warp == 5) {
+        // ======================= MMA issuer (+ zeroing of V rows past the context)
+        auto fix_tail = [&](int jj) {
+            // keys >= L of the tile: their V rows may hold anything (never written,
+            // or not loaded); P is 0 there, but 0 * NaN is NaN, so zero the rows
+            const int t0 = (j0 + jj) * BN;
+            const int first = L - t0;            // first invalid row in the tile
+            if (first >= BN) return;
+            const uint32_t vb = sbase + SV0 + (jj & 1) * 32768;
+            const int nchunks = (BN - first) * 2 * 8;   // rows x 2 halves x 8 chunks of 16 B
+            for (int c = lane; c < nchunks; c += 32) {
+                const int r = first + (c >> 4), h = (c >> 3) & 1, ch = c & 7;
+                st_shared_v4(vb + h * 16384 + r * 128 + ch * 16, 0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        };
+        auto issue_s = [&](int jj) {
+            if (lane == 0) {
+                tc_fence_after();
+                const uint32_t kb = sbase + SK0 + (jj & 1) * 32768;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    umma_f16(tS, sdesc_sw128(sbase + SQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                             IDESC_KMAJ, kk > 0);
+                }
+                umma_commit(bar(B_S));
+            }
+            __syncwarp();
+        };
+        bool ok = wait_w(bar(B_Q), 0) && wait_w(bar(B_KVF0), 0);
+        if (ok) {
+            fix_tail(0);
+            issue_s(0);
+            for (int jj = 0; jj < T; ++jj) {
+                if (!wait_w(bar(B_P), jj & 1)) break;
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t vb = sbase + SV0 + (jj & 1) * 32768;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t poff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        umma_f16(tO, sdesc_sw128(sbase + SP + poff, 16, 1024),
+                                 sdesc_sw128(vb + kk * 2048, 16384, 1024), IDESC_BMN, (jj > 0 || kk > 0));
+                    }
+                    umma_commit(bar(B_PV));
+                    umma_commit(bar(B_KVE0 + (jj & 1)));
+                }
+                __syncwarp();
+                if (jj + 1 < T) {
+                    if (!wait_w(bar(B_KVF0 + ((jj + 1) & 1)), ((jj + 1) >> 1) & 1)) break;
+                    fix_tail(jj + 1);
+                    issue_s(jj + 1);
+                }
+            }
+        }
+        // every MMA this thread issued has finished before TMEM is released
+        if (lane == 0) umma_commit(bar(B_DRAIN));
+        __syncwarp();
+        (void)mbar_wait_bounded(bar(B_DRAIN), 0);
+    } else {
+        // ======================= softmax warps: thread = query row = TMEM lane
+        const int r = threadIdx.x;                 // 0..127
+        const int i = i0 + r / G;
+        const int head = g * G + r % G;
+        const bool row_valid = i < i1;
+        // last key this row may attend; rows past the chunk (loaded only to fill the
+        // tile, never stored) take the tile's last valid row, so no row ever sees
+        // a key at or beyond L
+        const int pos = row_valid ? L - n + i : L - n + i1 - 1;
+        const int pos_min = L - n + i0;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int jj = 0; jj < T && ok; ++jj) {
+            const int t0 = (j0 + jj) * BN;
+            if (!wait_w(bar(B_S), jj & 1)) { ok = false; break; }
+            tc_fence_after();
+            float sv[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float tmp[32];
+                tmem_ld32(tS + lane_base + c * 32, tmp);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sv[c * 32 + e] = tmp[e];
+            }
+            const bool full = t0 + BN - 1 <= pos_min;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                float v = sv[c] * p.scale_log2;
+                if (!full && t0 + c > pos) v = -INFINITY;
+                sv[c] = v;
+                mx = fmaxf(mx, v);
+            }
+            float alpha = 1.f;
+            if (mx > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mx != -INFINITY)) {
+                alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx);
+                m_ref = mx;
+            }
+            if (jj > 0) {
+                if (!wait_w(bar(B_PV), (jj - 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float o[32];
+                        tmem_ld32(tO + lane_base + c * 32, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st32(tO + lane_base + c * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // P in bf16, K-major 128-byte-swizzled operand layout: row r, keys 0..127
+            float sum = 0.f;
+            const bool live = m_ref != -INFINITY;
+#pragma unroll
+            for (int c8 = 0; c8 < 16; ++c8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = live ? ex2(sv[c8 * 8 + 2 * e] - m_ref) : 0.f;
+                    const float p1 = live ? ex2(sv[c8 * 8 + 2 * e + 1] - m_ref) : 0.f;
+                    sum += p0 + p1;
+                    w[e] = pack_bf16(p0, p1);
+                }
+                const int kh = c8 >> 3, cw = c8 & 7;
+                st_shared_v4(sbase + SP + kh * 16384 + r * 128 + ((cw ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+            }
+            l = l * alpha + sum;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_P));
+        }
+        if (ok && wait_w(bar(B_PV), (T - 1) & 1)) {
+            tc_fence_after();
+            float o[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float tmp[32];
+                tmem_ld32(tO + lane_base + c * 32, tmp);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[c * 32 + e] = tmp[e];
+            }
+            if (row_valid) {
+                const size_t rh = (size_t)(row0 + i) * p.hq + head;
+                if (nsplit == 1) {
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    float4 *dst = reinterpret_cast<float4 *>(p.out + rh * D);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        dst[c] = make_float4(o[4 * c] * inv, o[4 * c + 1] * inv, o[4 * c + 2] * inv,
+                                             o[4 * c + 3] * inv);
+                } else {
+                    const size_t pi = rh * p.max_splits + split;
+                    float4 *dst = reinterpret_cast<float4 *>(p.part_o + pi * D);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        dst[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                    p.part_ml[pi * 2] = l > 0.f ? m_ref : -INFINITY;
+                    p.part_ml[pi * 2 + 1] = l;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// Log-sum-exp merge of prefill partitions: one warp per (query row, head).
+__global__ void __launch_bounds__(128) prefill_reduce_kernel(const PrefillParams p)
+{
+    const long wid = (long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (wid >= (long)p.total_rows * p.hq) return;
+    const int row = (int)(wid / p.hq), h = (int)(wid % p.hq);
+    if (row >= p.cu_q_lens[p.num_seqs]) return;
+    int lo = 0, hi = p.num_seqs;                  // cu[lo] <= row < cu[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.cu_q_lens[mid] <= row) lo = mid;
+        else hi = mid;
+    }
+    const int s = lo;
+    const int row0 = p.cu_q_lens[s], n = p.cu_q_lens[s + 1] - row0, L = p.context_lens[s];
+    if (n < 2 || L < n || L > p.max_blocks * BS) return;
+    const int tpt = BM / p.group;
+    const int i = row - row0, mt = i / tpt;
+    const int i1 = min(n, (mt + 1) * tpt);
+    const int KT = (L - n + i1 + BN - 1) / BN;
+    const int ns = (KT + p.tiles_per_split - 1) / p.tiles_per_split;
+    if (ns <= 1) return;
+    const size_t base = ((size_t)row * p.hq + h) * p.max_splits;
+    float M = -INFINITY;
+    for (int k = 0; k < ns; ++k) M = fmaxf(M, p.part_ml[(base + k) * 2]);
+    float Ls = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+        for (int k = 0; k < ns; ++k) {
+            const float f = ex2(p.part_ml[(base + k) * 2] - M);
+            Ls += f * p.part_ml[(base + k) * 2 + 1];
+            const float4 v = reinterpret_cast<const float4 *>(p.part_o + (base + k) * D)[lane];
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
+        }
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    reinterpret_cast<float4 *>(p.out + ((size_t)row * p.hq + h) * D)[lane] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
+constexpr int TILES_PER_SPLIT = 128;   // 16,384 keys per partition
+
+struct Plan {
+    size_t decode_bytes, part_o_off, part_ml_off, tile_off_off, total;
+    int max_splits, tiles_per_split;
+};
+
+}  // namespace
 
 namespace pkv_decode {
 kv_status run(float *out, const void *q, const void *k_cache, const void *v_cache,
@@ -13,7 +471,31 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
               int32_t num_blocks, float scale, kv_dtype dt, const float *k_scale, const float *v_scale,
               int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st);
 size_t workspace_bytes(int32_t num_seqs, int32_t hq, int32_t max_blocks, int32_t num_splits);
+bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int32_t hkv, kv_dtype dt,
+               CUtensorMap *km, CUtensorMap *vm);
 }  // namespace pkv_decode
+
+namespace {
+Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq, int32_t max_blocks,
+               int32_t num_splits)
+{
+    Plan pl{};
+    auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
+    pl.decode_bytes = up(pkv_decode::workspace_bytes(num_seqs, hq, max_blocks, num_splits));
+    pl.tiles_per_split = TILES_PER_SPLIT;
+    const int max_kv_tiles = (max_blocks * BS + BN - 1) / BN;
+    pl.max_splits = max_q_len >= 2 ? (max_kv_tiles + pl.tiles_per_split - 1) / pl.tiles_per_split : 0;
+    size_t off = pl.decode_bytes;
+    pl.part_o_off = off;
+    if (pl.max_splits > 1) off += up((size_t)total_q * hq * pl.max_splits * D * sizeof(float));
+    pl.part_ml_off = off;
+    if (pl.max_splits > 1) off += up((size_t)total_q * hq * pl.max_splits * 2 * sizeof(float));
+    pl.tile_off_off = off;
+    if (max_q_len >= 2) off += up((size_t)(num_seqs + 1) * sizeof(int32_t));
+    pl.total = off;
+    return pl;
+}
+}  // namespace
 
 namespace pkv_prefill {
 uint32_t take_status()
@@ -33,8 +515,10 @@ size_t paged_attention_chunked_prefill_workspace_size(int32_t num_seqs, int32_t 
                                                       int32_t max_blocks_per_seq,
                                                       int32_t num_splits)
 {
-    (void)total_q_tokens; (void)max_q_len; (void)num_kv_heads;
-    return pkv_decode::workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, num_splits);
+    (void)num_kv_heads;
+    if (num_seqs < 1 || total_q_tokens < 1 || max_q_len < 1 || num_q_heads < 1 || max_blocks_per_seq < 1)
+        return 0;
+    return make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, max_blocks_per_seq, num_splits).total;
 }
 
 kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32_t *cu_q_lens,
@@ -48,12 +532,74 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
                                           int32_t num_splits, void *workspace,
                                           size_t workspace_bytes, void *stream)
 {
-    if (!cu_q_lens || total_q_tokens < 0 || max_q_len < 1) return KV_ERR_INVALID;
-    if (max_q_len > 1) return KV_ERR_UNSUPPORTED;
-    return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                           cu_q_lens, total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
-                           k_scale, v_scale, num_splits, workspace, workspace_bytes,
-                           static_cast<cudaStream_t>(stream));
+    if (num_seqs == 0 || total_q_tokens == 0) return KV_OK;
+    if (num_seqs < 0 || total_q_tokens < 0 || max_q_len < 1 || !cu_q_lens || !context_lens || !out || !q ||
+        !k_cache || !v_cache || !block_tables || num_q_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 ||
+        num_blocks < 1 || num_q_heads % num_kv_heads)
+        return KV_ERR_INVALID;
+    const int G = num_q_heads / num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return KV_ERR_UNSUPPORTED;
+    if (dtype != KV_BF16 && dtype != KV_FP8_E4M3) return KV_ERR_UNSUPPORTED;
+    if (max_q_len >= 2 && dtype != KV_BF16) return KV_ERR_UNSUPPORTED;   // fp8 chunks: not in this build
+    if (!(scale > 0.f) || num_seqs > 65535 || num_kv_heads > 65535) return KV_ERR_INVALID;
+    if (!pkv_host::aligned(out, 16) || !pkv_host::aligned(q, 16)) return KV_ERR_INVALID;
+    const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, max_blocks_per_seq, num_splits);
+    if (pl.total && (!workspace || workspace_bytes < pl.total || !pkv_host::aligned(workspace, 256)))
+        return KV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    // decode rows (n = 1)
+    kv_status rs = pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                   cu_q_lens, total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks,
+                                   scale, dtype, k_scale, v_scale, num_splits, pl.decode_bytes ? ws : nullptr,
+                                   pl.decode_bytes, st);
+    if (rs != KV_OK || max_q_len < 2) return rs;
+    // prefill chunks (n >= 2)
+    PrefillParams p{};
+    p.out = out;
+    p.cu_q_lens = cu_q_lens;
+    p.context_lens = context_lens;
+    p.block_tables = block_tables;
+    p.tile_off = reinterpret_cast<int32_t *>(ws + pl.tile_off_off);
+    p.part_o = pl.max_splits > 1 ? reinterpret_cast<float *>(ws + pl.part_o_off) : nullptr;
+    p.part_ml = pl.max_splits > 1 ? reinterpret_cast<float *>(ws + pl.part_ml_off) : nullptr;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_seqs = num_seqs;
+    p.hq = num_q_heads;
+    p.hkv = num_kv_heads;
+    p.group = G;
+    p.num_blocks = num_blocks;
+    p.total_rows = total_q_tokens;
+    p.tiles_per_split = pl.tiles_per_split;
+    p.max_splits = std::max(1, pl.max_splits);
+    p.scale_log2 = scale * LOG2E;
+    CUtensorMap qm, km, vm;
+    const int tpt = BM / G;
+    if (!pkv_host::encode_tmap_3d(&qm, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, num_q_heads, total_q_tokens,
+                                  (uint64_t)D * 2, (uint64_t)num_q_heads * D * 2, 64, G, tpt,
+                                  CU_TENSOR_MAP_SWIZZLE_128B))
+        return KV_ERR_CUDA;
+    if (!pkv_decode::make_maps(k_cache, v_cache, num_blocks, num_kv_heads, dtype, &km, &vm)) return KV_ERR_CUDA;
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+            cudaSuccess)
+            return KV_ERR_CUDA;
+        configured = true;
+    }
+    tile_prefix_kernel<<<1, 1024, 0, st>>>(p);
+    // grid.x bounds the number of query tiles: sum over chunks of ceil(n/tpt)
+    const int64_t tiles_ub = (total_q_tokens + tpt - 1) / tpt + std::min<int64_t>(num_seqs, total_q_tokens / 2);
+    if (tiles_ub > INT32_MAX || p.max_splits > 65535) return KV_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)tiles_ub, num_kv_heads, p.max_splits);
+    prefill_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(qm, km, vm, p);
+    if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
+    if (p.max_splits > 1) {
+        const int64_t warps = (int64_t)total_q_tokens * num_q_heads;
+        prefill_reduce_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, st>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
+    }
+    return KV_OK;
 }
 
 }  // extern "C"

@@ -1,0 +1,91 @@
+"""GPU parity of the mixed chunked-prefill / decode call against the fp64 oracle
+(max-abs 1e-2 for the bf16 cache), bitwise permutation invariance, and the
+full-size mixed workload on sampled rows."""
+import numpy as np
+import pytest
+
+import paged_kv_cache_263_gb300 as pkv
+from oracle import model as omodel
+from paged_kv_cache_263_gb300.workload import DeviceWorkload
+from synth.workloads import make_workload, small_workload
+from tests.gpu_util import TOL, expected_full, max_abs, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    require_gpu()
+
+
+def _run(wl, poison=False):
+    dw = DeviceWorkload(wl, poison_cache=poison)
+    dw.step()
+    assert pkv.kv_last_device_status() == 0, pkv.kv_last_device_status_flags()
+    return dw, dw.out.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (16, 2), (32, 2)])
+def test_mixed_batch_small(hq, hkv):
+    lens = [1, 2, 20, 300, 64, 700, 129]
+    qlens = [1, 2, 17, 1, 64, 130, 129]          # a chunk equal to its whole context, too
+    wl = small_workload(700 + hq, lens=lens, q_lens=qlens, hq=hq, hkv=hkv)
+    _, _, ref = expected_full(wl)
+    _, got = _run(wl)
+    err = max_abs(got, ref)
+    assert err <= TOL["bf16"], err
+
+
+def test_chunk_spanning_several_partitions():
+    """A 40-row chunk over 40,000 keys: three 16,384-key partitions merged by LSE."""
+    wl = small_workload(800, lens=[40000, 33], q_lens=[40, 1], hq=16, hkv=2)
+    _, got = _run(wl)
+    cu = wl.cu_q_lens
+    for s in range(2):
+        ref = omodel.expected_rows(wl, s)
+        err = max_abs(got[cu[s]:cu[s + 1]], ref)
+        assert err <= TOL["bf16"], (s, err)
+
+
+def test_prefill_bitwise_identical_under_block_permutation():
+    outs = []
+    for perm_seed in (1, 2):
+        wl = small_workload(900, lens=[500, 37, 20000], q_lens=[130, 1, 77], hq=8, hkv=1)
+        wl.free_order = np.random.default_rng(perm_seed).permutation(wl.num_blocks).astype(np.int32)
+        outs.append(_run(wl)[1])
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_prefill_unwritten_slots_never_leak():
+    wl = small_workload(950, lens=[45, 200], q_lens=[45, 9], hq=8, hkv=2)
+    _, clean = _run(wl)
+    wl2 = small_workload(950, lens=[45, 200], q_lens=[45, 9], hq=8, hkv=2)
+    _, dirty = _run(wl2, poison=True)
+    assert np.isfinite(dirty).all()
+    assert np.array_equal(clean, dirty)
+
+
+def test_fp8_chunks_are_refused():
+    wl = small_workload(960, lens=[40, 40], q_lens=[4, 1], hq=8, hkv=2, kv_dtype="fp8")
+    dw = DeviceWorkload(wl)
+    with pytest.raises(pkv.KVError) as e:
+        dw.attention()
+    assert e.value.status == 3
+
+
+def test_mixed_prefill_workload_sampled():
+    wl = make_workload("mixed_prefill")
+    tb = omodel.build_tables(wl)
+    dw = DeviceWorkload(wl)
+    assert np.array_equal(dw.tables_host, tb.tables)
+    dw.step()
+    assert pkv.kv_last_device_status() == 0
+    out = dw.out.cpu().numpy()
+    cu = wl.cu_q_lens
+    rows = [0, 1, 15, 16, 17, 511, 1000, 1023]
+    ref = omodel.expected_rows(wl, 0, rows=rows)
+    err = max_abs(out[cu[0] + np.array(rows)], ref)
+    assert err <= TOL["bf16"], err
+    for s in (1, 100, 255):
+        err = max_abs(out[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s))
+        assert err <= TOL["bf16"], (s, err)
