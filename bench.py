@@ -122,14 +122,28 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
+def kernel_source_hash(path):
+    """sha256 of the device-code region of a kernel source file (between its
+    "device code begin" and "device code end" marker lines)."""
+    text = open(path).read()
+    a = text.index("// ---- device code begin")
+    b = text.index("// ---- device code end")
+    return hashlib.sha256(text[a:b].encode()).hexdigest()
+
+
 def _traffic(kernel_src):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
-    if that summary was taken on the current kernel source; else None."""
+    if that summary was taken on the current device code; else None."""
     try:
-        with open(os.path.join(ROOT, "profiles", "decode_llama8b_traffic.json")) as f:
-            d = json.load(f)
-        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-        return int(d["traffic_bytes_per_launch"]) if d.get("kernel_source_sha256") == sha else None
+        kv = {}
+        with open(os.path.join(ROOT, "profiles", "decode_llama8b_traffic.txt")) as f:
+            for ln in f:
+                if ":" in ln and not ln.startswith("#"):
+                    k, v = ln.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256") != kernel_source_hash(kernel_src):
+            return None
+        return int(kv["traffic_bytes_per_launch"])
     except Exception:
         return None
 
