@@ -199,6 +199,30 @@ PAGEDKV_API kv_status paged_attention_decode(float *out, const void *q, const vo
                                  const float *k_scale, const float *v_scale, int32_t num_splits,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
+/* Decode for callers that cannot allocate device memory.  The paper has no
+ * counterpart of this call; it is an addition of this library.  Some callers cannot call cudaMalloc
+ * where they run attention -- code inside an allocator or memory-pool hook of
+ * its own, a serving runtime that forbids allocation once it is up, or a host
+ * that links this library without any allocator -- so they cannot provide the
+ * workspace paged_attention_decode needs for split-KV partials.  This call is
+ * paged_attention_decode with that scratch held in one fixed-size device array
+ * inside the library (paged_attention_decode_static_scratch_bytes(): 32 MiB),
+ * which every GPU that loads the library keeps until the process exits.  The
+ * caller still passes every input and output.
+ *  - A call whose partials need more than that size returns KV_ERR_UNSUPPORTED
+ *    and launches nothing.  The call allocates no memory of any kind.
+ *  - All calls share the array: calls that overlap on the GPU (other streams,
+ *    other host threads on the same device) race on it and must be serialised.
+ *    It keeps the last call's contents; nothing in it has to start at zero.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture. */
+PAGEDKV_API size_t paged_attention_decode_static_scratch_bytes(void);
+PAGEDKV_API kv_status paged_attention_decode_static_scratch(
+    float *out, const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+    int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t num_blocks, float scale, kv_dtype dtype, const float *k_scale,
+    const float *v_scale, int32_t num_splits, void *stream);
+
 /* ------------------------------------------------------------------------
  * Paged attention over a mixed batch of chunked-prefill and decode queries
  * ([P1] "Serving systems": long prompts split into ~1K-token chunks interleaved

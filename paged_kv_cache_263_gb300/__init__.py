@@ -71,6 +71,9 @@ def lib():
             "paged_attention_chunked_prefill_workspace_size": (SZ, [I, I, I, I, I, I, I]),
             "paged_attention_chunked_prefill": (c.c_int, [P, P, P, P, I, I, I, P, P, P, I, I, I, I,
                                                           F, c.c_int, P, P, I, P, SZ, P]),
+            "paged_attention_decode_static_scratch_bytes": (SZ, []),
+            "paged_attention_decode_static_scratch": (c.c_int, [P, P, P, P, P, I, P, I, I, I, I, F, c.c_int, P,
+                                                                P, I, P]),
             "kv_last_device_status": (c.c_int, [P]),
             "kv_last_device_status_flags": (c.c_uint32, []),
         }
@@ -253,6 +256,31 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
                                         _cache_dtype(k_cache), _ptr(k_scale), _ptr(v_scale), int(num_splits),
                                         _ptr(workspace), ws_bytes, _stream(stream)), "paged_attention_decode")
     return out
+
+
+def paged_attention_decode_static_scratch(out, q, k_cache, v_cache, block_tables, context_lens, scale=None,
+                                          k_scale=None, v_scale=None, num_splits=0, stream=None):
+    """Decode for callers that cannot allocate device memory: same as
+    paged_attention_decode, but the split partials live in the library's own
+    fixed-size device array (see paged_attention_decode_static_scratch_bytes).
+    Calls that overlap on the GPU share that array and must be serialised."""
+    _need(out, "out", torch.float32)
+    _need(q, "q", torch.bfloat16)
+    _need(block_tables, "block_tables", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    B, hq, d = q.shape
+    nb, hkv = k_cache.shape[0], k_cache.shape[1]
+    if scale is None:
+        scale = HEAD_DIM ** -0.5
+    _check(lib().paged_attention_decode_static_scratch(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), B, hq, hkv, nb, float(scale), _cache_dtype(k_cache), _ptr(k_scale), _ptr(v_scale),
+        int(num_splits), _stream(stream)), "paged_attention_decode_static_scratch")
+    return out
+
+
+def paged_attention_decode_static_scratch_bytes() -> int:
+    return int(lib().paged_attention_decode_static_scratch_bytes())
 
 
 def paged_attention_chunked_prefill(out, q, cu_q_lens, context_lens, max_q_len, k_cache, v_cache,

@@ -36,6 +36,7 @@
 #include "common.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 // ---- device code begin (hashed with the ncu counters of profiles/)
 namespace {
@@ -640,6 +641,72 @@ kv_status paged_attention_decode(float *out, const void *q, const void *k_cache,
     return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            nullptr, num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                            k_scale, v_scale, num_splits, workspace, workspace_bytes,
+                           static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at the point where they run attention:
+// code running inside a memory pool or allocator hook of its own, a runtime
+// that forbids allocation once it has started serving, or a host that links
+// this library without any allocator.  For them the split-KV partials live in
+// one file-scope device array instead of a caller workspace.  Its size is
+// fixed (STATIC_SCRATCH_BYTES); every GPU that loads the library holds it until
+// the process exits.  Calls whose partials would not fit are refused with
+// KV_ERR_UNSUPPORTED.  All calls share the array, so calls that overlap on the
+// GPU (different streams, or different host threads on one device) race on it;
+// serialise them.  Nothing in it needs to start at zero: every partial that is
+// read was written earlier in the same call.  The first call on a device looks
+// up the array's device address (cudaGetSymbolAddress, with that device
+// current); make that first call before any stream capture.
+namespace {
+constexpr size_t STATIC_SCRATCH_BYTES = size_t(32) << 20;
+static __device__ __align__(256) uint8_t g_static_scratch[STATIC_SCRATCH_BYTES];
+constexpr int MAX_DEVICES = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[MAX_DEVICES] = {};
+
+kv_status static_scratch_address(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
+    if (dev < 0 || dev >= MAX_DEVICES) return KV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> g(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return KV_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return KV_OK;
+}
+}  // namespace
+
+extern "C" {
+
+size_t paged_attention_decode_static_scratch_bytes(void) { return STATIC_SCRATCH_BYTES; }
+
+kv_status paged_attention_decode_static_scratch(float *out, const void *q, const void *k_cache,
+                                                const void *v_cache, const int32_t *block_tables,
+                                                int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                                int32_t num_seqs, int32_t num_q_heads,
+                                                int32_t num_kv_heads, int32_t num_blocks, float scale,
+                                                kv_dtype dtype, const float *k_scale,
+                                                const float *v_scale, int32_t num_splits, void *stream)
+{
+    const size_t need = pkv_decode::workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, num_splits);
+    if (need > STATIC_SCRATCH_BYTES) return KV_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    if (need) {
+        kv_status st = static_scratch_address(&scratch);
+        if (st != KV_OK) return st;
+    }
+    return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                           nullptr, num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
+                           k_scale, v_scale, num_splits, scratch, need ? STATIC_SCRATCH_BYTES : 0,
                            static_cast<cudaStream_t>(stream));
 }
 
