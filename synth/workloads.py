@@ -214,6 +214,18 @@ def make_workload(name: str) -> Workload:
         return Workload("mixed_prefill", seed, 64, 8, pool, "bf16", lens, qlens,
                         rng.permutation(pool),
                         description="chunked-prefill mix: 1,024-token chunk over 100,000 cached tokens + 255 decodes")
+    if name == "mixed_prefill_small":
+        # the mixed batch scaled down for profiling: one 1,024-token chunk over
+        # 40,000 cached tokens plus 63 decodes (KV ~0.3 GB, still above L2)
+        seed = 2644
+        rng = np.random.Generator(np.random.PCG64(seed))
+        dec = rng.integers(1024, 8192, size=63, endpoint=True).astype(np.int32)
+        lens = np.concatenate([[41024], dec]).astype(np.int32)
+        qlens = np.concatenate([[1024], np.ones(63, np.int64)]).astype(np.int32)
+        pool = _pool_to_fit(lens, 0, -1)
+        return Workload("mixed_prefill_small", seed, 64, 8, pool, "bf16", lens, qlens,
+                        rng.permutation(pool),
+                        description="chunked-prefill mix for profiling: 1,024-token chunk over 40,000 cached tokens + 63 decodes")
     if name in ("split_fp8", "cfg5", "5"):
         seed = 2635
         rng = np.random.Generator(np.random.PCG64(seed))
