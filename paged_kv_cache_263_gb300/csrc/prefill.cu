@@ -13,20 +13,22 @@
 //  * A query tile packs 128/G chunk tokens x the G query heads of one KV head
 //    (row = token * G + head), so every K/V tile is shared by the whole GQA
 //    group.  Q (3-D TMA box) stays in shared memory for the CTA's life.
-//  * K/V tiles of 128 keys = 8 physical blocks, gathered through the block
+//  * K/V tiles of 64 keys = 4 physical blocks, gathered through the block
 //    table by 2-D TMA loads (128-byte swizzle), double-buffered.
-//  * S = Q K^T and O += P V run as tcgen05.mma (M=128, N=128, K=16 steps) issued
-//    by one thread, accumulators in tensor memory (S: 128 columns, O: 128).
-//    K is the K-major B operand of the first product; V is the MN-major B
-//    operand of the second, straight from the same swizzled tiles.
+//  * S[128x64] = Q K^T and O[128x128] += P V run as tcgen05.mma (K=16 steps)
+//    issued by one thread, accumulators in tensor memory (S: 64 columns,
+//    O: 128).  K is the K-major B operand of the first product; V is the
+//    MN-major B operand of the second, straight from the same swizzled tiles.
 //  * Four softmax warps own one TMEM lane (= one query row) per thread: they
 //    read S with tcgen05.ld, apply the causal mask on diagonal tiles, keep the
 //    online max / normaliser ("FlashAttention" section: running max and
 //    normaliser per block), write P in bf16 to shared memory in the operand
 //    layout, and rescale O in tensor memory only when the running max grew by
 //    more than 2^8 (otherwise the stale max is kept; exact in the end).
-//  * Long contexts are cut into partitions of whole 128-key tiles; partitions
-//    are merged by a fixed-order log-sum-exp kernel (no atomics).
+//  * 112 KiB of shared memory and 256 TMEM columns per CTA: two CTAs share an
+//    SM, so one CTA's softmax overlaps the other's tensor-core work.
+//  * Long contexts are cut into 16,384-key partitions of whole tiles, merged
+//    by a fixed-order log-sum-exp kernel (no atomics).
 #include "common.cuh"
 
 #include <algorithm>
@@ -37,18 +39,25 @@ __device__ uint32_t g_status;
 
 using namespace pkv;
 
-constexpr int BM = 128, BN = 128;
+constexpr int BM = 128, BN = 64;               // 128 query rows x 64 keys (4 blocks) per tile
 constexpr int THREADS = 192;                    // warps 0-3 softmax, 4 TMA producer, 5 MMA issuer
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
-constexpr uint32_t SQ = 0, SK0 = 32768, SV0 = 98304, SP = 163840, SBAR = 196608;
-constexpr int SMEM_BYTES = 196608 + 256 + 1024;
+// shared memory: Q 32 KiB | K 2 x 16 KiB | V 2 x 16 KiB | P 16 KiB | barriers.  114,944 bytes,
+// so two CTAs fit on one SM (227 KiB) and their MMA and softmax phases interleave
+constexpr uint32_t SQ = 0, SK0 = 32768, SV0 = 65536, SP = 98304, SBAR = 114688;
+constexpr uint32_t KV_STAGE = 16384, KV_HALF = 8192;
+constexpr int SMEM_BYTES = 114688 + 256;
 enum { B_Q = 0, B_KVF0 = 1, B_KVF1 = 2, B_KVE0 = 3, B_KVE1 = 4, B_S = 5, B_P = 6, B_PV = 7, B_DRAIN = 8, NBAR = 9 };
 
-// instruction descriptors, kind::f16: fp32 accumulate, bf16 A and B, M=128, N=128
-constexpr uint32_t IDESC_KMAJ = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                                ((uint32_t)(BM >> 4) << 24);
-constexpr uint32_t IDESC_BMN = IDESC_KMAJ | (1u << 16);   // B operand MN-major (V)
+// instruction descriptors, kind::f16: fp32 accumulate, bf16 A and B, M=128
+constexpr uint32_t idesc(int n, bool b_mn_major)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(BM >> 4) << 24);
+}
+constexpr uint32_t IDESC_S = idesc(BN, false);    // S[128 x 64] = Q K^T, K K-major
+constexpr uint32_t IDESC_PV = idesc(D, true);     // O[128 x 128] += P V, V MN-major
 
 struct PrefillParams {
     float *out;
@@ -133,13 +142,12 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     if (threadIdx.x == 0) p.tile_off[0] = 0;
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p)
 {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SBAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
@@ -172,6 +180,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int T = j1 - j0;
     const int nsplit = (KT + p.tiles_per_split - 1) / p.tiles_per_split;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (sbase & 1023u) {
+        // the 128-byte swizzle needs 1024-byte aligned tiles; never observed, but
+        // refuse rather than compute with a wrong layout
+        if (threadIdx.x == 0) flag(ST_TIMEOUT);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q), 1);
@@ -210,11 +224,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int st = jj & 1;
             if (jj >= 2 && !wait_w(bar(B_KVE0 + st), ((jj - 2) >> 1) & 1)) break;
             const int j = j0 + jj;
-            const int b = j * 8 + (lane & 7);
+            const int b = j * (BN / BS) + (lane & 3);
             int32_t id = -1;
-            if (lane < 8 && b < nblk) id = __ldg(bt + b);
-            const bool valid = lane < 8 && b < nblk && id >= 0 && id < p.num_blocks;
-            if (lane < 8 && b < nblk && !valid) flag(ST_BAD_BLOCK);
+            if (lane < BN / BS && b < nblk) id = __ldg(bt + b);
+            const bool valid = lane < BN / BS && b < nblk && id >= 0 && id < p.num_blocks;
+            if (lane < BN / BS && b < nblk && !valid) flag(ST_BAD_BLOCK);
             const unsigned vm = __ballot_sync(0xffffffffu, valid);
             if (lane == 0) {
                 fence_proxy_async_smem();
@@ -223,12 +237,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             if (valid) {
                 const int y = (id * p.hkv + g) * BS;
-                const uint32_t kd = sbase + SK0 + st * 32768 + lane * 2048;
-                const uint32_t vd = sbase + SV0 + st * 32768 + lane * 2048;
+                const uint32_t kd = sbase + SK0 + st * KV_STAGE + lane * 2048;
+                const uint32_t vd = sbase + SV0 + st * KV_STAGE + lane * 2048;
                 tma_load_2d(kd, &kmap, 0, y, bar(B_KVF0 + st));
-                tma_load_2d(kd + 16384, &kmap, 64, y, bar(B_KVF0 + st));
+                tma_load_2d(kd + KV_HALF, &kmap, 64, y, bar(B_KVF0 + st));
                 tma_load_2d(vd, &vmap, 0, y, bar(B_KVF0 + st));
-                tma_load_2d(vd + 16384, &vmap, 64, y, bar(B_KVF0 + st));
+                tma_load_2d(vd + KV_HALF, &vmap, 64, y, bar(B_KVF0 + st));
             }
             issued = jj + 1;
         }
@@ -245,11 +259,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int t0 = (j0 + jj) * BN;
             const int first = L - t0;            // first invalid row in the tile
             if (first >= BN) return;
-            const uint32_t vb = sbase + SV0 + (jj & 1) * 32768;
+            const uint32_t vb = sbase + SV0 + (jj & 1) * KV_STAGE;
             const int nchunks = (BN - first) * 2 * 8;   // rows x 2 halves x 8 chunks of 16 B
             for (int c = lane; c < nchunks; c += 32) {
                 const int r = first + (c >> 4), h = (c >> 3) & 1, ch = c & 7;
-                st_shared_v4(vb + h * 16384 + r * 128 + ch * 16, 0u, 0u, 0u, 0u);
+                st_shared_v4(vb + h * KV_HALF + r * 128 + ch * 16, 0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -257,12 +271,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         auto issue_s = [&](int jj) {
             if (lane == 0) {
                 tc_fence_after();
-                const uint32_t kb = sbase + SK0 + (jj & 1) * 32768;
+                const uint32_t kb = sbase + SK0 + (jj & 1) * KV_STAGE;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    umma_f16(tS, sdesc_sw128(sbase + SQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                             IDESC_KMAJ, kk > 0);
+                for (int kk = 0; kk < 8; ++kk) {   // D = 128 in steps of 16: 4 per 64-wide half
+                    const uint32_t qoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * KV_HALF + (kk & 3) * 32;
+                    umma_f16(tS, sdesc_sw128(sbase + SQ + qoff, 16, 1024), sdesc_sw128(kb + koff, 16, 1024),
+                             IDESC_S, kk > 0);
                 }
                 umma_commit(bar(B_S));
             }
@@ -276,12 +291,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!wait_w(bar(B_P), jj & 1)) break;
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint32_t vb = sbase + SV0 + (jj & 1) * 32768;
+                    const uint32_t vb = sbase + SV0 + (jj & 1) * KV_STAGE;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t poff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        umma_f16(tO, sdesc_sw128(sbase + SP + poff, 16, 1024),
-                                 sdesc_sw128(vb + kk * 2048, 16384, 1024), IDESC_BMN, (jj > 0 || kk > 0));
+                    for (int kk = 0; kk < BN / 16; ++kk) {   // 64 keys in steps of 16
+                        umma_f16(tO, sdesc_sw128(sbase + SP + kk * 32, 16, 1024),
+                                 sdesc_sw128(vb + kk * 2048, KV_HALF, 1024), IDESC_PV, (jj > 0 || kk > 0));
                     }
                     umma_commit(bar(B_PV));
                     umma_commit(bar(B_KVE0 + (jj & 1)));
@@ -316,9 +330,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int t0 = (j0 + jj) * BN;
             if (!wait_w(bar(B_S), jj & 1)) { ok = false; break; }
             tc_fence_after();
-            float sv[128];
+            float sv[BN];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < BN / 32; ++c) {
                 float tmp[32];
                 tmem_ld32(tS + lane_base + c * 32, tmp);
 #pragma unroll
@@ -327,7 +341,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool full = t0 + BN - 1 <= pos_min;
             float mx = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
+            for (int c = 0; c < BN; ++c) {
                 float v = sv[c] * p.scale_log2;
                 if (!full && t0 + c > pos) v = -INFINITY;
                 sv[c] = v;
@@ -353,11 +367,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_wait_st();
                 }
             }
-            // P in bf16, K-major 128-byte-swizzled operand layout: row r, keys 0..127
+            // P in bf16, K-major 128-byte-swizzled operand layout: row r, keys 0..63
             float sum = 0.f;
             const bool live = m_ref != -INFINITY;
 #pragma unroll
-            for (int c8 = 0; c8 < 16; ++c8) {
+            for (int c8 = 0; c8 < BN / 8; ++c8) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -366,8 +380,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     sum += p0 + p1;
                     w[e] = pack_bf16(p0, p1);
                 }
-                const int kh = c8 >> 3, cw = c8 & 7;
-                st_shared_v4(sbase + SP + kh * 16384 + r * 128 + ((cw ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+                st_shared_v4(sbase + SP + r * 128 + ((c8 ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
             }
             l = l * alpha + sum;
             fence_proxy_async_smem();
@@ -376,32 +389,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (ok && wait_w(bar(B_PV), (T - 1) & 1)) {
             tc_fence_after();
-            float o[128];
+            const size_t rh = (size_t)(row0 + (row_valid ? i : i0)) * p.hq + head;
+            const size_t pi = rh * p.max_splits + split;
+            const float inv = (nsplit == 1 && l > 0.f) ? 1.f / l : (nsplit == 1 ? 0.f : 1.f);
+            float4 *dst = reinterpret_cast<float4 *>(nsplit == 1 ? p.out + rh * D : p.part_o + pi * D);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float tmp[32];
-                tmem_ld32(tO + lane_base + c * 32, tmp);
+            for (int c = 0; c < 4; ++c) {       // 32 columns at a time (the load is warp-wide)
+                float o[32];
+                tmem_ld32(tO + lane_base + c * 32, o);
+                if (row_valid) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[c * 32 + e] = tmp[e];
-            }
-            if (row_valid) {
-                const size_t rh = (size_t)(row0 + i) * p.hq + head;
-                if (nsplit == 1) {
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
-                    float4 *dst = reinterpret_cast<float4 *>(p.out + rh * D);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        dst[c] = make_float4(o[4 * c] * inv, o[4 * c + 1] * inv, o[4 * c + 2] * inv,
-                                             o[4 * c + 3] * inv);
-                } else {
-                    const size_t pi = rh * p.max_splits + split;
-                    float4 *dst = reinterpret_cast<float4 *>(p.part_o + pi * D);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        dst[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-                    p.part_ml[pi * 2] = l > 0.f ? m_ref : -INFINITY;
-                    p.part_ml[pi * 2 + 1] = l;
+                    for (int e = 0; e < 8; ++e)
+                        dst[c * 8 + e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv,
+                                                     o[4 * e + 3] * inv);
                 }
+            }
+            if (row_valid && nsplit > 1) {
+                p.part_ml[pi * 2] = l > 0.f ? m_ref : -INFINITY;
+                p.part_ml[pi * 2 + 1] = l;
             }
         }
     }
@@ -455,7 +460,7 @@ __global__ void __launch_bounds__(128) prefill_reduce_kernel(const PrefillParams
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
-constexpr int TILES_PER_SPLIT = 128;   // 16,384 keys per partition
+constexpr int TILES_PER_SPLIT = 16384 / BN;   // 16,384 keys per partition
 
 struct Plan {
     size_t decode_bytes, part_o_off, part_ml_off, tile_off_off, total;
