@@ -33,6 +33,9 @@ __global__ void __launch_bounds__(256)
                              int64_t num_slots, const float *__restrict__ ks,
                              const float *__restrict__ vs)
 {
+    // the attention kernel that follows may begin scheduling at once; it waits
+    // for this grid to finish before it reads the cache
+    griddep_launch_dependents();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total_chunks;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int chunk = static_cast<int>(i & 15);

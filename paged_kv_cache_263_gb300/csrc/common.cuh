@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pagedkv.h"
 
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ != 1030)
@@ -339,3 +341,40 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 }  // namespace pkv
 #endif  // __CUDACC__
+
+#if defined(__CUDACC__)
+namespace pkv {
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel on the stream is still
+// running; it must wait here before reading anything an earlier kernel wrote.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// lets the next kernel on the stream (if launched with that attribute) start
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+}  // namespace pkv
+#endif
+
+#if defined(__CUDACC__)
+namespace pkv_host {
+// Launch with programmatic stream serialisation (the kernel calls
+// pkv::griddep_wait() before it reads what earlier kernels produced).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+}  // namespace pkv_host
+#endif

@@ -112,6 +112,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int split = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, cq = lane & 3;
+    // launched with programmatic serialisation: the CTA may be resident before
+    // the previous kernel on the stream (typically the cache write) finished
+    griddep_wait();
 
     int row = s;
     if (p.cu_q_lens) {
@@ -384,6 +387,8 @@ __global__ void __launch_bounds__(THREADS, 2)
             (void)mbar_wait_bounded(bar0 + 8 * (kk % GE::STAGES), (kk / GE::STAGES) & 1);
     }
 
+    // the LSE merge (next on the stream) may start scheduling now
+    griddep_launch_dependents();
     // ---------------- merge the warps' partial softmax states
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -455,6 +460,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 // Log-sum-exp merge of the split partitions: one warp per (sequence, q head).
 __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p)
 {
+    griddep_wait();   // the partials come from the decode kernel just before
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (wid >= p.num_seqs * p.hq) return;
@@ -506,8 +512,7 @@ cudaError_t launch_one(const CUtensorMap &km, const CUtensorMap &vm, const Decod
         configured = true;
     }
     dim3 grid(p.num_splits, p.hkv, p.num_seqs);
-    decode_kernel<FP8, NT><<<grid, THREADS, Geo<FP8>::SMEM, st>>>(km, vm, p);
-    return cudaGetLastError();
+    return pkv_host::launch_pdl(decode_kernel<FP8, NT>, grid, dim3(THREADS), Geo<FP8>::SMEM, st, km, vm, p);
 }
 
 }  // namespace
@@ -606,8 +611,8 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     if (e != cudaSuccess) return KV_ERR_CUDA;
     if (p.num_splits > 1) {
         const int warps = num_seqs * hq;
-        reduce_kernel<<<(warps + 3) / 4, 128, 0, st>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
+        if (pkv_host::launch_pdl(reduce_kernel, dim3((warps + 3) / 4), dim3(128), 0, st, p) != cudaSuccess)
+            return KV_ERR_CUDA;
     }
     return KV_OK;
 }
