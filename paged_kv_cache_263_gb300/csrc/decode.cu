@@ -16,8 +16,8 @@
 //  * Every (block, KV head) tile of K and of V is contiguous in HBM (4 KiB bf16,
 //    2 KiB fp8).  Each warp owns a private ring of stages; its lane 0 issues
 //    TMA tiled loads (128-byte swizzle) of the K and V tile of a future block
-//    into a stage, completion counted on the stage's mbarrier.  ~48 KiB of
-//    loads per SM stay in flight, which HBM3e needs at this tile size.
+//    into a stage, completion counted on the stage's mbarrier.  Three CTAs per
+//    SM keep ~190 KiB of loads in flight, which HBM3e needs at this tile size.
 //  * Scores: S^T[16 tokens][8 heads] = K[16][128] . Q^T[128][8] on the tensor
 //    cores (mma.sync m16n8k16, tokens on M, the GQA group on N) -- G = 8 fills
 //    the tile exactly.  K comes from shared memory with ldmatrix (conflict-free
@@ -71,11 +71,25 @@ struct DecodeParams {
     float scale_log2;          // softmax scale * log2(e)
 };
 
+// Ring depth per warp and CTAs per SM (compile-time).  Measured on GB300:
+// 2 bf16 stages (4 fp8) of 8 KiB per warp with 3 CTAs per SM beat deeper
+// rings with fewer CTAs on every decode workload -- more CTAs hide each
+// CTA's ramp-up, and 3 x 4 warps x 16 KiB still keeps ~190 KiB in flight.
+#ifndef PKV_DECODE_STAGES_BF16
+#define PKV_DECODE_STAGES_BF16 2
+#endif
+#ifndef PKV_DECODE_STAGES_FP8
+#define PKV_DECODE_STAGES_FP8 4
+#endif
+#ifndef PKV_DECODE_MIN_CTAS
+#define PKV_DECODE_MIN_CTAS 3
+#endif
+
 template <bool FP8>
 struct Geo {
     static constexpr int TILE = FP8 ? 2048 : 4096;       // bytes of one K or V tile
     static constexpr int STAGE = 2 * TILE;               // K + V
-    static constexpr int STAGES = FP8 ? 6 : 3;           // 24 KiB ring per warp
+    static constexpr int STAGES = FP8 ? PKV_DECODE_STAGES_FP8 : PKV_DECODE_STAGES_BF16;
     static constexpr int RING = STAGES * STAGE;
     static constexpr int SMEM = WARPS * RING + 1024 + 256;
 };
@@ -99,7 +113,7 @@ __device__ __forceinline__ void issue_stage(uint32_t dst, uint32_t bar, const CU
 }
 
 template <bool FP8, int NT>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p)
 {
@@ -520,10 +534,15 @@ cudaError_t launch_one(const CUtensorMap &km, const CUtensorMap &vm, const Decod
 // ---------------------------------------------------------------- host side
 namespace pkv_decode {
 
-// Chooses the partition length (blocks) and the number of partitions.
+// Chooses the partition length (blocks) and the number of partitions.  Auto
+// mode lengthens partitions with the longest context (64 blocks up to 8K
+// tokens, 128 up to 64K, 256 beyond): measured on GB300 this keeps enough
+// CTAs for the short batches while long ones pay less per-CTA ramp-up and
+// partial-merge traffic.
 void plan_splits(int32_t max_blocks, int32_t num_splits, int32_t *part_blocks, int32_t *splits)
 {
-    int32_t s = num_splits > 0 ? num_splits : (max_blocks + 63) / 64;
+    const int32_t auto_part = max_blocks <= 512 ? 64 : (max_blocks <= 4096 ? 128 : 256);
+    int32_t s = num_splits > 0 ? num_splits : (max_blocks + auto_part - 1) / auto_part;
     s = std::max(1, std::min(s, max_blocks));
     int32_t pb = (max_blocks + s - 1) / s;
     *part_blocks = pb;
