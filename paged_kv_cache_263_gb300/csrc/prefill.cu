@@ -9,24 +9,27 @@
 // prefill vs decode (a) prefill is a dense O(N^2) contraction, (e) chunked
 // prefill.  Rows with n = 1 are decode rows and go to the decode kernel.
 //
-// Tensor-core kernel, one CTA per (128-row query tile, KV head, KV partition):
+// Tensor-core kernel, one CTA per (pair of 128-row query tiles, KV head, KV
+// partition):
 //  * A query tile packs 128/G chunk tokens x the G query heads of one KV head
 //    (row = token * G + head), so every K/V tile is shared by the whole GQA
-//    group.  Q (3-D TMA box) stays in shared memory for the CTA's life.
+//    group; the two tiles of a pair share every K/V tile as well.  Q (3-D TMA
+//    boxes) stays in shared memory for the CTA's life.
 //  * K/V tiles of 64 keys = 4 physical blocks, gathered through the block
-//    table by 2-D TMA loads (128-byte swizzle), double-buffered.
+//    table by 2-D TMA loads (128-byte swizzle) into a 3-stage ring.
 //  * S[128x64] = Q K^T and O[128x128] += P V run as tcgen05.mma (K=16 steps)
-//    issued by one thread, accumulators in tensor memory (S: 64 columns,
-//    O: 128).  K is the K-major B operand of the first product; V is the
-//    MN-major B operand of the second, straight from the same swizzled tiles.
-//  * Four softmax warps own one TMEM lane (= one query row) per thread: they
-//    read S with tcgen05.ld, apply the causal mask on diagonal tiles, keep the
-//    online max / normaliser ("FlashAttention" section: running max and
-//    normaliser per block), write P in bf16 to shared memory in the operand
-//    layout, and rescale O in tensor memory only when the running max grew by
-//    more than 2^8 (otherwise the stale max is kept; exact in the end).
-//  * 112 KiB of shared memory and 256 TMEM columns per CTA: two CTAs share an
-//    SM, so one CTA's softmax overlaps the other's tensor-core work.
+//    issued by one thread, accumulators in tensor memory (per tile: S 64
+//    columns, O 128).  K is the K-major B operand of the first product; V is
+//    the MN-major B operand of the second, straight from the same tiles.
+//  * Two softmax warpgroups, one per query tile, own one TMEM lane (= one query
+//    row) per thread.  They read S with tcgen05.ld, apply the causal mask on
+//    diagonal tiles, keep the online max / normaliser ("FlashAttention"
+//    section: running max and normaliser per block), compute P before waiting
+//    for the previous PV product, write P in bf16 to shared memory in the
+//    operand layout, and rescale O in tensor memory only when the running max
+//    grew by more than 2^8 (otherwise the stale max is kept; exact in the end).
+//    The MMA thread alternates between the two tiles, so one group's softmax
+//    overlaps the other group's tensor-core work.
 //  * Long contexts are cut into 16,384-key partitions of whole tiles, merged
 //    by a fixed-order log-sum-exp kernel (no atomics).
 #include "common.cuh"
@@ -40,15 +43,30 @@ __device__ uint32_t g_status;
 using namespace pkv;
 
 constexpr int BM = 128, BN = 64;               // 128 query rows x 64 keys (4 blocks) per tile
-constexpr int THREADS = 192;                    // warps 0-3 softmax, 4 TMA producer, 5 MMA issuer
+// warps 0-3 softmax of query tile 0, 4-7 softmax of query tile 1, 8 TMA producer,
+// 9 MMA issuer
+constexpr int THREADS = 320;
+constexpr int KV_STAGES = 4;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
-// shared memory: Q 32 KiB | K 2 x 16 KiB | V 2 x 16 KiB | P 16 KiB | barriers.  114,944 bytes,
-// so two CTAs fit on one SM (227 KiB) and their MMA and softmax phases interleave
-constexpr uint32_t SQ = 0, SK0 = 32768, SV0 = 65536, SP = 98304, SBAR = 114688;
-constexpr uint32_t KV_STAGE = 16384, KV_HALF = 8192;
-constexpr int SMEM_BYTES = 114688 + 256;
-enum { B_Q = 0, B_KVF0 = 1, B_KVF1 = 2, B_KVE0 = 3, B_KVE1 = 4, B_S = 5, B_P = 6, B_PV = 7, B_DRAIN = 8, NBAR = 9 };
+// shared memory: Q 2 x 32 KiB | 4 stages of (K 16 KiB, V 16 KiB) | P 2 x 16 KiB | barriers
+constexpr uint32_t SQ = 0, Q_TILE = 32768;
+constexpr uint32_t SKV = 65536, KV_STAGE_BYTES = 32768, V_OFF = 16384, KV_HALF = 8192;
+constexpr uint32_t SP = SKV + KV_STAGES * KV_STAGE_BYTES, P_TILE = 16384;
+constexpr uint32_t SBAR = SP + 2 * P_TILE;
+constexpr int SMEM_BYTES = SBAR + 256;
+// barriers
+enum {
+    B_Q = 0,
+    B_KVF = 1,                      // + stage: K and V of a tile landed
+    B_KVE = B_KVF + KV_STAGES,      // + stage: every MMA reading the stage is done
+    B_S = B_KVE + KV_STAGES,        // + 2*group + buffer: an S tile of the group is in TMEM
+    B_P = B_S + 4,                  // + group: the group's P is in shared memory (128 arrivals)
+    B_PV = B_P + 2,                 // + group: the group's PV product finished
+    B_DRAIN = B_PV + 2,
+    NBAR
+};
+static_assert(NBAR * 8 + 8 <= 256, "barrier area");
 
 // instruction descriptors, kind::f16: fp32 accumulate, bf16 A and B, M=128
 constexpr uint32_t idesc(int n, bool b_mn_major)
@@ -64,7 +82,7 @@ struct PrefillParams {
     const int32_t *cu_q_lens;
     const int32_t *context_lens;
     const int32_t *block_tables;
-    int32_t *tile_off;   // [num_seqs + 1] query tiles per sequence, prefix sums
+    int32_t *tile_off;   // [num_seqs + 1] pairs of query tiles per sequence, prefix sums
     float *part_o;       // [rows][Hq][max_splits][128]
     float *part_ml;      // [rows][Hq][max_splits][2]
     int max_blocks, num_seqs, hq, hkv, group, num_blocks, total_rows;
@@ -108,7 +126,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
             const int n = b - a, L = p.context_lens[s];
             if (n >= 2) {
                 if (a < 0 || b > p.total_rows || L < n || L > p.max_blocks * BS) flag(ST_BAD_LEN);
-                else tiles = (n + tpt - 1) / tpt;
+                else tiles = ((n + tpt - 1) / tpt + 1) / 2;    // pairs of 128-row query tiles
             } else if (n < 0) {
                 flag(ST_BAD_LEN);
             }
@@ -142,7 +160,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     if (threadIdx.x == 0) p.tile_off[0] = 0;
 }
 
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p)
 {
@@ -159,7 +177,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         return __all_sync(0xffffffffu, wait_bar(b, parity, abort_flag));
     };
 
-    // ---- which query tile / KV head / partition
+    // ---- which pair of query tiles / KV head / partition
     const int x = blockIdx.x, g = blockIdx.y, split = blockIdx.z;
     if (x >= p.tile_off[p.num_seqs]) return;
     int lo = 0, hi = p.num_seqs;                 // tile_off[lo] <= x < tile_off[hi]
@@ -168,11 +186,13 @@ __global__ void __launch_bounds__(THREADS, 2)
         if (p.tile_off[mid] <= x) lo = mid;
         else hi = mid;
     }
-    const int s = lo, mt = x - p.tile_off[s];
+    const int s = lo, pair = x - p.tile_off[s];
     const int row0 = p.cu_q_lens[s], n = p.cu_q_lens[s + 1] - row0, L = p.context_lens[s];
     const int G = p.group, tpt = BM / G;
-    const int i0 = mt * tpt, i1 = min(n, i0 + tpt);
-    const int kmax = L - n + i1;                 // keys visible to the tile's last row
+    const int tiles = (n + tpt - 1) / tpt;
+    const bool has1 = 2 * pair + 1 < tiles;      // the pair's second query tile exists
+    const int last = has1 ? 2 * pair + 1 : 2 * pair;
+    const int kmax = L - n + min(n, (last + 1) * tpt);   // keys visible to the pair's last row
     const int KT = (kmax + BN - 1) / BN;
     const int j0 = split * p.tiles_per_split;
     if (j0 >= KT) return;
@@ -189,40 +209,48 @@ __global__ void __launch_bounds__(THREADS, 2)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q), 1);
-        mbar_init(bar(B_KVF0), 1);
-        mbar_init(bar(B_KVF1), 1);
-        mbar_init(bar(B_KVE0), 1);
-        mbar_init(bar(B_KVE1), 1);
-        mbar_init(bar(B_S), 1);
-        mbar_init(bar(B_P), 128);
-        mbar_init(bar(B_PV), 1);
+        for (int i = 0; i < KV_STAGES; ++i) {
+            mbar_init(bar(B_KVF + i), 1);
+            mbar_init(bar(B_KVE + i), 1);
+        }
+        for (int i = 0; i < 4; ++i) mbar_init(bar(B_S + i), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_P + i), 128);
+            mbar_init(bar(B_PV + i), 1);
+        }
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + 128;
+    // TMEM columns: S double-buffered per group, 64 each (group gi, buffer b at
+    // (2 gi + b) * 64); O of group gi at 256 + 128 gi
+    auto tS = [&](int gi, int b) -> uint32_t { return tmem + (2 * gi + b) * BN; };
+    auto tO = [&](int gi) -> uint32_t { return tmem + 256 + gi * D; };
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ======================= TMA producer
         const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks;
         const int nblk = (L + BS - 1) / BS;
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar(B_Q), 2 * 16384);
-            tma_load_3d(sbase + SQ, &qmap, 0, g * G, row0 + i0, bar(B_Q));
-            tma_load_3d(sbase + SQ + 16384, &qmap, 64, g * G, row0 + i0, bar(B_Q));
+            mbar_arrive_expect_tx(bar(B_Q), (has1 ? 4 : 2) * 16384);
+            for (int gi = 0; gi < (has1 ? 2 : 1); ++gi) {
+                const int zq = row0 + (2 * pair + gi) * tpt;
+                tma_load_3d(sbase + SQ + gi * Q_TILE, &qmap, 0, g * G, zq, bar(B_Q));
+                tma_load_3d(sbase + SQ + gi * Q_TILE + 16384, &qmap, 64, g * G, zq, bar(B_Q));
+            }
         }
         int issued = 0;
         for (int jj = 0; jj < T; ++jj) {
-            const int st = jj & 1;
-            if (jj >= 2 && !wait_w(bar(B_KVE0 + st), ((jj - 2) >> 1) & 1)) break;
+            const int st = jj % KV_STAGES;
+            if (jj >= KV_STAGES && !wait_w(bar(B_KVE + st), ((jj - KV_STAGES) / KV_STAGES) & 1)) break;
             const int j = j0 + jj;
             const int b = j * (BN / BS) + (lane & 3);
             int32_t id = -1;
@@ -232,26 +260,26 @@ __global__ void __launch_bounds__(THREADS, 2)
             const unsigned vm = __ballot_sync(0xffffffffu, valid);
             if (lane == 0) {
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar(B_KVF0 + st), __popc(vm) * 4 * 2048);
+                mbar_arrive_expect_tx(bar(B_KVF + st), __popc(vm) * 4 * 2048);
             }
             __syncwarp();
             if (valid) {
                 const int y = (id * p.hkv + g) * BS;
-                const uint32_t kd = sbase + SK0 + st * KV_STAGE + lane * 2048;
-                const uint32_t vd = sbase + SV0 + st * KV_STAGE + lane * 2048;
-                tma_load_2d(kd, &kmap, 0, y, bar(B_KVF0 + st));
-                tma_load_2d(kd + KV_HALF, &kmap, 64, y, bar(B_KVF0 + st));
-                tma_load_2d(vd, &vmap, 0, y, bar(B_KVF0 + st));
-                tma_load_2d(vd + KV_HALF, &vmap, 64, y, bar(B_KVF0 + st));
+                const uint32_t kd = sbase + SKV + st * KV_STAGE_BYTES + lane * 2048;
+                const uint32_t vd = kd + V_OFF;
+                tma_load_2d(kd, &kmap, 0, y, bar(B_KVF + st));
+                tma_load_2d(kd + KV_HALF, &kmap, 64, y, bar(B_KVF + st));
+                tma_load_2d(vd, &vmap, 0, y, bar(B_KVF + st));
+                tma_load_2d(vd + KV_HALF, &vmap, 64, y, bar(B_KVF + st));
             }
             issued = jj + 1;
         }
         if (*abort_flag) {
             // let loads already in flight land before the CTA exits
-            for (int jj = max(0, issued - 2); jj < issued; ++jj)
-                (void)mbar_wait_bounded(bar(B_KVF0 + (jj & 1)), (jj >> 1) & 1);
+            for (int jj = max(0, issued - KV_STAGES); jj < issued; ++jj)
+                (void)mbar_wait_bounded(bar(B_KVF + jj % KV_STAGES), (jj / KV_STAGES) & 1);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ======================= MMA issuer (+ zeroing of V rows past the context)
         auto fix_tail = [&](int jj) {
             // keys >= L of the tile: their V rows may hold anything (never written,
@@ -259,7 +287,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             const int t0 = (j0 + jj) * BN;
             const int first = L - t0;            // first invalid row in the tile
             if (first >= BN) return;
-            const uint32_t vb = sbase + SV0 + (jj & 1) * KV_STAGE;
+            const uint32_t vb = sbase + SKV + (jj % KV_STAGES) * KV_STAGE_BYTES + V_OFF;
             const int nchunks = (BN - first) * 2 * 8;   // rows x 2 halves x 8 chunks of 16 B
             for (int c = lane; c < nchunks; c += 32) {
                 const int r = first + (c >> 4), h = (c >> 3) & 1, ch = c & 7;
@@ -268,44 +296,60 @@ __global__ void __launch_bounds__(THREADS, 2)
             fence_proxy_async_smem();
             __syncwarp();
         };
-        auto issue_s = [&](int jj) {
+        // S[gi] = Q[gi] K^T for KV tile jj
+        auto issue_s = [&](int gi, int jj) {
             if (lane == 0) {
                 tc_fence_after();
-                const uint32_t kb = sbase + SK0 + (jj & 1) * KV_STAGE;
+                const uint32_t kb = sbase + SKV + (jj % KV_STAGES) * KV_STAGE_BYTES;
+                const uint32_t qb = sbase + SQ + gi * Q_TILE;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {   // D = 128 in steps of 16: 4 per 64-wide half
                     const uint32_t qoff = (kk >> 2) * 16384 + (kk & 3) * 32;
                     const uint32_t koff = (kk >> 2) * KV_HALF + (kk & 3) * 32;
-                    umma_f16(tS, sdesc_sw128(sbase + SQ + qoff, 16, 1024), sdesc_sw128(kb + koff, 16, 1024),
-                             IDESC_S, kk > 0);
+                    umma_f16(tS(gi, jj & 1), sdesc_sw128(qb + qoff, 16, 1024),
+                             sdesc_sw128(kb + koff, 16, 1024), IDESC_S, kk > 0);
                 }
-                umma_commit(bar(B_S));
+                umma_commit(bar(B_S + 2 * gi + (jj & 1)));
             }
             __syncwarp();
         };
-        bool ok = wait_w(bar(B_Q), 0) && wait_w(bar(B_KVF0), 0);
-        if (ok) {
-            fix_tail(0);
-            issue_s(0);
-            for (int jj = 0; jj < T; ++jj) {
-                if (!wait_w(bar(B_P), jj & 1)) break;
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint32_t vb = sbase + SV0 + (jj & 1) * KV_STAGE;
+        // O[gi] += P[gi] V for KV tile jj
+        auto issue_pv = [&](int gi, int jj) {
+            if (lane == 0) {
+                tc_fence_after();
+                const uint32_t vb = sbase + SKV + (jj % KV_STAGES) * KV_STAGE_BYTES + V_OFF;
+                const uint32_t pb = sbase + SP + gi * P_TILE;
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {   // 64 keys in steps of 16
-                        umma_f16(tO, sdesc_sw128(sbase + SP + kk * 32, 16, 1024),
-                                 sdesc_sw128(vb + kk * 2048, KV_HALF, 1024), IDESC_PV, (jj > 0 || kk > 0));
-                    }
-                    umma_commit(bar(B_PV));
-                    umma_commit(bar(B_KVE0 + (jj & 1)));
-                }
-                __syncwarp();
-                if (jj + 1 < T) {
-                    if (!wait_w(bar(B_KVF0 + ((jj + 1) & 1)), ((jj + 1) >> 1) & 1)) break;
-                    fix_tail(jj + 1);
-                    issue_s(jj + 1);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)   // 64 keys in steps of 16
+                    umma_f16(tO(gi), sdesc_sw128(pb + kk * 32, 16, 1024),
+                             sdesc_sw128(vb + kk * 2048, KV_HALF, 1024), IDESC_PV, (jj > 0 || kk > 0));
+                umma_commit(bar(B_PV + gi));
+            }
+            __syncwarp();
+        };
+        const int ng = has1 ? 2 : 1;
+        // S of the first two tiles up front; afterwards S(jj+2) is issued as soon as
+        // PV(jj) is, so every softmax finds its S ready
+        bool ok = wait_w(bar(B_Q), 0);
+        for (int jj = 0; ok && jj < min(2, T); ++jj) {
+            if (!wait_w(bar(B_KVF + jj), 0)) { ok = false; break; }
+            fix_tail(jj);
+            for (int gi = 0; gi < ng; ++gi) issue_s(gi, jj);
+        }
+        for (int jj = 0; jj < T && ok; ++jj) {
+            for (int gi = 0; gi < ng; ++gi) {
+                if (!wait_w(bar(B_P + gi), jj & 1)) { ok = false; break; }
+                issue_pv(gi, jj);
+            }
+            if (!ok) break;
+            // the stage of tile jj is free once every MMA issued so far is done
+            if (lane == 0) umma_commit(bar(B_KVE + jj % KV_STAGES));
+            __syncwarp();
+            if (jj + 2 < T) {
+                const int sn = (jj + 2) % KV_STAGES;
+                if (!wait_w(bar(B_KVF + sn), ((jj + 2) / KV_STAGES) & 1)) { ok = false; break; }
+                fix_tail(jj + 2);
+                for (int gi = 0; gi < ng; ++gi) issue_s(gi, jj + 2);
             }
         }
         // every MMA this thread issued has finished before TMEM is released
@@ -313,107 +357,114 @@ __global__ void __launch_bounds__(THREADS, 2)
         __syncwarp();
         (void)mbar_wait_bounded(bar(B_DRAIN), 0);
     } else {
-        // ======================= softmax warps: thread = query row = TMEM lane
-        const int r = threadIdx.x;                 // 0..127
-        const int i = i0 + r / G;
-        const int head = g * G + r % G;
-        const bool row_valid = i < i1;
-        // last key this row may attend; rows past the chunk (loaded only to fill the
-        // tile, never stored) take the tile's last valid row, so no row ever sees
-        // a key at or beyond L
-        const int pos = row_valid ? L - n + i : L - n + i1 - 1;
-        const int pos_min = L - n + i0;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        float m_ref = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int jj = 0; jj < T && ok; ++jj) {
-            const int t0 = (j0 + jj) * BN;
-            if (!wait_w(bar(B_S), jj & 1)) { ok = false; break; }
-            tc_fence_after();
-            float sv[BN];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                float tmp[32];
-                tmem_ld32(tS + lane_base + c * 32, tmp);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) sv[c * 32 + e] = tmp[e];
-            }
-            const bool full = t0 + BN - 1 <= pos_min;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-                float v = sv[c] * p.scale_log2;
-                if (!full && t0 + c > pos) v = -INFINITY;
-                sv[c] = v;
-                mx = fmaxf(mx, v);
-            }
-            float alpha = 1.f;
-            if (mx > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mx != -INFINITY)) {
-                alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx);
-                m_ref = mx;
-            }
-            if (jj > 0) {
-                if (!wait_w(bar(B_PV), (jj - 1) & 1)) { ok = false; break; }
+        // ======================= softmax warpgroups: thread = query row = TMEM lane
+        const int gi = warp >> 2;                  // which query tile of the pair
+        if (gi == 0 || has1) {
+            const int r = threadIdx.x - gi * 128;  // row of the tile, 0..127
+            const int i0 = (2 * pair + gi) * tpt, i1 = min(n, i0 + tpt);
+            const int i = i0 + r / G;
+            const int head = g * G + r % G;
+            const bool row_valid = i < i1;
+            // last key this row may attend; rows past the chunk (loaded only to fill
+            // the tile, never stored) take the tile's last valid row, so no row ever
+            // sees a key at or beyond L
+            const int pos = row_valid ? L - n + i : L - n + i1 - 1;
+            const int pos_min = L - n + i0;
+            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+            const uint32_t pbase = sbase + SP + gi * P_TILE;
+            float m_ref = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int jj = 0; jj < T && ok; ++jj) {
+                const int t0 = (j0 + jj) * BN;
+                if (!wait_w(bar(B_S + 2 * gi + (jj & 1)), (jj >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                float sv[BN];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        float o[32];
-                        tmem_ld32(tO + lane_base + c * 32, o);
+                for (int c = 0; c < BN / 32; ++c) {
+                    float tmp[32];
+                    tmem_ld32(tS(gi, jj & 1) + lane_base + c * 32, tmp);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tmem_st32(tO + lane_base + c * 32, o);
-                    }
-                    tmem_wait_st();
+                    for (int e = 0; e < 32; ++e) sv[c * 32 + e] = tmp[e];
                 }
-            }
-            // P in bf16, K-major 128-byte-swizzled operand layout: row r, keys 0..63
-            float sum = 0.f;
-            const bool live = m_ref != -INFINITY;
+                const bool full = t0 + BN - 1 <= pos_min;
+                float mx = -INFINITY;
 #pragma unroll
-            for (int c8 = 0; c8 < BN / 8; ++c8) {
-                uint32_t w[4];
+                for (int c = 0; c < BN; ++c) {
+                    float v = sv[c] * p.scale_log2;
+                    if (!full && t0 + c > pos) v = -INFINITY;
+                    sv[c] = v;
+                    mx = fmaxf(mx, v);
+                }
+                float alpha = 1.f;
+                if (mx > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mx != -INFINITY)) {
+                    alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx);
+                    m_ref = mx;
+                }
+                // exponentials first: this overlaps the previous PV product
+                float sum = 0.f;
+                const bool live = m_ref != -INFINITY;
+                uint32_t pw[BN / 2];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = live ? ex2(sv[c8 * 8 + 2 * e] - m_ref) : 0.f;
-                    const float p1 = live ? ex2(sv[c8 * 8 + 2 * e + 1] - m_ref) : 0.f;
+                for (int e = 0; e < BN / 2; ++e) {
+                    const float p0 = live ? ex2(sv[2 * e] - m_ref) : 0.f;
+                    const float p1 = live ? ex2(sv[2 * e + 1] - m_ref) : 0.f;
                     sum += p0 + p1;
-                    w[e] = pack_bf16(p0, p1);
+                    pw[e] = pack_bf16(p0, p1);
                 }
-                st_shared_v4(sbase + SP + r * 128 + ((c8 ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
-            }
-            l = l * alpha + sum;
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(B_P));
-        }
-        if (ok && wait_w(bar(B_PV), (T - 1) & 1)) {
-            tc_fence_after();
-            const size_t rh = (size_t)(row0 + (row_valid ? i : i0)) * p.hq + head;
-            const size_t pi = rh * p.max_splits + split;
-            const float inv = (nsplit == 1 && l > 0.f) ? 1.f / l : (nsplit == 1 ? 0.f : 1.f);
-            float4 *dst = reinterpret_cast<float4 *>(nsplit == 1 ? p.out + rh * D : p.part_o + pi * D);
+                l = l * alpha + sum;
+                if (jj > 0) {
+                    // the previous PV has read P and written O: both may change now
+                    if (!wait_w(bar(B_PV + gi), (jj - 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {       // 32 columns at a time (the load is warp-wide)
-                float o[32];
-                tmem_ld32(tO + lane_base + c * 32, o);
-                if (row_valid) {
+                        for (int c = 0; c < 4; ++c) {
+                            float o[32];
+                            tmem_ld32(tO(gi) + lane_base + c * 32, o);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[c * 8 + e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv,
-                                                     o[4 * e + 3] * inv);
+                            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                            tmem_st32(tO(gi) + lane_base + c * 32, o);
+                        }
+                        tmem_wait_st();
+                    }
                 }
+                // P in bf16, K-major 128-byte-swizzled operand layout: row r, keys 0..63
+#pragma unroll
+                for (int c8 = 0; c8 < BN / 8; ++c8)
+                    st_shared_v4(pbase + r * 128 + ((c8 ^ (r & 7)) << 4), pw[4 * c8], pw[4 * c8 + 1],
+                                 pw[4 * c8 + 2], pw[4 * c8 + 3]);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(B_P + gi));
             }
-            if (row_valid && nsplit > 1) {
-                p.part_ml[pi * 2] = l > 0.f ? m_ref : -INFINITY;
-                p.part_ml[pi * 2 + 1] = l;
+            if (ok && wait_w(bar(B_PV + gi), (T - 1) & 1)) {
+                tc_fence_after();
+                const size_t rh = (size_t)(row0 + (row_valid ? i : i0)) * p.hq + head;
+                const size_t pi = rh * p.max_splits + split;
+                const float inv = (nsplit == 1 && l > 0.f) ? 1.f / l : (nsplit == 1 ? 0.f : 1.f);
+                float4 *dst = reinterpret_cast<float4 *>(nsplit == 1 ? p.out + rh * D : p.part_o + pi * D);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {       // 32 columns at a time (the load is warp-wide)
+                    float o[32];
+                    tmem_ld32(tO(gi) + lane_base + c * 32, o);
+                    if (row_valid) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[c * 8 + e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv,
+                                                         o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+                    }
+                }
+                if (row_valid && nsplit > 1) {
+                    p.part_ml[pi * 2] = l > 0.f ? m_ref : -INFINITY;
+                    p.part_ml[pi * 2 + 1] = l;
+                }
             }
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // Log-sum-exp merge of prefill partitions: one warp per (query row, head).
@@ -435,7 +486,10 @@ __global__ void __launch_bounds__(128) prefill_reduce_kernel(const PrefillParams
     if (n < 2 || L < n || L > p.max_blocks * BS) return;
     const int tpt = BM / p.group;
     const int i = row - row0, mt = i / tpt;
-    const int i1 = min(n, (mt + 1) * tpt);
+    // the CTA that computed this row covered the key range of its tile pair
+    const int tiles = (n + tpt - 1) / tpt;
+    const int last = min(tiles - 1, (mt / 2) * 2 + 1);
+    const int i1 = min(n, (last + 1) * tpt);
     const int KT = (L - n + i1 + BN - 1) / BN;
     const int ns = (KT + p.tiles_per_split - 1) / p.tiles_per_split;
     if (ns <= 1) return;
