@@ -379,35 +379,36 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!wait_w(bar(B_S + 2 * gi + (jj & 1)), (jj >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 float sv[BN];
+                tmem_ld64(tS(gi, jj & 1) + lane_base, sv);
+                // raw scores; the scale (> 0) is applied inside the exponent's FFMA,
+                // so the max is taken on the raw values
+                float mraw = -INFINITY;
+                if (t0 + BN - 1 <= pos_min) {            // every key of the tile is visible
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    float tmp[32];
-                    tmem_ld32(tS(gi, jj & 1) + lane_base + c * 32, tmp);
+                    for (int c = 0; c < BN; ++c) mraw = fmaxf(mraw, sv[c]);
+                } else {                                 // diagonal tile: causal mask
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) sv[c * 32 + e] = tmp[e];
+                    for (int c = 0; c < BN; ++c) {
+                        if (t0 + c > pos) sv[c] = -INFINITY;
+                        mraw = fmaxf(mraw, sv[c]);
+                    }
                 }
-                const bool full = t0 + BN - 1 <= pos_min;
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    float v = sv[c] * p.scale_log2;
-                    if (!full && t0 + c > pos) v = -INFINITY;
-                    sv[c] = v;
-                    mx = fmaxf(mx, v);
-                }
+                const float mx = mraw * p.scale_log2;
                 float alpha = 1.f;
                 if (mx > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mx != -INFINITY)) {
                     alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx);
                     m_ref = mx;
                 }
-                // exponentials first: this overlaps the previous PV product
+                // exponentials first: this overlaps the previous PV product.  With no
+                // visible key yet (m_ref = -inf) every score is -inf and the
+                // reference 0 keeps the exponent at -inf, i.e. p = 0.
+                const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;
                 float sum = 0.f;
-                const bool live = m_ref != -INFINITY;
                 uint32_t pw[BN / 2];
 #pragma unroll
                 for (int e = 0; e < BN / 2; ++e) {
-                    const float p0 = live ? ex2(sv[2 * e] - m_ref) : 0.f;
-                    const float p1 = live ? ex2(sv[2 * e + 1] - m_ref) : 0.f;
+                    const float p0 = ex2(fmaf(sv[2 * e], p.scale_log2, mneg));
+                    const float p1 = ex2(fmaf(sv[2 * e + 1], p.scale_log2, mneg));
                     sum += p0 + p1;
                     pw[e] = pack_bf16(p0, p1);
                 }
