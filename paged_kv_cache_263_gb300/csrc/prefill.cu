@@ -13,23 +13,25 @@
 // partition):
 //  * A query tile packs 128/G chunk tokens x the G query heads of one KV head
 //    (row = token * G + head), so every K/V tile is shared by the whole GQA
-//    group; the two tiles of a pair share every K/V tile as well.  Q (3-D TMA
-//    boxes) stays in shared memory for the CTA's life.
+//    group; the two tiles of a pair share every K/V tile as well.
 //  * K/V tiles of 64 keys = 4 physical blocks, gathered through the block
-//    table by 2-D TMA loads (128-byte swizzle) into a 3-stage ring.
+//    table by 2-D TMA loads (128-byte swizzle) into a 6-stage ring.
 //  * S[128x64] = Q K^T and O[128x128] += P V run as tcgen05.mma (K=16 steps)
-//    issued by one thread, accumulators in tensor memory (per tile: S 64
-//    columns, O 128).  K is the K-major B operand of the first product; V is
+//    issued by one thread.  The A operands (Q, written once, and P) are read
+//    from tensor memory, so shared memory only streams K and V -- with A from
+//    shared memory these narrow products were bound by shared-memory
+//    bandwidth, not by the tensor cores.  Accumulators live in tensor memory
+//    too: per query tile Q 64 columns, S 64 (P overwrites its first 32 with
+//    bf16 pairs), O 128.  K is the K-major B operand of the first product, V
 //    the MN-major B operand of the second, straight from the same tiles.
 //  * Two softmax warpgroups, one per query tile, own one TMEM lane (= one query
 //    row) per thread.  They read S with tcgen05.ld, apply the causal mask on
 //    diagonal tiles, keep the online max / normaliser ("FlashAttention"
-//    section: running max and normaliser per block), compute P before waiting
-//    for the previous PV product, write P in bf16 to shared memory in the
-//    operand layout, and rescale O in tensor memory only when the running max
-//    grew by more than 2^8 (otherwise the stale max is kept; exact in the end).
-//    The MMA thread alternates between the two tiles, so one group's softmax
-//    overlaps the other group's tensor-core work.
+//    section: running max and normaliser per block), write P, and rescale O in
+//    tensor memory only when the running max grew by more than 2^8 (otherwise
+//    the stale max is kept; exact in the end).  The MMA thread alternates
+//    between the two tiles, so one group's softmax overlaps the other group's
+//    tensor-core work.
 //  * Long contexts are cut into 16,384-key partitions of whole tiles, merged
 //    by a fixed-order log-sum-exp kernel (no atomics).
 #include "common.cuh"
@@ -46,24 +48,23 @@ constexpr int BM = 128, BN = 64;               // 128 query rows x 64 keys (4 bl
 // warps 0-3 softmax of query tile 0, 4-7 softmax of query tile 1, 8 TMA producer,
 // 9 MMA issuer
 constexpr int THREADS = 320;
-constexpr int KV_STAGES = 4;
+constexpr int KV_STAGES = 6;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
-// shared memory: Q 2 x 32 KiB | 4 stages of (K 16 KiB, V 16 KiB) | P 2 x 16 KiB | barriers
-constexpr uint32_t SQ = 0, Q_TILE = 32768;
-constexpr uint32_t SKV = 65536, KV_STAGE_BYTES = 32768, V_OFF = 16384, KV_HALF = 8192;
-constexpr uint32_t SP = SKV + KV_STAGES * KV_STAGE_BYTES, P_TILE = 16384;
-constexpr uint32_t SBAR = SP + 2 * P_TILE;
+// shared memory: 6 stages of (K 16 KiB, V 16 KiB) | barriers.  Q and P live in
+// tensor memory, so shared memory only streams K and V.
+constexpr uint32_t SKV = 0, KV_STAGE_BYTES = 32768, V_OFF = 16384, KV_HALF = 8192;
+constexpr uint32_t SBAR = KV_STAGES * KV_STAGE_BYTES;
 constexpr int SMEM_BYTES = SBAR + 256;
 // barriers
 enum {
-    B_Q = 0,
-    B_KVF = 1,                      // + stage: K and V of a tile landed
+    B_KVF = 0,                      // + stage: K and V of a tile landed
     B_KVE = B_KVF + KV_STAGES,      // + stage: every MMA reading the stage is done
-    B_S = B_KVE + KV_STAGES,        // + 2*group + buffer: an S tile of the group is in TMEM
-    B_P = B_S + 4,                  // + group: the group's P is in shared memory (128 arrivals)
-    B_PV = B_P + 2,                 // + group: the group's PV product finished
-    B_DRAIN = B_PV + 2,
+    B_QR = B_KVE + KV_STAGES,       // + group: the group's Q is in TMEM (128 arrivals)
+    B_S = B_QR + 2,                 // + group: S of the group's next tile is in TMEM
+    B_P = B_S + 2,                  // + group: the group's P is in TMEM (128 arrivals)
+    B_PVD = B_P + 2,                // + group: the group's last PV product finished
+    B_DRAIN = B_PVD + 2,
     NBAR
 };
 static_assert(NBAR * 8 + 8 <= 256, "barrier area");
@@ -79,6 +80,7 @@ constexpr uint32_t IDESC_PV = idesc(D, true);     // O[128 x 128] += P V, V MN-m
 
 struct PrefillParams {
     float *out;
+    const uint16_t *q;   // [rows][Hq][128] bf16
     const int32_t *cu_q_lens;
     const int32_t *context_lens;
     const int32_t *block_tables;
@@ -161,8 +163,8 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p)
+    prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                   const PrefillParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
@@ -208,15 +210,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(B_Q), 1);
         for (int i = 0; i < KV_STAGES; ++i) {
             mbar_init(bar(B_KVF + i), 1);
             mbar_init(bar(B_KVE + i), 1);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(bar(B_S + i), 1);
         for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_QR + i), 128);
+            mbar_init(bar(B_S + i), 1);
             mbar_init(bar(B_P + i), 128);
-            mbar_init(bar(B_PV + i), 1);
+            mbar_init(bar(B_PVD + i), 1);
         }
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
@@ -230,23 +232,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // TMEM columns: S double-buffered per group, 64 each (group gi, buffer b at
-    // (2 gi + b) * 64); O of group gi at 256 + 128 gi
-    auto tS = [&](int gi, int b) -> uint32_t { return tmem + (2 * gi + b) * BN; };
+    // TMEM columns per query tile gi: Q at 64 gi (64 columns of bf16 pairs), S at
+    // 128 + 64 gi (64 fp32 columns; P overwrites the first 32 with bf16 pairs once
+    // S has been read), O at 256 + 128 gi
+    auto tQ = [&](int gi) -> uint32_t { return tmem + gi * 64; };
+    auto tS = [&](int gi) -> uint32_t { return tmem + 128 + gi * BN; };
     auto tO = [&](int gi) -> uint32_t { return tmem + 256 + gi * D; };
 
     if (warp == 8) {
         // ======================= TMA producer
         const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks;
         const int nblk = (L + BS - 1) / BS;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar(B_Q), (has1 ? 4 : 2) * 16384);
-            for (int gi = 0; gi < (has1 ? 2 : 1); ++gi) {
-                const int zq = row0 + (2 * pair + gi) * tpt;
-                tma_load_3d(sbase + SQ + gi * Q_TILE, &qmap, 0, g * G, zq, bar(B_Q));
-                tma_load_3d(sbase + SQ + gi * Q_TILE + 16384, &qmap, 64, g * G, zq, bar(B_Q));
-            }
-        }
         int issued = 0;
         for (int jj = 0; jj < T; ++jj) {
             const int st = jj % KV_STAGES;
@@ -296,61 +292,62 @@ __global__ void __launch_bounds__(THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
         };
-        // S[gi] = Q[gi] K^T for KV tile jj
+        // S[gi] = Q[gi] K^T for KV tile jj: A = Q from TMEM, B = K (K-major) from smem
         auto issue_s = [&](int gi, int jj) {
             if (lane == 0) {
                 tc_fence_after();
                 const uint32_t kb = sbase + SKV + (jj % KV_STAGES) * KV_STAGE_BYTES;
-                const uint32_t qb = sbase + SQ + gi * Q_TILE;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {   // D = 128 in steps of 16: 4 per 64-wide half
-                    const uint32_t qoff = (kk >> 2) * 16384 + (kk & 3) * 32;
                     const uint32_t koff = (kk >> 2) * KV_HALF + (kk & 3) * 32;
-                    umma_f16(tS(gi, jj & 1), sdesc_sw128(qb + qoff, 16, 1024),
-                             sdesc_sw128(kb + koff, 16, 1024), IDESC_S, kk > 0);
+                    umma_f16_ts(tS(gi), tQ(gi) + kk * 8, sdesc_sw128(kb + koff, 16, 1024), IDESC_S, kk > 0);
                 }
-                umma_commit(bar(B_S + 2 * gi + (jj & 1)));
+                umma_commit(bar(B_S + gi));
             }
             __syncwarp();
         };
-        // O[gi] += P[gi] V for KV tile jj
+        // O[gi] += P[gi] V for KV tile jj: A = P from TMEM, B = V (MN-major) from smem
         auto issue_pv = [&](int gi, int jj) {
             if (lane == 0) {
                 tc_fence_after();
                 const uint32_t vb = sbase + SKV + (jj % KV_STAGES) * KV_STAGE_BYTES + V_OFF;
-                const uint32_t pb = sbase + SP + gi * P_TILE;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)   // 64 keys in steps of 16
-                    umma_f16(tO(gi), sdesc_sw128(pb + kk * 32, 16, 1024),
-                             sdesc_sw128(vb + kk * 2048, KV_HALF, 1024), IDESC_PV, (jj > 0 || kk > 0));
-                umma_commit(bar(B_PV + gi));
+                    umma_f16_ts(tO(gi), tS(gi) + kk * 8, sdesc_sw128(vb + kk * 2048, KV_HALF, 1024), IDESC_PV,
+                                (jj > 0 || kk > 0));
+                if (jj == T - 1) umma_commit(bar(B_PVD + gi));
             }
             __syncwarp();
         };
         const int ng = has1 ? 2 : 1;
-        // S of the first two tiles up front; afterwards S(jj+2) is issued as soon as
-        // PV(jj) is, so every softmax finds its S ready
-        bool ok = wait_w(bar(B_Q), 0);
-        for (int jj = 0; ok && jj < min(2, T); ++jj) {
-            if (!wait_w(bar(B_KVF + jj), 0)) { ok = false; break; }
-            fix_tail(jj);
-            for (int gi = 0; gi < ng; ++gi) issue_s(gi, jj);
+        bool ok = wait_w(bar(B_KVF), 0);
+        for (int gi = 0; ok && gi < ng; ++gi) {
+            if (!wait_w(bar(B_QR + gi), 0)) { ok = false; break; }
+        }
+        if (ok) {
+            fix_tail(0);
+            for (int gi = 0; gi < ng; ++gi) issue_s(gi, 0);
         }
         for (int jj = 0; jj < T && ok; ++jj) {
+            const bool more = jj + 1 < T;
             for (int gi = 0; gi < ng; ++gi) {
                 if (!wait_w(bar(B_P + gi), jj & 1)) { ok = false; break; }
+                // in issue order: PV(jj) reads P from the S columns before S(jj+1)
+                // overwrites them
                 issue_pv(gi, jj);
+                if (more) {
+                    if (gi == 0) {
+                        const int sn = (jj + 1) % KV_STAGES;
+                        if (!wait_w(bar(B_KVF + sn), ((jj + 1) / KV_STAGES) & 1)) { ok = false; break; }
+                        fix_tail(jj + 1);
+                    }
+                    issue_s(gi, jj + 1);
+                }
             }
             if (!ok) break;
             // the stage of tile jj is free once every MMA issued so far is done
             if (lane == 0) umma_commit(bar(B_KVE + jj % KV_STAGES));
             __syncwarp();
-            if (jj + 2 < T) {
-                const int sn = (jj + 2) % KV_STAGES;
-                if (!wait_w(bar(B_KVF + sn), ((jj + 2) / KV_STAGES) & 1)) { ok = false; break; }
-                fix_tail(jj + 2);
-                for (int gi = 0; gi < ng; ++gi) issue_s(gi, jj + 2);
-            }
         }
         // every MMA this thread issued has finished before TMEM is released
         if (lane == 0) umma_commit(bar(B_DRAIN));
@@ -365,21 +362,41 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int i = i0 + r / G;
             const int head = g * G + r % G;
             const bool row_valid = i < i1;
-            // last key this row may attend; rows past the chunk (loaded only to fill
+            // last key this row may attend; rows past the chunk (computed only to fill
             // the tile, never stored) take the tile's last valid row, so no row ever
             // sees a key at or beyond L
             const int pos = row_valid ? L - n + i : L - n + i1 - 1;
             const int pos_min = L - n + i0;
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-            const uint32_t pbase = sbase + SP + gi * P_TILE;
+            {
+                // this row of Q into the group's Q columns (bf16 pairs), once
+                uint32_t qw[64];
+                const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + ((size_t)(row0 + i) * p.hq + head) * D);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 v = row_valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+                    qw[4 * c] = v.x;
+                    qw[4 * c + 1] = v.y;
+                    qw[4 * c + 2] = v.z;
+                    qw[4 * c + 3] = v.w;
+                }
+                uint32_t (&q0)[32] = *reinterpret_cast<uint32_t (*)[32]>(qw);
+                uint32_t (&q1)[32] = *reinterpret_cast<uint32_t (*)[32]>(qw + 32);
+                tmem_st32u(tQ(gi) + lane_base, q0);
+                tmem_st32u(tQ(gi) + lane_base + 32, q1);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(B_QR + gi));
+            }
             float m_ref = -INFINITY, l = 0.f;
             bool ok = true;
             for (int jj = 0; jj < T && ok; ++jj) {
                 const int t0 = (j0 + jj) * BN;
-                if (!wait_w(bar(B_S + 2 * gi + (jj & 1)), (jj >> 1) & 1)) { ok = false; break; }
+                // S(jj) is committed after PV(jj-1): O and the P columns are free too
+                if (!wait_w(bar(B_S + gi), jj & 1)) { ok = false; break; }
                 tc_fence_after();
                 float sv[BN];
-                tmem_ld64(tS(gi, jj & 1) + lane_base, sv);
+                tmem_ld64(tS(gi) + lane_base, sv);
                 // raw scores; the scale (> 0) is applied inside the exponent's FFMA,
                 // so the max is taken on the raw values
                 float mraw = -INFINITY;
@@ -399,8 +416,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx);
                     m_ref = mx;
                 }
-                // exponentials first: this overlaps the previous PV product.  With no
-                // visible key yet (m_ref = -inf) every score is -inf and the
+                // With no visible key yet (m_ref = -inf) every score is -inf and the
                 // reference 0 keeps the exponent at -inf, i.e. p = 0.
                 const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;
                 float sum = 0.f;
@@ -413,32 +429,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                     pw[e] = pack_bf16(p0, p1);
                 }
                 l = l * alpha + sum;
-                if (jj > 0) {
-                    // the previous PV has read P and written O: both may change now
-                    if (!wait_w(bar(B_PV + gi), (jj - 1) & 1)) { ok = false; break; }
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            float o[32];
-                            tmem_ld32(tO(gi) + lane_base + c * 32, o);
+                    for (int c = 0; c < 4; ++c) {
+                        float o[32];
+                        tmem_ld32(tO(gi) + lane_base + c * 32, o);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                            tmem_st32(tO(gi) + lane_base + c * 32, o);
-                        }
-                        tmem_wait_st();
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st32(tO(gi) + lane_base + c * 32, o);
                     }
                 }
-                // P in bf16, K-major 128-byte-swizzled operand layout: row r, keys 0..63
-#pragma unroll
-                for (int c8 = 0; c8 < BN / 8; ++c8)
-                    st_shared_v4(pbase + r * 128 + ((c8 ^ (r & 7)) << 4), pw[4 * c8], pw[4 * c8 + 1],
-                                 pw[4 * c8 + 2], pw[4 * c8 + 3]);
-                fence_proxy_async_smem();
+                // P in bf16 pairs over the first 32 S columns (the A operand of PV)
+                tmem_st32u(tS(gi) + lane_base, pw);
+                tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(B_P + gi));
             }
-            if (ok && wait_w(bar(B_PV + gi), (T - 1) & 1)) {
+            if (ok && wait_w(bar(B_PVD + gi), 0)) {
                 tc_fence_after();
                 const size_t rh = (size_t)(row0 + (row_valid ? i : i0)) * p.hq + head;
                 const size_t pi = rh * p.max_splits + split;
@@ -617,6 +624,7 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     // prefill chunks (n >= 2)
     PrefillParams p{};
     p.out = out;
+    p.q = static_cast<const uint16_t *>(q);
     p.cu_q_lens = cu_q_lens;
     p.context_lens = context_lens;
     p.block_tables = block_tables;
@@ -633,12 +641,8 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     p.tiles_per_split = pl.tiles_per_split;
     p.max_splits = std::max(1, pl.max_splits);
     p.scale_log2 = scale * LOG2E;
-    CUtensorMap qm, km, vm;
+    CUtensorMap km, vm;
     const int tpt = BM / G;
-    if (!pkv_host::encode_tmap_3d(&qm, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, num_q_heads, total_q_tokens,
-                                  (uint64_t)D * 2, (uint64_t)num_q_heads * D * 2, 64, G, tpt,
-                                  CU_TENSOR_MAP_SWIZZLE_128B))
-        return KV_ERR_CUDA;
     if (!pkv_decode::make_maps(k_cache, v_cache, num_blocks, num_kv_heads, dtype, &km, &vm)) return KV_ERR_CUDA;
     static bool configured = false;
     if (!configured) {
@@ -652,7 +656,7 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     const int64_t tiles_ub = (total_q_tokens + tpt - 1) / tpt + std::min<int64_t>(num_seqs, total_q_tokens / 2);
     if (tiles_ub > INT32_MAX || p.max_splits > 65535) return KV_ERR_UNSUPPORTED;
     dim3 grid((unsigned)tiles_ub, num_kv_heads, p.max_splits);
-    prefill_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(qm, km, vm, p);
+    prefill_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(km, vm, p);
     if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
     if (p.max_splits > 1) {
         const int64_t warps = (int64_t)total_q_tokens * num_q_heads;
