@@ -17,7 +17,7 @@
 //  * K/V tiles of 64 keys = 4 physical blocks, gathered through the block
 //    table by 2-D TMA loads (128-byte swizzle) into a 6-stage ring.
 //  * S[128x64] = Q K^T and O[128x128] += P V run as tcgen05.mma (K=16 steps)
-//    issued by one thread.  The A operands (Q, written once, and P) are read
+//    issued by one thread per query tile.  The A operands (Q, written once, and P) are read
 //    from tensor memory, so shared memory only streams K and V -- with A from
 //    shared memory these narrow products were bound by shared-memory
 //    bandwidth, not by the tensor cores.  Accumulators live in tensor memory
@@ -29,9 +29,10 @@
 //    diagonal tiles, keep the online max / normaliser ("FlashAttention"
 //    section: running max and normaliser per block), write P, and rescale O in
 //    tensor memory only when the running max grew by more than 2^8 (otherwise
-//    the stale max is kept; exact in the end).  The MMA thread alternates
-//    between the two tiles, so one group's softmax overlaps the other group's
-//    tensor-core work.
+//    the stale max is kept; exact in the end).  Each tile has its own MMA
+//    issuer, so one group's softmax overlaps the other group's tensor-core
+//    work; descriptors are precomputed so the issuers keep up with the
+//    tensor cores even for the 64-wide products.
 //  * Long contexts are cut into 16,384-key partitions of whole tiles, merged
 //    by a fixed-order log-sum-exp kernel (no atomics).
 #include "common.cuh"
@@ -46,8 +47,8 @@ using namespace pkv;
 
 constexpr int BM = 128, BN = 64;               // 128 query rows x 64 keys (4 blocks) per tile
 // warps 0-3 softmax of query tile 0, 4-7 softmax of query tile 1, 8 TMA producer,
-// 9 MMA issuer
-constexpr int THREADS = 320;
+// 9 and 10 MMA issuers of query tile 0 and 1
+constexpr int THREADS = 352;
 constexpr int KV_STAGES = 6;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -64,7 +65,8 @@ enum {
     B_S = B_QR + 2,                 // + group: S of the group's next tile is in TMEM
     B_P = B_S + 2,                  // + group: the group's P is in TMEM (128 arrivals)
     B_PVD = B_P + 2,                // + group: the group's last PV product finished
-    B_DRAIN = B_PVD + 2,
+    B_DRAIN = B_PVD + 2,            // + group: every MMA of the group's issuer finished
+    B_TAIL = B_DRAIN + 2,           // the V rows past the context are zeroed
     NBAR
 };
 static_assert(NBAR * 8 + 8 <= 256, "barrier area");
@@ -212,15 +214,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < KV_STAGES; ++i) {
             mbar_init(bar(B_KVF + i), 1);
-            mbar_init(bar(B_KVE + i), 1);
+            mbar_init(bar(B_KVE + i), has1 ? 2 : 1);   // one release per MMA issuer
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_QR + i), 128);
             mbar_init(bar(B_S + i), 1);
             mbar_init(bar(B_P + i), 128);
             mbar_init(bar(B_PVD + i), 1);
+            mbar_init(bar(B_DRAIN + i), 1);
         }
-        mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_TAIL), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -269,90 +272,87 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tma_load_2d(vd + KV_HALF, &vmap, 64, y, bar(B_KVF + st));
             }
             issued = jj + 1;
+            const int first = L - j * BN;            // first row of the tile at or past L
+            if (first < BN) {
+                // keys >= L: their V rows may hold anything (never written, or not
+                // loaded); P is 0 there but 0 * NaN is NaN, so zero them once the
+                // tile has landed, before any PV product reads it
+                if (!wait_w(bar(B_KVF + st), (jj / KV_STAGES) & 1)) break;
+                const uint32_t vb = sbase + SKV + st * KV_STAGE_BYTES + V_OFF;
+                for (int c = lane; c < (BN - first) * 16; c += 32) {
+                    const int r = first + (c >> 4), h = (c >> 3) & 1, ch = c & 7;
+                    st_shared_v4(vb + h * KV_HALF + r * 128 + ch * 16, 0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_TAIL));
+            }
         }
         if (*abort_flag) {
             // let loads already in flight land before the CTA exits
             for (int jj = max(0, issued - KV_STAGES); jj < issued; ++jj)
                 (void)mbar_wait_bounded(bar(B_KVF + jj % KV_STAGES), (jj / KV_STAGES) & 1);
         }
-    } else if (warp == 9) {
-        // ======================= MMA issuer (+ zeroing of V rows past the context)
-        auto fix_tail = [&](int jj) {
-            // keys >= L of the tile: their V rows may hold anything (never written,
-            // or not loaded); P is 0 there, but 0 * NaN is NaN, so zero the rows
-            const int t0 = (j0 + jj) * BN;
-            const int first = L - t0;            // first invalid row in the tile
-            if (first >= BN) return;
-            const uint32_t vb = sbase + SKV + (jj % KV_STAGES) * KV_STAGE_BYTES + V_OFF;
-            const int nchunks = (BN - first) * 2 * 8;   // rows x 2 halves x 8 chunks of 16 B
-            for (int c = lane; c < nchunks; c += 32) {
-                const int r = first + (c >> 4), h = (c >> 3) & 1, ch = c & 7;
-                st_shared_v4(vb + h * KV_HALF + r * 128 + ch * 16, 0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        };
-        // S[gi] = Q[gi] K^T for KV tile jj: A = Q from TMEM, B = K (K-major) from smem
-        auto issue_s = [&](int gi, int jj) {
-            if (lane == 0) {
-                tc_fence_after();
-                const uint32_t kb = sbase + SKV + (jj % KV_STAGES) * KV_STAGE_BYTES;
+    } else if (warp == 9 || warp == 10) {
+        // ======================= MMA issuers: warp 9 for query tile 0, warp 10 for tile 1
+        const int gi = warp - 9;
+        if (gi == 0 || has1) {
+            // shared-memory descriptors of stage 0; other stages and K steps are
+            // constant byte offsets added to the start-address field (in 16-byte
+            // units; shared memory is < 256 KiB, so the 14-bit field never carries)
+            const uint64_t kdesc0 = sdesc_sw128(sbase + SKV, 16, 1024);
+            const uint64_t vdesc0 = sdesc_sw128(sbase + SKV + V_OFF, KV_HALF, 1024);
+            const uint32_t tq = tQ(gi), ts = tS(gi), to = tO(gi);
+            // S = Q K^T for KV tile jj: A = Q from TMEM, B = K (K-major) from smem
+            auto issue_s = [&](int jj) {
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint64_t kd = kdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {   // D = 128 in steps of 16: 4 per 64-wide half
-                    const uint32_t koff = (kk >> 2) * KV_HALF + (kk & 3) * 32;
-                    umma_f16_ts(tS(gi), tQ(gi) + kk * 8, sdesc_sw128(kb + koff, 16, 1024), IDESC_S, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk)   // D = 128 in steps of 16: 4 per 64-wide half
+                        umma_f16_ts(ts, tq + kk * 8, kd + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4),
+                                    IDESC_S, kk > 0);
+                    umma_commit(bar(B_S + gi));
                 }
-                umma_commit(bar(B_S + gi));
-            }
-            __syncwarp();
-        };
-        // O[gi] += P[gi] V for KV tile jj: A = P from TMEM, B = V (MN-major) from smem
-        auto issue_pv = [&](int gi, int jj) {
-            if (lane == 0) {
-                tc_fence_after();
-                const uint32_t vb = sbase + SKV + (jj % KV_STAGES) * KV_STAGE_BYTES + V_OFF;
+                __syncwarp();
+            };
+            // O += P V for KV tile jj: A = P from TMEM, B = V (MN-major) from smem
+            auto issue_pv = [&](int jj) {
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint64_t vd = vdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)   // 64 keys in steps of 16
-                    umma_f16_ts(tO(gi), tS(gi) + kk * 8, sdesc_sw128(vb + kk * 2048, KV_HALF, 1024), IDESC_PV,
-                                (jj > 0 || kk > 0));
-                if (jj == T - 1) umma_commit(bar(B_PVD + gi));
-            }
-            __syncwarp();
-        };
-        const int ng = has1 ? 2 : 1;
-        bool ok = wait_w(bar(B_KVF), 0);
-        for (int gi = 0; ok && gi < ng; ++gi) {
-            if (!wait_w(bar(B_QR + gi), 0)) { ok = false; break; }
-        }
-        if (ok) {
-            fix_tail(0);
-            for (int gi = 0; gi < ng; ++gi) issue_s(gi, 0);
-        }
-        for (int jj = 0; jj < T && ok; ++jj) {
-            const bool more = jj + 1 < T;
-            for (int gi = 0; gi < ng; ++gi) {
-                if (!wait_w(bar(B_P + gi), jj & 1)) { ok = false; break; }
+                    for (int kk = 0; kk < BN / 16; ++kk)   // 64 keys in steps of 16
+                        umma_f16_ts(to, ts + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), IDESC_PV,
+                                    (jj > 0 || kk > 0) ? 1u : 0u);
+                    if (jj == T - 1) umma_commit(bar(B_PVD + gi));
+                    // the stage is released once both issuers' MMAs reading it are done
+                    umma_commit(bar(B_KVE + jj % KV_STAGES));
+                }
+                __syncwarp();
+            };
+            // a tile holding keys >= L is read by PV only after the producer zeroed them
+            auto tail_ready = [&](int jj) -> bool {
+                return (j0 + jj + 1) * BN <= L || wait_w(bar(B_TAIL), 0);
+            };
+            bool ok = wait_w(bar(B_QR + gi), 0) && wait_w(bar(B_KVF), 0);
+            if (ok) issue_s(0);
+            for (int jj = 0; jj < T && ok; ++jj) {
+                if (!wait_w(bar(B_P + gi), jj & 1) || !tail_ready(jj)) { ok = false; break; }
                 // in issue order: PV(jj) reads P from the S columns before S(jj+1)
                 // overwrites them
-                issue_pv(gi, jj);
-                if (more) {
-                    if (gi == 0) {
-                        const int sn = (jj + 1) % KV_STAGES;
-                        if (!wait_w(bar(B_KVF + sn), ((jj + 1) / KV_STAGES) & 1)) { ok = false; break; }
-                        fix_tail(jj + 1);
-                    }
-                    issue_s(gi, jj + 1);
+                issue_pv(jj);
+                if (jj + 1 < T) {
+                    const int sn = (jj + 1) % KV_STAGES;
+                    if (!wait_w(bar(B_KVF + sn), ((jj + 1) / KV_STAGES) & 1)) { ok = false; break; }
+                    issue_s(jj + 1);
                 }
             }
-            if (!ok) break;
-            // the stage of tile jj is free once every MMA issued so far is done
-            if (lane == 0) umma_commit(bar(B_KVE + jj % KV_STAGES));
+            // every MMA this issuer started has finished before TMEM is released
+            if (lane == 0) umma_commit(bar(B_DRAIN + gi));
             __syncwarp();
+            (void)mbar_wait_bounded(bar(B_DRAIN + gi), 0);
         }
-        // every MMA this thread issued has finished before TMEM is released
-        if (lane == 0) umma_commit(bar(B_DRAIN));
-        __syncwarp();
-        (void)mbar_wait_bounded(bar(B_DRAIN), 0);
     } else {
         // ======================= softmax warpgroups: thread = query row = TMEM lane
         const int gi = warp >> 2;                  // which query tile of the pair
