@@ -399,17 +399,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld64(tS(gi) + lane_base, sv);
                 // raw scores; the scale (> 0) is applied inside the exponent's FFMA,
                 // so the max is taken on the raw values
-                float mraw = -INFINITY;
-                if (t0 + BN - 1 <= pos_min) {            // every key of the tile is visible
+                if (t0 + BN - 1 > pos_min) {             // diagonal tile: causal mask
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) mraw = fmaxf(mraw, sv[c]);
-                } else {                                 // diagonal tile: causal mask
-#pragma unroll
-                    for (int c = 0; c < BN; ++c) {
+                    for (int c = 0; c < BN; ++c)
                         if (t0 + c > pos) sv[c] = -INFINITY;
-                        mraw = fmaxf(mraw, sv[c]);
-                    }
                 }
+                // max over the 64 scores as 8 independent chains (latency, not issue,
+                // bounds this loop)
+                float mk[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mk[k] = sv[k];
+#pragma unroll
+                for (int c = 8; c < BN; ++c) mk[c & 7] = fmaxf(mk[c & 7], sv[c]);
+                const float mraw = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
+                                         fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
                 const float mx = mraw * p.scale_log2;
                 float alpha = 1.f;
                 if (mx > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mx != -INFINITY)) {
@@ -419,15 +422,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // With no visible key yet (m_ref = -inf) every score is -inf and the
                 // reference 0 keeps the exponent at -inf, i.e. p = 0.
                 const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;
-                float sum = 0.f;
+                float sk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 uint32_t pw[BN / 2];
 #pragma unroll
                 for (int e = 0; e < BN / 2; ++e) {
                     const float p0 = ex2(fmaf(sv[2 * e], p.scale_log2, mneg));
                     const float p1 = ex2(fmaf(sv[2 * e + 1], p.scale_log2, mneg));
-                    sum += p0 + p1;
+                    sk[e & 7] += p0 + p1;
                     pw[e] = pack_bf16(p0, p1);
                 }
+                const float sum = ((sk[0] + sk[1]) + (sk[2] + sk[3])) + ((sk[4] + sk[5]) + (sk[6] + sk[7]));
                 l = l * alpha + sum;
                 if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
