@@ -231,7 +231,10 @@ PAGEDKV_API kv_status paged_attention_decode_static_scratch(
  * context_len-n_s .. context_len-1, row i attends keys 0 .. context_len-n_s+i
  * (causal inside the chunk, everything before it visible).  Rows with n_s = 1
  * are decode rows and take the decode kernel; chunks (n_s >= 2) take the
- * tensor-core (tcgen05) kernel.
+ * tensor-core (tcgen05) kernel.  When the batch has chunks, the decode rows run
+ * on a stream the library owns (one per device), forked from `stream` with an
+ * event and joined back into it before the call returns: work enqueued on
+ * `stream` afterwards sees the whole output.
  *
  *  out, q          device [total_q_tokens][num_q_heads][128] (fp32 / bf16)
  *  cu_q_lens       device int32 [num_seqs+1], cu_q_lens[0] = 0, non-decreasing,

@@ -38,6 +38,7 @@
 #include "common.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace {
 
@@ -401,15 +402,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int c = 0; c < BN; ++c)
                         if (t0 + c > pos) sv[c] = -INFINITY;
                 }
-                // max over the 64 scores as 8 independent chains (latency, not issue,
-                // bounds this loop)
-                float mk[8];
+                // max over the 64 scores: four independent chains of 3-input maxima
+                float mk[4];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mk[k] = sv[k];
+                for (int k = 0; k < 4; ++k) mk[k] = fmaxf(sv[k], sv[4 + k]);        // elements 0..7
 #pragma unroll
-                for (int c = 8; c < BN; ++c) mk[c & 7] = fmaxf(mk[c & 7], sv[c]);
-                const float mraw = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
-                                         fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+                for (int c = 8; c < BN; c += 8) {                                      // elements c..c+7
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) mk[k] = max3(mk[k], sv[c + k], sv[c + 4 + k]);
+                }
+                const float mraw = max3(mk[0], mk[1], fmaxf(mk[2], mk[3]));
                 const float mx = mraw * p.scale_log2;
                 float alpha = 1.f;
                 if (mx > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mx != -INFINITY)) {
@@ -419,16 +421,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // With no visible key yet (m_ref = -inf) every score is -inf and the
                 // reference 0 keeps the exponent at -inf, i.e. p = 0.
                 const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;
-                float sk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // exponent argument and running sum on packed fp32 pairs
+                const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2), mn2 = f2_pack(mneg, mneg);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
                 uint32_t pw[BN / 2];
 #pragma unroll
                 for (int e = 0; e < BN / 2; ++e) {
-                    const float p0 = ex2(fmaf(sv[2 * e], p.scale_log2, mneg));
-                    const float p1 = ex2(fmaf(sv[2 * e + 1], p.scale_log2, mneg));
-                    sk[e & 7] += p0 + p1;
+                    float y0, y1;
+                    f2_unpack(f2_fma(f2_pack(sv[2 * e], sv[2 * e + 1]), sl2, mn2), y0, y1);
+                    const float p0 = ex2(y0), p1 = ex2(y1);
+                    acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
                     pw[e] = pack_bf16(p0, p1);
                 }
-                const float sum = ((sk[0] + sk[1]) + (sk[2] + sk[3])) + ((sk[4] + sk[5]) + (sk[6] + sk[7]));
+                const uint64_t a2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+                float s0, s1;
+                f2_unpack(a2, s0, s1);
+                const float sum = s0 + s1;
                 l = l * alpha + sum;
                 if (jj > 0) {
                     // PV(jj-1) finished: O holds every earlier tile, and PV(jj-2), which
@@ -572,6 +580,33 @@ Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq,
 }
 }  // namespace
 
+namespace {
+// A library-owned stream per device on which the decode rows of a mixed batch
+// run next to the chunk tiles (memory-bound next to tensor-bound work), joined
+// back into the caller's stream with events.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int MAX_DEVICES = 64;
+std::mutex g_side_mu;
+SideStream g_side[MAX_DEVICES];
+
+SideStream *side_stream()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+    SideStream &ss = g_side[dev];
+    if (!ss.stream) {
+        if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+    }
+    return &ss;
+}
+}  // namespace
+
 namespace pkv_prefill {
 uint32_t take_status()
 {
@@ -623,12 +658,27 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
         return KV_ERR_INVALID;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    // decode rows (n = 1)
-    kv_status rs = pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                                   cu_q_lens, total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks,
-                                   scale, dtype, k_scale, v_scale, num_splits, pl.decode_bytes ? ws : nullptr,
-                                   pl.decode_bytes, st);
-    if (rs != KV_OK || max_q_len < 2) return rs;
+    auto decode_rows = [&](cudaStream_t on) {
+        return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
+                               total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
+                               k_scale, v_scale, num_splits, pl.decode_bytes ? ws : nullptr, pl.decode_bytes, on);
+    };
+    if (max_q_len < 2) return decode_rows(st);   // decode rows only
+    // decode rows (n = 1) on the side stream, forked from and joined into the
+    // caller's stream; the chunk tiles run on the caller's stream meanwhile
+    std::lock_guard<std::mutex> side_lock(g_side_mu);
+    SideStream *side = side_stream();
+    if (!side) return KV_ERR_CUDA;
+    if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+        return KV_ERR_CUDA;
+    kv_status rs = decode_rows(side->stream);
+    if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return KV_ERR_CUDA;
+    struct Join {   // the caller's stream waits for the decode rows however this call ends
+        cudaStream_t st;
+        SideStream *side;
+        ~Join() { cudaStreamWaitEvent(st, side->join, 0); }
+    } join{st, side};
+    if (rs != KV_OK) return rs;
     // prefill chunks (n >= 2)
     PrefillParams p{};
     p.out = out;
