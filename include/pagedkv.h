@@ -230,11 +230,14 @@ PAGEDKV_API kv_status paged_attention_decode_static_scratch(
  * cu_q_lens[s] .. cu_q_lens[s+1]-1; its n_s rows sit at positions
  * context_len-n_s .. context_len-1, row i attends keys 0 .. context_len-n_s+i
  * (causal inside the chunk, everything before it visible).  Rows with n_s = 1
- * are decode rows and take the decode kernel; chunks (n_s >= 2) take the
- * tensor-core (tcgen05) kernel.  When the batch has chunks, the decode rows run
- * on a stream the library owns (one per device), forked from `stream` with an
+ * are decode rows and take the decode kernel; with a bf16 cache, chunks
+ * (n_s >= 2) take the tensor-core (tcgen05) kernel, and the decode rows run on
+ * a stream the library owns (one per device), forked from `stream` with an
  * event and joined back into it before the call returns: work enqueued on
- * `stream` afterwards sees the whole output.
+ * `stream` afterwards sees the whole output.  With an fp8 cache and chunks,
+ * every row of the batch (chunk rows included) is a decode problem of its own
+ * over the keys it may see, on `stream`: total_q_tokens <= 65535 (else
+ * KV_ERR_UNSUPPORTED), partitions of 16,384 keys, num_splits ignored.
  *
  *  out, q          device [total_q_tokens][num_q_heads][128] (fp32 / bf16)
  *  cu_q_lens       device int32 [num_seqs+1], cu_q_lens[0] = 0, non-decreasing,
@@ -242,7 +245,8 @@ PAGEDKV_API kv_status paged_attention_decode_static_scratch(
  *  context_lens    device int32 [num_seqs]; includes the chunk; n_s <= len
  *  max_q_len       host int: an upper bound on every n_s (sizes the grid)
  *  other arguments as for paged_attention_decode; workspace must be at least
- *  paged_attention_chunked_prefill_workspace_size() bytes.
+ *  paged_attention_chunked_prefill_workspace_size() bytes (one size serves
+ *  both cache dtypes).
  * ---------------------------------------------------------------------- */
 PAGEDKV_API size_t paged_attention_chunked_prefill_workspace_size(int32_t num_seqs, int32_t total_q_tokens,
                                                       int32_t max_q_len, int32_t num_q_heads,

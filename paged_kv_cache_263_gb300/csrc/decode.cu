@@ -56,9 +56,10 @@ struct DecodeParams {
     const int32_t *context_lens;
     const int32_t *cu_q_lens;  // mixed batches: only sequences with one query row
     int total_rows;            // rows of q/out (mixed batches)
+    int row_mode;              // every row of a mixed batch is its own problem (see row_keys)
     const float *k_scale;
     const float *v_scale;
-    float *part_o;             // [B][Hq][S][128]
+    float *part_o;             // [B][Hq][S][128]   (B = rows in row mode)
     float *part_ml;            // [B][Hq][S][2]
     int max_blocks;
     int num_seqs;
@@ -96,6 +97,28 @@ struct Geo {
 
 __device__ __forceinline__ void flag(uint32_t bits) { atomicOr(&g_status, bits); }
 
+// Row mode: query row r of a mixed batch as a decode problem of its own.  The
+// sequence seq owning the row is found by binary search over cu_q_lens; with n
+// rows in its chunk and context length L (chunk included), row i = r - cu[seq]
+// of the chunk sees keys 0 .. L - n + i, so the problem has L - n + i + 1 keys.
+// Returns 0 (flagged by the caller as a bad length) for a malformed batch.
+__device__ __forceinline__ int row_keys(const DecodeParams &p, int r, int &seq)
+{
+    const int32_t *cu = p.cu_q_lens;
+    int lo = 0, hi = p.num_seqs;                 // cu[lo] <= r < cu[hi] if well formed
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(cu + mid) <= r) lo = mid;
+        else hi = mid;
+    }
+    seq = lo;
+    const int a = __ldg(cu + lo), b = __ldg(cu + lo + 1);
+    if (r < a || r >= b) return 0;
+    const int n = b - a, L = __ldg(p.context_lens + lo);
+    if (n > L || L > p.max_blocks * BS) return 0;
+    return L - n + (r - a) + 1;
+}
+
 template <bool FP8>
 __device__ __forceinline__ void issue_stage(uint32_t dst, uint32_t bar, const CUtensorMap *km,
                                             const CUtensorMap *vm, int32_t y)
@@ -123,24 +146,30 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
                                                 ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WARPS * GE::RING);
 
-    const int split = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+    const int split = blockIdx.x, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, cq = lane & 3;
     // launched with programmatic serialisation: the CTA may be resident before
     // the previous kernel on the stream (typically the cache write) finished
     griddep_wait();
 
-    int row = s;
-    if (p.cu_q_lens) {
-        int a = p.cu_q_lens[s], b = p.cu_q_lens[s + 1];
-        if (b - a != 1) return;
-        if (a < 0 || b > p.total_rows) {
-            if (split == 0 && g == 0 && threadIdx.x == 0) flag(ST_BAD_LEN);
-            return;
+    // s: sequence (block table); row: row of q/out; wi: index of the partials
+    int s = blockIdx.z, row = s, wi = s, L;
+    if (p.row_mode) {
+        row = wi = blockIdx.z;
+        L = row_keys(p, row, s);
+    } else {
+        if (p.cu_q_lens) {
+            int a = p.cu_q_lens[s], b = p.cu_q_lens[s + 1];
+            if (b - a != 1) return;
+            if (a < 0 || b > p.total_rows) {
+                if (split == 0 && g == 0 && threadIdx.x == 0) flag(ST_BAD_LEN);
+                return;
+            }
+            row = a;
         }
-        row = a;
+        L = p.context_lens[s];
     }
-    const int L = p.context_lens[s];
     if (L < 1 || L > p.max_blocks * BS) {
         if (split == 0) {
             if (threadIdx.x == 0) flag(ST_BAD_LEN);
@@ -461,7 +490,7 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
         if (nsplit_s == 1) {
             p.out[((size_t)row * p.hq + h) * D + d] = Ls > 0.f ? O * vsc / Ls : 0.f;
         } else {
-            const size_t pi = ((size_t)s * p.hq + h) * p.num_splits + split;
+            const size_t pi = ((size_t)wi * p.hq + h) * p.num_splits + split;
             p.part_o[pi * D + d] = O * vsc;
             if (d == 0) {
                 p.part_ml[pi * 2] = (Ls > 0.f) ? M : -INFINITY;
@@ -477,20 +506,25 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p)
     griddep_wait();   // the partials come from the decode kernel just before
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (wid >= p.num_seqs * p.hq) return;
-    const int s = wid / p.hq, h = wid % p.hq;
-    int row = s;
-    if (p.cu_q_lens) {
-        int a = p.cu_q_lens[s], b = p.cu_q_lens[s + 1];
-        if (b - a != 1 || a < 0 || b > p.total_rows) return;
-        row = a;
+    if (wid >= (p.row_mode ? p.total_rows : p.num_seqs) * p.hq) return;
+    const int wi = wid / p.hq, h = wid % p.hq;   // wi: sequence, or row in row mode
+    int row = wi, L;
+    if (p.row_mode) {
+        int seq;
+        L = row_keys(p, row, seq);
+    } else {
+        if (p.cu_q_lens) {
+            int a = p.cu_q_lens[wi], b = p.cu_q_lens[wi + 1];
+            if (b - a != 1 || a < 0 || b > p.total_rows) return;
+            row = a;
+        }
+        L = p.context_lens[wi];
     }
-    const int L = p.context_lens[s];
     if (L < 1 || L > p.max_blocks * BS) return;
     const int nblk = (L + BS - 1) / BS;
     const int ns = (nblk + p.part_blocks - 1) / p.part_blocks;
     if (ns <= 1) return;
-    const size_t base = ((size_t)s * p.hq + h) * p.num_splits;
+    const size_t base = ((size_t)wi * p.hq + h) * p.num_splits;
     float M = -INFINITY;
     for (int i = 0; i < ns; ++i) M = fmaxf(M, p.part_ml[(base + i) * 2]);
     float Ls = 0.f;
@@ -525,7 +559,7 @@ cudaError_t launch_one(const CUtensorMap &km, const CUtensorMap &vm, const Decod
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    dim3 grid(p.num_splits, p.hkv, p.num_seqs);
+    dim3 grid(p.num_splits, p.hkv, p.row_mode ? p.total_rows : p.num_seqs);
     return pkv_host::launch_pdl(decode_kernel<FP8, NT>, grid, dim3(THREADS), Geo<FP8>::SMEM, st, km, vm, p);
 }
 
@@ -549,15 +583,39 @@ void plan_splits(int32_t max_blocks, int32_t num_splits, int32_t *part_blocks, i
     *splits = (max_blocks + pb - 1) / pb;
 }
 
+// Row mode (every query row of a mixed batch a problem of its own): there are
+// as many problems as rows, so partitions need not add parallelism; they are
+// ROW_PART_BLOCKS blocks (16,384 keys) long, whatever the caller asked for.
+constexpr int32_t ROW_PART_BLOCKS = 1024;
+
+void plan_rows(int32_t max_blocks, int32_t *part_blocks, int32_t *splits)
+{
+    *part_blocks = std::min(max_blocks, ROW_PART_BLOCKS);
+    *splits = (max_blocks + *part_blocks - 1) / *part_blocks;
+}
+
+static size_t partial_bytes(int32_t problems, int32_t hq, int32_t splits)
+{
+    if (splits <= 1) return 0;
+    size_t n = (size_t)problems * hq * splits;
+    size_t bytes = n * D * sizeof(float) + n * 2 * sizeof(float);
+    return (bytes + 255) & ~size_t(255);
+}
+
 size_t workspace_bytes(int32_t num_seqs, int32_t hq, int32_t max_blocks, int32_t num_splits)
 {
     if (num_seqs < 1 || hq < 1 || max_blocks < 1) return 0;
     int32_t pb, s;
     plan_splits(max_blocks, num_splits, &pb, &s);
-    if (s <= 1) return 0;
-    size_t n = (size_t)num_seqs * hq * s;
-    size_t bytes = n * D * sizeof(float) + n * 2 * sizeof(float);
-    return (bytes + 255) & ~size_t(255);
+    return partial_bytes(num_seqs, hq, s);
+}
+
+size_t workspace_bytes_rows(int32_t total_rows, int32_t hq, int32_t max_blocks)
+{
+    if (total_rows < 1 || hq < 1 || max_blocks < 1) return 0;
+    int32_t pb, s;
+    plan_rows(max_blocks, &pb, &s);
+    return partial_bytes(total_rows, hq, s);
 }
 
 bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int32_t hkv,
@@ -576,13 +634,19 @@ bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int
 }
 
 // Validates host-visible arguments shared by decode and the decode rows of a
-// mixed batch, then launches decode (+ reduce).
+// mixed batch, then launches decode (+ reduce).  row_mode (needs cu_q_lens):
+// every row of the batch, chunk rows included, is a decode problem over the
+// keys it may see.
 kv_status run(float *out, const void *q, const void *k_cache, const void *v_cache,
               const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
               const int32_t *cu_q_lens, int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t hkv,
               int32_t num_blocks, float scale, kv_dtype dt, const float *k_scale, const float *v_scale,
-              int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st)
+              int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st,
+              bool row_mode)
 {
+    if (row_mode && (!cu_q_lens || total_rows < 0)) return KV_ERR_INVALID;
+    if (row_mode && total_rows == 0) return KV_OK;
+    if (row_mode && total_rows > 65535) return KV_ERR_UNSUPPORTED;
     if (num_seqs == 0) return KV_OK;
     if (num_seqs < 0 || hq < 1 || hkv < 1 || num_blocks < 1 || max_blocks < 1) return KV_ERR_INVALID;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return KV_ERR_INVALID;
@@ -603,6 +667,7 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     p.context_lens = context_lens;
     p.cu_q_lens = cu_q_lens;
     p.total_rows = cu_q_lens ? total_rows : num_seqs;
+    p.row_mode = row_mode ? 1 : 0;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     p.max_blocks = max_blocks;
@@ -612,13 +677,16 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     p.group = G;
     p.num_blocks = num_blocks;
     p.scale_log2 = scale * LOG2E;
-    plan_splits(max_blocks, num_splits, &p.part_blocks, &p.num_splits);
+    if (row_mode) plan_rows(max_blocks, &p.part_blocks, &p.num_splits);
+    else plan_splits(max_blocks, num_splits, &p.part_blocks, &p.num_splits);
     if (p.num_splits > 65535) return KV_ERR_UNSUPPORTED;
-    const size_t need = workspace_bytes(num_seqs, hq, max_blocks, num_splits);
+    const int32_t problems = row_mode ? total_rows : num_seqs;
+    const size_t need = row_mode ? workspace_bytes_rows(total_rows, hq, max_blocks)
+                                 : workspace_bytes(num_seqs, hq, max_blocks, num_splits);
     if (need) {
         if (!workspace || workspace_bytes_given < need || !pkv_host::aligned(workspace, 256))
             return KV_ERR_INVALID;
-        const size_t n = (size_t)num_seqs * hq * p.num_splits;
+        const size_t n = (size_t)problems * hq * p.num_splits;
         p.part_o = static_cast<float *>(workspace);
         p.part_ml = p.part_o + n * D;
     }
@@ -629,8 +697,9 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     else e = G == 16 ? launch_one<true, 2>(km, vm, p, st) : launch_one<true, 1>(km, vm, p, st);
     if (e != cudaSuccess) return KV_ERR_CUDA;
     if (p.num_splits > 1) {
-        const int warps = num_seqs * hq;
-        if (pkv_host::launch_pdl(reduce_kernel, dim3((warps + 3) / 4), dim3(128), 0, st, p) != cudaSuccess)
+        const int64_t warps = (int64_t)problems * hq;
+        if (pkv_host::launch_pdl(reduce_kernel, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, st, p) !=
+            cudaSuccess)
             return KV_ERR_CUDA;
     }
     return KV_OK;
@@ -665,7 +734,7 @@ kv_status paged_attention_decode(float *out, const void *q, const void *k_cache,
     return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            nullptr, num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                            k_scale, v_scale, num_splits, workspace, workspace_bytes,
-                           static_cast<cudaStream_t>(stream));
+                           static_cast<cudaStream_t>(stream), false);
 }
 
 }  // extern "C"
@@ -731,7 +800,7 @@ kv_status paged_attention_decode_static_scratch(float *out, const void *q, const
     return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            nullptr, num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                            k_scale, v_scale, num_splits, scratch, need ? STATIC_SCRATCH_BYTES : 0,
-                           static_cast<cudaStream_t>(stream));
+                           static_cast<cudaStream_t>(stream), false);
 }
 
 }  // extern "C"

@@ -9,32 +9,40 @@
 // prefill vs decode (a) prefill is a dense O(N^2) contraction, (e) chunked
 // prefill.  Rows with n = 1 are decode rows and go to the decode kernel.
 //
-// Tensor-core kernel, one CTA per (pair of 128-row query tiles, KV head, KV
-// partition):
+// Tensor-core kernel (bf16 cache), one CTA per (pair of 128-row query tiles,
+// KV head, 16,384-key partition):
 //  * A query tile packs 128/G chunk tokens x the G query heads of one KV head
 //    (row = token * G + head), so every K/V tile is shared by the whole GQA
-//    group; the two tiles of a pair share every K/V tile as well.
+//    group; the two tiles of a pair share every K/V tile as well.  Both Q tiles
+//    land in shared memory with one 3-D TMA load each.
 //  * K/V tiles of 64 keys = 4 physical blocks, gathered through the block
-//    table by 2-D TMA loads (128-byte swizzle) into a 6-stage ring.
-//  * S[128x64] = Q K^T and O[128x128] += P V run as tcgen05.mma (K=16 steps)
-//    issued by one thread per query tile.  The A operands (Q, written once, and P) are read
-//    from tensor memory, so shared memory only streams K and V -- with A from
-//    shared memory these narrow products were bound by shared-memory
-//    bandwidth, not by the tensor cores.  Accumulators live in tensor memory
-//    too: per query tile Q 64 columns, S 64 (P overwrites its first 32 with
-//    bf16 pairs), O 128.  K is the K-major B operand of the first product, V
-//    the MN-major B operand of the second, straight from the same tiles.
-//  * Two softmax warpgroups, one per query tile, own one TMEM lane (= one query
-//    row) per thread.  They read S with tcgen05.ld, apply the causal mask on
-//    diagonal tiles, keep the online max / normaliser ("FlashAttention"
-//    section: running max and normaliser per block), write P, and rescale O in
-//    tensor memory only when the running max grew by more than 2^8 (otherwise
-//    the stale max is kept; exact in the end).  Each tile has its own MMA
-//    issuer, so one group's softmax overlaps the other group's tensor-core
-//    work; descriptors are precomputed so the issuers keep up with the
-//    tensor cores even for the 64-wide products.
+//    table by 2-D TMA loads (128-byte swizzle) into a 4-stage ring (warp 8).
+//  * S[128x64] = Q K^T and O[128x128] += P V run as tcgen05.mma (K=16 steps),
+//    one issuing warp per query tile (warps 9 and 10).  S is double-buffered
+//    per tile in tensor memory, so QK^T of tile j+2 runs while the softmax
+//    works on tile j.  P (bf16) is written over its S buffer and read by the
+//    second product as the A operand straight from tensor memory; K is the
+//    K-major B operand of the first product, V the MN-major B operand of the
+//    second, both from the same shared-memory stage.  Tensor memory: S 2 x 64
+//    columns and O 128 columns per query tile, 512 in all.
+//  * Two softmax warpgroups (warps 0-7), one per query tile, own one TMEM lane
+//    (= one query row) per thread.  They read S with tcgen05.ld, apply the
+//    causal mask on diagonal tiles, keep the online max / normaliser
+//    ("FlashAttention" section: running max and normaliser per block) on
+//    packed fp32 pairs, write P, and rescale O in tensor memory only when the
+//    running max grew by more than 2^8 (otherwise the stale max is kept; exact
+//    in the end).
+//  * Keys at or past the context end inside the last tile are masked in S; the
+//    producer zeroes their V rows after the load lands (0 x garbage could be
+//    NaN), signalled on its own barrier.
 //  * Long contexts are cut into 16,384-key partitions of whole tiles, merged
 //    by a fixed-order log-sum-exp kernel (no atomics).
+//  * Decode rows (n = 1) of the batch run on a library-owned side stream in
+//    the decode kernel, concurrently with the chunk tiles.
+//
+// fp8 cache with chunks: each row of the batch becomes a decode problem of its
+// own in the decode kernel (its keys 0 .. L-n+i), which widens e4m3 exactly in
+// registers; a tcgen05 kind::f8f6f4 variant of this kernel is not built.
 #include "common.cuh"
 
 #include <algorithm>
@@ -552,8 +560,10 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
               const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
               const int32_t *cu_q_lens, int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t hkv,
               int32_t num_blocks, float scale, kv_dtype dt, const float *k_scale, const float *v_scale,
-              int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st);
+              int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st,
+              bool row_mode);
 size_t workspace_bytes(int32_t num_seqs, int32_t hq, int32_t max_blocks, int32_t num_splits);
+size_t workspace_bytes_rows(int32_t total_rows, int32_t hq, int32_t max_blocks);
 bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int32_t hkv, kv_dtype dt,
                CUtensorMap *km, CUtensorMap *vm);
 }  // namespace pkv_decode
@@ -577,6 +587,14 @@ Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq,
     if (max_q_len >= 2) off += up((size_t)(num_seqs + 1) * sizeof(int32_t));
     pl.total = off;
     return pl;
+}
+
+// Workspace of an fp8 batch with chunks: every row is a decode problem with
+// partitions as long as the chunk kernel's, so this never exceeds make_plan's
+// total for the same shape (the size query serves both dtypes).
+size_t rows_bytes(int32_t total_q, int32_t hq, int32_t max_blocks)
+{
+    return pkv_decode::workspace_bytes_rows(total_q, hq, max_blocks);
 }
 }  // namespace
 
@@ -628,7 +646,8 @@ size_t paged_attention_chunked_prefill_workspace_size(int32_t num_seqs, int32_t 
     (void)num_kv_heads;
     if (num_seqs < 1 || total_q_tokens < 1 || max_q_len < 1 || num_q_heads < 1 || max_blocks_per_seq < 1)
         return 0;
-    return make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, max_blocks_per_seq, num_splits).total;
+    const size_t t = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, max_blocks_per_seq, num_splits).total;
+    return max_q_len >= 2 ? std::max(t, rows_bytes(total_q_tokens, num_q_heads, max_blocks_per_seq)) : t;
 }
 
 kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32_t *cu_q_lens,
@@ -650,18 +669,25 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     const int G = num_q_heads / num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return KV_ERR_UNSUPPORTED;
     if (dtype != KV_BF16 && dtype != KV_FP8_E4M3) return KV_ERR_UNSUPPORTED;
-    if (max_q_len >= 2 && dtype != KV_BF16) return KV_ERR_UNSUPPORTED;   // fp8 chunks: not in this build
     if (!(scale > 0.f) || num_seqs > 65535 || num_kv_heads > 65535) return KV_ERR_INVALID;
     if (!pkv_host::aligned(out, 16) || !pkv_host::aligned(q, 16)) return KV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (max_q_len >= 2 && dtype == KV_FP8_E4M3) {
+        // fp8 cache with chunks: every row (chunk or decode) goes through the
+        // decode kernel as a problem of its own, over the keys it may see
+        return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
+                               total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
+                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, true);
+    }
     const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, max_blocks_per_seq, num_splits);
     if (pl.total && (!workspace || workspace_bytes < pl.total || !pkv_host::aligned(workspace, 256)))
         return KV_ERR_INVALID;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     auto decode_rows = [&](cudaStream_t on) {
         return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
-                               k_scale, v_scale, num_splits, pl.decode_bytes ? ws : nullptr, pl.decode_bytes, on);
+                               k_scale, v_scale, num_splits, pl.decode_bytes ? ws : nullptr, pl.decode_bytes, on,
+                               false);
     };
     if (max_q_len < 2) return decode_rows(st);   // decode rows only
     // decode rows (n = 1) on the side stream, forked from and joined into the

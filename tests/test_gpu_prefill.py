@@ -1,6 +1,6 @@
 """GPU parity of the mixed chunked-prefill / decode call against the fp64 oracle
-(max-abs 1e-2 for the bf16 cache), bitwise permutation invariance, and the
-full-size mixed workload on sampled rows."""
+(max-abs 1e-2 for the bf16 cache, 5e-2 for fp8), bitwise permutation
+invariance, and the full-size mixed workload on sampled rows."""
 import numpy as np
 import pytest
 
@@ -65,12 +65,35 @@ def test_prefill_unwritten_slots_never_leak():
     assert np.array_equal(clean, dirty)
 
 
-def test_fp8_chunks_are_refused():
-    wl = small_workload(960, lens=[40, 40], q_lens=[4, 1], hq=8, hkv=2, kv_dtype="fp8")
-    dw = DeviceWorkload(wl)
-    with pytest.raises(pkv.KVError) as e:
-        dw.attention()
-    assert e.value.status == 3
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (16, 2), (32, 2)])
+def test_fp8_mixed_batch_small(hq, hkv):
+    """fp8 cache with chunks: every row is its own decode problem over keys 0 .. L-n+i."""
+    lens = [1, 2, 20, 300, 64, 700, 129]
+    qlens = [1, 2, 17, 1, 64, 130, 129]
+    wl = small_workload(960 + hq, lens=lens, q_lens=qlens, hq=hq, hkv=hkv, kv_dtype="fp8")
+    _, _, ref = expected_full(wl)
+    _, got = _run(wl)
+    err = max_abs(got, ref)
+    assert err <= TOL["fp8"], err
+
+
+def test_fp8_chunk_spanning_several_partitions():
+    wl = small_workload(970, lens=[40000, 33], q_lens=[40, 1], hq=16, hkv=2, kv_dtype="fp8")
+    _, got = _run(wl)
+    cu = wl.cu_q_lens
+    for s in range(2):
+        err = max_abs(got[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s))
+        assert err <= TOL["fp8"], (s, err)
+
+
+def test_fp8_chunks_bitwise_identical_under_block_permutation_and_poison():
+    outs = []
+    for perm_seed, poison in ((1, False), (2, True)):
+        wl = small_workload(980, lens=[500, 37, 20000], q_lens=[130, 1, 77], hq=8, hkv=1, kv_dtype="fp8")
+        wl.free_order = np.random.default_rng(perm_seed).permutation(wl.num_blocks).astype(np.int32)
+        outs.append(_run(wl, poison=poison)[1])
+    assert np.isfinite(outs[1]).all()
+    assert np.array_equal(outs[0], outs[1])
 
 
 def test_mixed_prefill_workload_sampled():
