@@ -412,6 +412,197 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------------------------------ swap
+SWAP_METRIC = "KV block swap over the host link: GB/s moved (swap-out + swap-in of 1.07 GB)"
+
+
+def _link_peaks(torch, dev, nbytes, reps=5):
+    """Measured copy-engine bandwidth of one contiguous pinned host <-> device
+    copy of nbytes each way (best of reps), in GB/s."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev)
+    out = {}
+    for name, fn in (("d2h", lambda: h.copy_(d, non_blocking=True)), ("h2d", lambda: d.copy_(h, non_blocking=True))):
+        best = None
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            torch.cuda.synchronize(dev)
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        out[name] = nbytes / (best * 1e-3) / 1e9
+    del h, d
+    return out
+
+
+def run_swap(args):
+    """One step = swap-out of 16,384 (block, all 8 KV heads) bf16 blocks of K and
+    V (1.07 GB, the page's preempted request) from a 32,768-block pool to pinned
+    host memory, then swap-in of the same bytes into 16,384 other blocks."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_263_gb300 as pkv
+    from paged_kv_cache_263_gb300 import build as pkv_build
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkv_build.build()
+    NB, HKV, N = 32768, 8, 16384
+    rng = np.random.Generator(np.random.PCG64(2636 + rank))
+    perm = rng.permutation(NB).astype(np.int32)
+    out_ids = torch.from_numpy(perm[:N].copy()).to(dev)
+    in_ids = torch.from_numpy(perm[N:].copy()).to(dev)
+    k = torch.empty((NB, HKV, 16, 128), dtype=torch.bfloat16, device=dev).normal_()
+    v = torch.empty_like(k).normal_()
+    hk = torch.empty((N, HKV, 16, 128), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    moved = 2 * N * HKV * 16 * 128 * 2                       # bytes of one direction (K + V)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # correctness of the timed configuration before timing: a sample of blocks
+    pkv.kv_swap_out(k, v, out_ids, hk, hv)
+    pkv.kv_swap_in(k, v, in_ids, hk, hv)
+    torch.cuda.synchronize(dev)
+    if pkv.kv_last_device_status() != 0:
+        raise RuntimeError("device status after swap")
+    for j in (0, 1, N // 2, N - 1):
+        a, b = int(perm[j]), int(perm[N + j])
+        if not (torch.equal(k[a], k[b]) and torch.equal(v[a], v[b]) and torch.equal(hk[j], k[a].cpu())):
+            raise RuntimeError(f"swap mismatch at {j}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = Clocks(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        pkv.kv_swap_out(k, v, out_ids, hk, hv)
+        pkv.kv_swap_in(k, v, in_ids, hk, hv)
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        pkv.kv_swap_out(k, v, out_ids, hk, hv)
+        ev[i][1].record(stream)
+        pkv.kv_swap_in(k, v, in_ids, hk, hv)
+        ev[i][2].record(stream)
+    t1.record(stream)
+    barrier()
+    ck = clocks.stop()
+    ms_step = max_over_ranks(t0.elapsed_time(t1) / K, dev)
+    out_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    in_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+
+    # end to end: the block ids come from the host scheduler each step
+    h_out = torch.from_numpy(perm[:N].copy()).pin_memory()
+    h_in = torch.from_numpy(perm[N:].copy()).pin_memory()
+    E = max(3, min(K, 20))
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        out_ids.copy_(h_out, non_blocking=True)
+        in_ids.copy_(h_in, non_blocking=True)
+        pkv.kv_swap_out(k, v, out_ids, hk, hv)
+        pkv.kv_swap_in(k, v, in_ids, hk, hv)
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, dev)
+
+    link = _link_peaks(torch, dev, moved)
+    out_gbs = moved / (out_ms * 1e-3) / 1e9
+    in_gbs = moved / (in_ms * 1e-3) / 1e9
+    peak = min(link["d2h"], link["h2d"])
+    achieved = 2 * moved / ((out_ms + in_ms) * 1e-3) / 1e9
+    line = {
+        "metric": SWAP_METRIC, "value": weak_scaling_value(2 * moved, ws, ms_step), "unit": "GB/s",
+        "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bytes moved)",
+        "data": "synthetic",
+        "config": {"workload": "swap", "pool_blocks": NB, "num_kv_heads": HKV, "blocks_per_direction": N,
+                   "bytes_per_direction": moved, "host_memory": "pinned (cudaHostAlloc via torch)",
+                   "l2": "no flush: 1.07 GB each way, 8x the 129 MB L2",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "swap_out": {"ms": out_ms, "GB/s": out_gbs}, "swap_in": {"ms": in_ms, "GB/s": in_gbs},
+        "roofline": {"bound": "host link", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": "measured live: one contiguous pinned copy of "
+                     "the same bytes each way by the copy engine (d2h %.1f, h2d %.1f GB/s); lower of the two"
+                     % (link["d2h"], link["h2d"]),
+                     "kernel": "swap_kernel (out and in)", "bytes_per_launch": moved,
+                     "avg_launch_ms": (out_ms + in_ms) / 2, "traffic": None},
+        "e2e": {"value": weak_scaling_value(2 * moved, ws, e2e_ms), "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": moved + 2 * N * 4, "d2h_bytes_per_step": moved},
+        "gpu_launches": 2 * K,
+        "clocks": ck,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = _swap_cpu_baseline(args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def _swap_cpu_baseline(budget_s):
+    """The swap oracle (numpy gather of the listed blocks, then scatter into
+    others) on host arrays: 2,048 of the 16,384 blocks, 134 MB each way."""
+    import numpy as np
+    from oracle.swap import swap_in as o_in, swap_out as o_out
+    rng = np.random.Generator(np.random.PCG64(2636))
+    NB, HKV, N = 4096, 8, 2048
+    k = rng.integers(0, 1 << 16, size=(NB, HKV, 16, 128), dtype=np.uint16)
+    v = rng.integers(0, 1 << 16, size=(NB, HKV, 16, 128), dtype=np.uint16)
+    perm = rng.permutation(NB)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        hk, hv = o_out(k, v, perm[:N])
+        o_in(k, v, perm[N:], hk, hv)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    moved = 2 * 2 * N * HKV * 16 * 128 * 2
+    return {"value": moved * reps / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{N} of 16,384 blocks each way (numpy gather/scatter), {reps} round trips in {el:.1f} s"}
+
+
+def run_swap_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    steps = []
+    for _ in range(args.warmup):
+        _swap_cpu_baseline(0.0)
+    for _ in range(args.steps):
+        steps.append(_swap_cpu_baseline(0.0))
+    v = statistics.mean(s["value"] for s in steps)
+    line = {"impl": "reference", "metric": SWAP_METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bytes", "data": "synthetic",
+            "config": {"workload": "swap", "sample": steps[0]["sample"], "device": "host cores"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": steps[0]["sample"]},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -426,6 +617,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload == "swap":
+        return run_swap_reference(args) if args.impl == "reference" else run_swap(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

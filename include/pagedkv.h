@@ -147,6 +147,78 @@ PAGEDKV_API kv_status kv_pool_stats(const kv_pool *pool, kv_pool_stats_t *out);
 PAGEDKV_API kv_status kv_pool_fail_alloc_after(kv_pool *pool, int32_t k);
 
 /* ------------------------------------------------------------------------
+ * Prefix cache: keeps the full blocks of finished requests so that a later
+ * request starting with the same tokens reuses their K/V instead of
+ * prefilling them again ([P1] opening section: hash the prefix, reuse the
+ * computed blocks across requests; [P2] "Block sharing versus prefix
+ * caching?", "SGLang -- RadixAttention": finished requests' cache filed in a
+ * tree of shared beginnings, LRU eviction; [P3] block management (h)(ii)).
+ *
+ *  - Matching is on exact token ids, block-aligned, from the very start
+ *    ([P2] "Why does my prefix cache hit rate not match what I expect?"): the
+ *    cached block j of a sequence stands for tokens[0 .. 16(j+1)) under a
+ *    tenant key `salt` ([P2] "The isolation question": key the cache per
+ *    tenant).  Only full 16-token blocks are cached.  Lookup hashes the chain
+ *    block by block; every candidate is then compared token by token with its
+ *    parent identity, so a hash collision never returns a wrong block.
+ *  - The cache holds one pool reference per cached block.  Blocks form a tree
+ *    (block j's parent is block j-1 of the same prefix).  Eviction frees, one
+ *    at a time, the least recently used leaf that only the cache holds
+ *    (refcount 1); recency is a clock advanced once per match or insert and
+ *    stamped on every block the call touches (ties: the block cached first).
+ *  - Host only; all calls on one cache are serialised by its mutex.  The pool
+ *    must outlive the cache.
+ * ---------------------------------------------------------------------- */
+typedef struct kv_prefix_cache kv_prefix_cache; /* opaque, host-only */
+
+typedef struct {
+    int64_t lookups;          /* kv_prefix_match calls */
+    int64_t query_blocks;     /* full blocks asked for by those calls */
+    int64_t hit_blocks;       /* full blocks they returned */
+    int64_t inserted_blocks;  /* blocks newly cached */
+    int64_t evicted_blocks;   /* blocks freed by eviction */
+    int32_t cached_blocks;    /* blocks the cache holds now */
+    int32_t evictable_blocks; /* of those, how many repeated eviction could free now */
+} kv_prefix_stats_t;
+
+/* Creates an empty cache over `pool` (not NULL). */
+PAGEDKV_API kv_status kv_prefix_cache_create(kv_pool *pool, kv_prefix_cache **out);
+
+/* Drops the cache's reference on every cached block, then frees the cache. */
+PAGEDKV_API void kv_prefix_cache_destroy(kv_prefix_cache *cache);
+
+/* Longest run of cached blocks matching tokens[0 .. n_tokens) from the start
+ * under `salt`, at most max_blocks of them: their ids go to out_block_ids
+ * (capacity max_blocks), their count to *out_n_blocks.  The caller receives one
+ * pool reference per returned block (drop it with kv_block_free).  The blocks
+ * returned are marked used now. */
+PAGEDKV_API kv_status kv_prefix_match(kv_prefix_cache *cache, const int32_t *tokens, int32_t n_tokens,
+                                      uint64_t salt, int32_t max_blocks, int32_t *out_block_ids,
+                                      int32_t *out_n_blocks);
+
+/* Caches the full blocks of a sequence: block j (j < min(n_tokens / 16,
+ * n_blocks)) holds tokens[16j .. 16j+15] in physical block block_ids[j], whose
+ * K/V the caller has written.  Every listed block must be live (KV_ERR_INVALID,
+ * nothing changes, otherwise).  A block whose prefix is already cached keeps the
+ * cached copy (marked used now); a new one gets one pool reference held by the
+ * cache.  *out_n_new (nullable) = blocks newly cached. */
+PAGEDKV_API kv_status kv_prefix_insert(kv_prefix_cache *cache, const int32_t *tokens, int32_t n_tokens,
+                                       uint64_t salt, const int32_t *block_ids, int32_t n_blocks,
+                                       int32_t *out_n_new);
+
+/* Evicts up to n blocks (least recently used evictable leaf first), returning
+ * them to the pool; their ids go to out_ids (nullable, capacity n) in eviction
+ * order, their count to *out_n (nullable). */
+PAGEDKV_API kv_status kv_prefix_evict(kv_prefix_cache *cache, int32_t n, int32_t *out_ids, int32_t *out_n);
+
+/* kv_block_alloc on the cache's pool after evicting as many cached blocks as
+ * the free list is short of n.  If the pool is still short the call fails with
+ * KV_ERR_OUT_OF_BLOCKS; evictions it made stand. */
+PAGEDKV_API kv_status kv_prefix_alloc(kv_prefix_cache *cache, int32_t n, int32_t *out_ids);
+
+PAGEDKV_API kv_status kv_prefix_stats(const kv_prefix_cache *cache, kv_prefix_stats_t *out);
+
+/* ------------------------------------------------------------------------
  * Cache write ("blocks allocated on demand as a sequence grows" [P1]
  * "PagedAttention: an OS idea"; [P3] block management (c)).
  *  k, v          device, bf16 [num_tokens][num_kv_heads][128]
@@ -264,6 +336,34 @@ PAGEDKV_API kv_status paged_attention_chunked_prefill(float *out, const void *q,
                                           const float *k_scale, const float *v_scale,
                                           int32_t num_splits, void *workspace,
                                           size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Swap of KV blocks to host memory and back ([P2] "When it runs out anyway":
+ * ship a preempted request's blocks over the host link and bring them back;
+ * [P3] block management (f) preemption, swap out to CPU).
+ *
+ *  kv_swap_out copies, for i < n, every (block, KV head) tile of K and V of
+ *  block block_ids[i] to host_k[i] / host_v[i]; kv_swap_in copies host_k[i] /
+ *  host_v[i] into block block_ids[i] (the ids of a swap-in must be distinct; the
+ *  blocks may differ from the ones swapped out -- rewrite the block table).
+ *
+ *  k_cache/v_cache  device, the pool layout above, num_blocks blocks
+ *  block_ids        device int32 [n]; an id outside 0..num_blocks-1 is skipped
+ *                   and flagged (KV_ERR_DEVICE_BOUNDS, flag 1)
+ *  host_k/host_v    page-locked host memory the device can address
+ *                   (cudaHostAlloc / cudaHostRegister), each
+ *                   n x num_kv_heads x 16 x 128 elements of the cache dtype in
+ *                   list order, 16-byte aligned; other memory -> KV_ERR_INVALID
+ *  One kernel on `stream` moves the data over the host link; the host buffers
+ *  must stay valid until the stream has passed it.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API kv_status kv_swap_out(const void *k_cache, const void *v_cache, int32_t num_blocks,
+                                  int32_t num_kv_heads, kv_dtype dtype, const int32_t *block_ids, int32_t n,
+                                  void *host_k, void *host_v, void *stream);
+
+PAGEDKV_API kv_status kv_swap_in(void *k_cache, void *v_cache, int32_t num_blocks, int32_t num_kv_heads,
+                                 kv_dtype dtype, const int32_t *block_ids, int32_t n, const void *host_k,
+                                 const void *host_v, void *stream);
 
 /* Waits for `stream`, then returns and clears the sticky device status word
  * set by earlier calls (KV_OK or KV_ERR_DEVICE_BOUNDS); KV_ERR_CUDA if the

@@ -18,7 +18,7 @@ __all__ = [
     "paged_attention_workspace_size", "paged_attention_decode",
     "paged_attention_chunked_prefill_workspace_size", "paged_attention_chunked_prefill",
     "kv_last_device_status", "kv_last_device_status_flags", "KV_BF16", "KV_FP8_E4M3",
-    "HEAD_DIM", "BLOCK_SIZE", "library_path",
+    "HEAD_DIM", "BLOCK_SIZE", "library_path", "PrefixCache", "kv_swap_out", "kv_swap_in",
 ]
 
 HEAD_DIM = 128
@@ -44,6 +44,13 @@ class _Stats(ctypes.Structure):
                 ("cow_copies", ctypes.c_int64), ("alloc_failures", ctypes.c_int64)]
 
 
+class _PrefixStats(ctypes.Structure):
+    _fields_ = [("lookups", ctypes.c_int64), ("query_blocks", ctypes.c_int64),
+                ("hit_blocks", ctypes.c_int64), ("inserted_blocks", ctypes.c_int64),
+                ("evicted_blocks", ctypes.c_int64), ("cached_blocks", ctypes.c_int32),
+                ("evictable_blocks", ctypes.c_int32)]
+
+
 def lib():
     """The loaded library; raises if it has not been built."""
     global _lib
@@ -64,6 +71,13 @@ def lib():
             "kv_block_refcount": (c.c_int, [P, I, c.POINTER(I)]),
             "kv_pool_stats": (c.c_int, [P, c.POINTER(_Stats)]),
             "kv_pool_fail_alloc_after": (c.c_int, [P, I]),
+            "kv_prefix_cache_create": (c.c_int, [P, c.POINTER(P)]),
+            "kv_prefix_cache_destroy": (None, [P]),
+            "kv_prefix_match": (c.c_int, [P, P, I, c.c_uint64, I, P, c.POINTER(I)]),
+            "kv_prefix_insert": (c.c_int, [P, P, I, c.c_uint64, P, I, c.POINTER(I)]),
+            "kv_prefix_evict": (c.c_int, [P, I, P, c.POINTER(I)]),
+            "kv_prefix_alloc": (c.c_int, [P, I, P]),
+            "kv_prefix_stats": (c.c_int, [P, c.POINTER(_PrefixStats)]),
             "reshape_and_cache": (c.c_int, [P, P, P, P, P, I, I, I, c.c_int, P, P, P]),
             "paged_attention_workspace_size": (SZ, [I, I, I, I]),
             "paged_attention_decode": (c.c_int, [P, P, P, P, P, I, P, I, I, I, I, F, c.c_int, P, P,
@@ -74,6 +88,8 @@ def lib():
             "paged_attention_decode_static_scratch_bytes": (SZ, []),
             "paged_attention_decode_static_scratch": (c.c_int, [P, P, P, P, P, I, P, I, I, I, I, F, c.c_int, P,
                                                                 P, I, P]),
+            "kv_swap_out": (c.c_int, [P, P, I, I, c.c_int, P, I, P, P, P]),
+            "kv_swap_in": (c.c_int, [P, P, I, I, c.c_int, P, I, P, P, P]),
             "kv_last_device_status": (c.c_int, [P]),
             "kv_last_device_status_flags": (c.c_uint32, []),
         }
@@ -200,6 +216,73 @@ class KVPool:
         _check(lib().kv_pool_fail_alloc_after(self._p, int(k)), "kv_pool_fail_alloc_after")
 
 
+class PrefixCache:
+    """Block-hash prefix cache over a KVPool (kept alive by this object): exact,
+    block-aligned matching from the first token under a tenant key, LRU
+    eviction of leaves that only the cache holds."""
+
+    def __init__(self, pool: KVPool):
+        self.pool = pool
+        self._c = ctypes.c_void_p()
+        _check(lib().kv_prefix_cache_create(pool._p, ctypes.byref(self._c)), "kv_prefix_cache_create")
+
+    def close(self):
+        if self._c:
+            lib().kv_prefix_cache_destroy(self._c)
+            self._c = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _tokens(tokens):
+        import numpy as np
+        return np.ascontiguousarray(tokens, dtype=np.int32)
+
+    def match(self, tokens, salt: int = 0, max_blocks=None):
+        """Ids of the longest cached prefix (one reference each for the caller)."""
+        import numpy as np
+        t = self._tokens(tokens)
+        cap = t.size // BLOCK_SIZE if max_blocks is None else int(max_blocks)
+        out = np.empty(max(cap, 0), dtype=np.int32)
+        n = ctypes.c_int32()
+        _check(lib().kv_prefix_match(self._c, t.ctypes.data_as(ctypes.c_void_p), t.size, int(salt) & (2**64 - 1),
+                                     cap, out.ctypes.data_as(ctypes.c_void_p), ctypes.byref(n)), "kv_prefix_match")
+        return out[:n.value]
+
+    def insert(self, tokens, block_ids, salt: int = 0) -> int:
+        import numpy as np
+        t = self._tokens(tokens)
+        b = np.ascontiguousarray(block_ids, dtype=np.int32)
+        n = ctypes.c_int32()
+        _check(lib().kv_prefix_insert(self._c, t.ctypes.data_as(ctypes.c_void_p), t.size, int(salt) & (2**64 - 1),
+                                      b.ctypes.data_as(ctypes.c_void_p), b.size, ctypes.byref(n)),
+               "kv_prefix_insert")
+        return int(n.value)
+
+    def evict(self, n: int):
+        import numpy as np
+        out = np.empty(max(int(n), 0), dtype=np.int32)
+        k = ctypes.c_int32()
+        _check(lib().kv_prefix_evict(self._c, int(n), out.ctypes.data_as(ctypes.c_void_p), ctypes.byref(k)),
+               "kv_prefix_evict")
+        return out[:k.value]
+
+    def alloc(self, n: int):
+        import numpy as np
+        out = np.empty(max(int(n), 0), dtype=np.int32)
+        _check(lib().kv_prefix_alloc(self._c, int(n), out.ctypes.data_as(ctypes.c_void_p)), "kv_prefix_alloc")
+        return out
+
+    def stats(self) -> dict:
+        s = _PrefixStats()
+        _check(lib().kv_prefix_stats(self._c, ctypes.byref(s)), "kv_prefix_stats")
+        return {f: int(getattr(s, f)) for f, _ in _PrefixStats._fields_}
+
+
 # ------------------------------------------------------------------ kernels
 def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None, stream=None):
     """Scatter K/V rows [T][Hkv][128] (bf16) into the paged caches at slot_mapping."""
@@ -308,6 +391,36 @@ def paged_attention_chunked_prefill(out, q, cu_q_lens, context_lens, max_q_len, 
         _ptr(k_scale), _ptr(v_scale), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)),
         "paged_attention_chunked_prefill")
     return out
+
+
+def _swap_args(k_cache, v_cache, block_ids, host_k, host_v):
+    _need(k_cache, "k_cache", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn))
+    _need(v_cache, "v_cache", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn))
+    _need(block_ids, "block_ids", torch.int32)
+    n = block_ids.numel()
+    for name, h in (("host_k", host_k), ("host_v", host_v)):
+        _need(h, name, k_cache.dtype, dev=False)
+        if h.is_cuda or not h.is_pinned():
+            raise ValueError(f"{name} must be pinned host memory")
+        if tuple(h.shape) != (n,) + tuple(k_cache.shape[1:]):
+            raise ValueError(f"{name} must be [n][Hkv][16][128]")
+    return n
+
+
+def kv_swap_out(k_cache, v_cache, block_ids, host_k, host_v, stream=None):
+    """Copy the listed blocks' K/V tiles to pinned host tensors [n][Hkv][16][128]."""
+    n = _swap_args(k_cache, v_cache, block_ids, host_k, host_v)
+    _check(lib().kv_swap_out(_ptr(k_cache), _ptr(v_cache), k_cache.shape[0], k_cache.shape[1],
+                             _cache_dtype(k_cache), _ptr(block_ids), n, _ptr(host_k), _ptr(host_v),
+                             _stream(stream)), "kv_swap_out")
+
+
+def kv_swap_in(k_cache, v_cache, block_ids, host_k, host_v, stream=None):
+    """Copy pinned host tensors [n][Hkv][16][128] into the listed (distinct) blocks."""
+    n = _swap_args(k_cache, v_cache, block_ids, host_k, host_v)
+    _check(lib().kv_swap_in(_ptr(k_cache), _ptr(v_cache), k_cache.shape[0], k_cache.shape[1],
+                            _cache_dtype(k_cache), _ptr(block_ids), n, _ptr(host_k), _ptr(host_v),
+                            _stream(stream)), "kv_swap_in")
 
 
 def kv_last_device_status(stream=None) -> int:

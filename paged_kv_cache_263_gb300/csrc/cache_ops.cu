@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(256)
 
 namespace pkv_decode { uint32_t take_status(); }
 namespace pkv_prefill { uint32_t take_status(); }
+namespace pkv_swap { uint32_t take_status(); }
 
 static uint32_t take_status_cache()
 {
@@ -154,7 +155,8 @@ kv_status reshape_and_cache(const void *k, const void *v, void *k_cache, void *v
 kv_status kv_last_device_status(void *stream)
 {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KV_ERR_CUDA;
-    uint32_t f = take_status_cache() | pkv_decode::take_status() | pkv_prefill::take_status();
+    uint32_t f = take_status_cache() | pkv_decode::take_status() | pkv_prefill::take_status() |
+                 pkv_swap::take_status();
     g_last_flags = f;
     return f ? KV_ERR_DEVICE_BOUNDS : KV_OK;
 }
