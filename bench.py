@@ -260,6 +260,21 @@ def run_reference(args):
     return 0
 
 
+def _launches_per_step(pkv, wl):
+    """Kernels one step launches: the cache write, then the attention call's
+    kernels (decode + optional LSE merge; for a batch with chunks also the
+    tile-count prefix, the chunk kernel and its optional merge; the decode
+    kernel of the batch's one-row sequences always launches)."""
+    mb = wl.max_blocks_per_seq
+    dec_split = pkv.paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, mb, wl.num_splits) > 0
+    n = 1 + 1 + (1 if dec_split else 0)
+    if not wl.is_decode:
+        if wl.kv_dtype == "fp8":           # every row in the decode kernel, 16,384-key partitions
+            return 1 + 1 + (1 if mb > 1024 else 0)
+        n += 2 + (1 if mb * 16 > 16384 else 0)
+    return n
+
+
 # ------------------------------------------------------------------ ours
 def run_ours(args):
     import torch
@@ -360,16 +375,20 @@ def run_ours(args):
     value = weak_scaling_value(step_bytes, ws, ms_per_step)
     attn_bytes = ab["kv_unique"] + ab["q"] + ab["o"] + ab["meta"]
     attn_avg = statistics.mean(attn_ms)
-    if wl.is_decode:
+    hpeak, _ = _peaks()
+    tpeak, tkind = _tensor_peak()
+    # memory-bound unless the chunk rows' flops per byte reach the ridge point
+    hbm_bound = wl.is_decode or prefill_flops(wl) / attn_bytes < tpeak * 1e12 / (hpeak * 1e9)
+    if hbm_bound:
         achieved = attn_bytes / (attn_avg * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "peak_kind": peak_kind,
-                    "kernel": "paged_attention_decode (decode kernel + LSE reduce)",
+                    "kernel": "paged_attention_decode (decode kernel + LSE reduce)" if wl.is_decode else
+                              "paged_attention_chunked_prefill (whole call)",
                     "bytes_per_launch": attn_bytes, "avg_launch_ms": attn_avg,
                     "traffic": _traffic(os.path.join(ROOT, "paged_kv_cache_263_gb300", "csrc", "decode.cu"))
                     if wl.name == "llama8b" else None}
     else:
-        tpeak, tkind = _tensor_peak()
         flops = prefill_flops(wl)
         achieved = flops / (attn_avg * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
@@ -377,9 +396,7 @@ def run_ours(args):
                     "kernel": "paged_attention_chunked_prefill (whole call: chunk tiles on tcgen05 "
                               "+ decode rows + LSE merges), prefill flops only",
                     "flops_per_launch": flops, "avg_launch_ms": attn_avg, "traffic": None}
-    splits_used = pkv.paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, wl.max_blocks_per_seq,
-                                                     wl.num_splits) > 0
-    launches_per_step = 1 + 1 + (1 if splits_used else 0)
+    launches_per_step = _launches_per_step(pkv, wl)
     kv_bytes = ab["kv_unique"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,

@@ -23,6 +23,14 @@ Recipes (the shapes follow Llama-3 layers; "1K" = 1,024 tokens):
 5. ``split_fp8`` 8 sequences of 131,072 tokens; Hq 64, Hkv 8; fp8-e4m3 cache with
                  per-head scales; 16 split-KV partitions.
 
+Further shapes: ``spec_verify`` (64 sequences of the ``llama8b`` recipe, each
+verifying a 4-token draft: 4 causal query rows per sequence) and
+``spec_verify8`` (32 sequences, lengths uniform in [1K, 8K], Hq 64, Hkv 8,
+8-token drafts) -- speculative decoding's verification pass ("M.65 Inference
+serving", speculative decoding: a draft of N = 4-8 tokens verified in one
+forward pass); ``mixed_prefill_small`` (the mixed batch scaled down for
+profiling).
+
 For every sequence the step's "new" tokens (the last ``q_len`` positions) are
 the ones appended by the cache write in the step; all earlier positions are
 written while the workload is set up.
@@ -37,7 +45,7 @@ import torch
 
 from . import IH4_MAX_ABS, normal_bf16, stream_key
 
-__all__ = ["Workload", "make_workload", "WORKLOADS", "small_workload"]
+__all__ = ["Workload", "make_workload", "WORKLOADS", "EXTRA_WORKLOADS", "small_workload"]
 
 Q_STREAM, K_STREAM, V_STREAM = 0, 1, 2
 
@@ -234,10 +242,30 @@ def make_workload(name: str) -> Workload:
         return Workload("split_fp8", seed, 64, 8, pool, "fp8", lens, np.ones(8, np.int32),
                         rng.permutation(pool), num_splits=16,
                         description="long-context split-KV decode, fp8-e4m3 cache, 16 partitions")
+    if name == "spec_verify":
+        # speculative-decoding verification at the Llama-3-8B layer shape: every
+        # sequence checks a 4-token draft in one pass (4 causal query rows)
+        seed = 2637
+        rng = np.random.Generator(np.random.PCG64(seed))
+        lens = rng.integers(512, 4096, size=64, endpoint=True).astype(np.int32)
+        pool = 65536
+        return Workload("spec_verify", seed, 32, 8, pool, "bf16", lens, np.full(64, 4, np.int32),
+                        rng.permutation(pool),
+                        description="speculative verify: 64 sequences x 4 draft tokens, Llama-3-8B layer shape")
+    if name == "spec_verify8":
+        # the same at the Llama-3-70B layer shape with an 8-token draft
+        seed = 2638
+        rng = np.random.Generator(np.random.PCG64(seed))
+        lens = rng.integers(1024, 8192, size=32, endpoint=True).astype(np.int32)
+        pool = _pool_to_fit(lens, 0, -1)
+        return Workload("spec_verify8", seed, 64, 8, pool, "bf16", lens, np.full(32, 8, np.int32),
+                        rng.permutation(pool),
+                        description="speculative verify: 32 sequences x 8 draft tokens, Llama-3-70B layer shape")
     raise KeyError(name)
 
 
 WORKLOADS = ("tiny", "llama8b", "llama70b_prefix", "mixed_prefill", "split_fp8")
+EXTRA_WORKLOADS = ("mixed_prefill_small", "spec_verify", "spec_verify8")
 
 
 def small_workload(seed: int, lens, q_lens=None, hq=8, hkv=2, kv_dtype="bf16", num_blocks=None,

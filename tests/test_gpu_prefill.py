@@ -112,3 +112,24 @@ def test_mixed_prefill_workload_sampled():
     for s in (1, 100, 255):
         err = max_abs(out[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s))
         assert err <= TOL["bf16"], (s, err)
+
+
+@pytest.mark.parametrize("hq,hkv,n", [(32, 8, 4), (64, 8, 8), (16, 2, 6), (8, 8, 5)])
+def test_spec_verify_shapes_small(hq, hkv, n):
+    """Speculative verification: every sequence checks an n-token draft, n causal
+    rows each ("M.65 Inference serving", speculative decoding, N = 4-8)."""
+    lens = [n, 40, 300, 1025, 16, 17, 4096]
+    wl = small_workload(1100 + n, lens=lens, q_lens=[n] * len(lens), hq=hq, hkv=hkv)
+    _, _, ref = expected_full(wl)
+    _, got = _run(wl)
+    assert max_abs(got, ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("name", ["spec_verify", "spec_verify8"])
+def test_spec_verify_workloads_sampled(name):
+    wl = make_workload(name)
+    _, out = _run(wl)
+    cu = wl.cu_q_lens
+    for s in (0, 1, wl.num_seqs // 2, wl.num_seqs - 1):
+        err = max_abs(out[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s))
+        assert err <= TOL["bf16"], (s, err)
