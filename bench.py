@@ -269,6 +269,8 @@ def _launches_per_step(pkv, wl):
     dec_split = pkv.paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, mb, wl.num_splits) > 0
     n = 1 + 1 + (1 if dec_split else 0)
     if not wl.is_decode:
+        if int(wl.q_lens.max()) * wl.group <= 64:     # short chunks: multi-row decode mode only
+            return n
         if wl.kv_dtype == "fp8":           # every row in the decode kernel, 16,384-key partitions
             return 1 + 1 + (1 if mb > 1024 else 0)
         n += 2 + (1 if mb * 16 > 16384 else 0)

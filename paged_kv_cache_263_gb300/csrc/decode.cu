@@ -57,6 +57,7 @@ struct DecodeParams {
     const int32_t *cu_q_lens;  // mixed batches: only sequences with one query row
     int total_rows;            // rows of q/out (mixed batches)
     int row_mode;              // every row of a mixed batch is its own problem (see row_keys)
+    int col_groups;            // multi-row mode: CTAs per (split, KV head, sequence) over the columns
     const float *k_scale;
     const float *v_scale;
     float *part_o;             // [B][Hq][S][128]   (B = rows in row mode)
@@ -102,7 +103,7 @@ __device__ __forceinline__ void flag(uint32_t bits) { atomicOr(&g_status, bits);
 // rows in its chunk and context length L (chunk included), row i = r - cu[seq]
 // of the chunk sees keys 0 .. L - n + i, so the problem has L - n + i + 1 keys.
 // Returns 0 (flagged by the caller as a bad length) for a malformed batch.
-__device__ __forceinline__ int row_keys(const DecodeParams &p, int r, int &seq)
+__device__ __forceinline__ int row_keys(const DecodeParams &p, int r, int &seq, int &L)
 {
     const int32_t *cu = p.cu_q_lens;
     int lo = 0, hi = p.num_seqs;                 // cu[lo] <= r < cu[hi] if well formed
@@ -112,11 +113,13 @@ __device__ __forceinline__ int row_keys(const DecodeParams &p, int r, int &seq)
         else hi = mid;
     }
     seq = lo;
+    L = 0;
     const int a = __ldg(cu + lo), b = __ldg(cu + lo + 1);
     if (r < a || r >= b) return 0;
-    const int n = b - a, L = __ldg(p.context_lens + lo);
-    if (n > L || L > p.max_blocks * BS) return 0;
-    return L - n + (r - a) + 1;
+    const int n = b - a, len = __ldg(p.context_lens + lo);
+    if (n > len || len > p.max_blocks * BS) return 0;
+    L = len;
+    return len - n + (r - a) + 1;
 }
 
 template <bool FP8>
@@ -135,7 +138,13 @@ __device__ __forceinline__ void issue_stage(uint32_t dst, uint32_t bar, const CU
     }
 }
 
-template <bool FP8, int NT>
+// MR (multi-row): one CTA covers CW = 8 NT columns of the (query row, head)
+// pairs of one sequence and one KV head -- the n rows of a chunk x the G heads
+// of the group, column c -> row c / G, head c % G -- so a short chunk (a
+// speculative draft being verified) reads each K/V tile once for all its
+// rows.  Row i of the chunk sees keys 0 .. L-n+i; longer chunks take several
+// column groups (CTAs next to each other in the grid, sharing tiles in L2).
+template <bool FP8, int NT, bool MR>
 __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p)
@@ -146,18 +155,42 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
                                                 ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WARPS * GE::RING);
 
-    const int split = blockIdx.x, g = blockIdx.y;
+    constexpr int CW = NT * 8;               // columns of this CTA
+    const int g = blockIdx.y;
+    int split = blockIdx.x, cg = 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, cq = lane & 3;
     // launched with programmatic serialisation: the CTA may be resident before
     // the previous kernel on the stream (typically the cache write) finished
     griddep_wait();
 
-    // s: sequence (block table); row: row of q/out; wi: index of the partials
-    int s = blockIdx.z, row = s, wi = s, L;
-    if (p.row_mode) {
+    // s: sequence (block table); row: (first) row of q/out; wi: index of the
+    // partials; nq: query rows of the sequence this CTA covers
+    int s = blockIdx.z, row = s, wi = s, L, nq = 1;
+    if constexpr (MR) {
+        cg = split % p.col_groups;
+        split /= p.col_groups;
+        const int a = p.cu_q_lens[s], b = p.cu_q_lens[s + 1];
+        nq = b - a;
+        L = p.context_lens[s];
+        if (nq == 0) return;
+        if (nq < 0 || a < 0 || b > p.total_rows || nq > L || L < 1 || L > p.max_blocks * BS) {
+            if (split == 0 && cg == 0) {
+                if (threadIdx.x == 0) flag(ST_BAD_LEN);
+                if (nq > 0 && a >= 0 && b <= p.total_rows)
+                    for (int i = threadIdx.x; i < nq * p.group * D; i += THREADS) {
+                        const int r = i / (p.group * D), rem = i % (p.group * D);
+                        p.out[((size_t)(a + r) * p.hq + g * p.group) * D + rem] = 0.f;
+                    }
+            }
+            return;
+        }
+        if (cg * CW >= nq * p.group) return;
+        row = a;
+    } else if (p.row_mode) {
+        int Lseq;
         row = wi = blockIdx.z;
-        L = row_keys(p, row, s);
+        L = row_keys(p, row, s, Lseq);
     } else {
         if (p.cu_q_lens) {
             int a = p.cu_q_lens[s], b = p.cu_q_lens[s + 1];
@@ -229,9 +262,11 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
     uint32_t qf[NT][8][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        const int hl = nt * 8 + gq;
-        const bool hv = hl < p.group;
-        const uint16_t *qr = p.q + ((size_t)row * p.hq + g * p.group + (hv ? hl : 0)) * D;
+        // column -> (row offset, head of the group)
+        const int gc = cg * CW + nt * 8 + gq;
+        const int qi = MR ? gc / p.group : 0, hl = MR ? gc % p.group : gc;
+        const bool hv = MR ? qi < nq : hl < p.group;
+        const uint16_t *qr = p.q + ((size_t)(row + (hv ? qi : 0)) * p.hq + g * p.group + (hv ? hl : 0)) * D;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             if constexpr (!FP8) {
@@ -246,6 +281,17 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
             }
         }
     }
+    // MR: keys visible to this lane's two columns of each n-tile (2 cq, 2 cq + 1):
+    // row i sees keys < L - nq + i + 1; padding columns see everything (their Q
+    // is zero and their output is never stored)
+    int lim[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int qi = (cg * CW + nt * 8 + 2 * cq + e) / p.group;
+            lim[nt][e] = (MR && qi < nq) ? L - nq + qi + 1 : L;
+        }
     float sl = p.scale_log2;
     float vsc = 1.f;
     if constexpr (FP8) {
@@ -336,7 +382,8 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int t = gq + ((i >> 1) << 3);
-                    x[i] = t < nvalid ? sacc[nt][i] * sl : -INFINITY;
+                    const bool vis = MR ? blk * BS + t < lim[nt][i & 1] : t < nvalid;
+                    x[i] = vis ? sacc[nt][i] * sl : -INFINITY;
                 }
                 float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
@@ -345,11 +392,15 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
                     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
                 }
                 const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-                const float al0 = ex2(m[nt][0] - mn0), al1 = ex2(m[nt][1] - mn1);
+                // MR: a column may have seen no key yet (all masked): exponents are
+                // taken against 0 then, so p = 0 and nothing becomes NaN
+                const float r0 = (MR && mn0 == -INFINITY) ? 0.f : mn0;
+                const float r1 = (MR && mn1 == -INFINITY) ? 0.f : mn1;
+                const float al0 = ex2(m[nt][0] - r0), al1 = ex2(m[nt][1] - r1);
                 m[nt][0] = mn0;
                 m[nt][1] = mn1;
-                const float p0 = ex2(x[0] - mn0), p1 = ex2(x[1] - mn1);
-                const float p2 = ex2(x[2] - mn0), p3 = ex2(x[3] - mn1);
+                const float p0 = ex2(x[0] - r0), p1 = ex2(x[1] - r1);
+                const float p2 = ex2(x[2] - r0), p3 = ex2(x[3] - r1);
                 l[nt][0] = l[nt][0] * al0 + (p0 + p2);
                 l[nt][1] = l[nt][1] * al1 + (p1 + p3);
 #pragma unroll
@@ -472,8 +523,9 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
     __syncthreads();
     const bool any_to = sm_to[0] | sm_to[1] | sm_to[2] | sm_to[3];
     const int G = p.group;
-    for (int idx = threadIdx.x; idx < G * D; idx += THREADS) {
-        const int hl = idx / D, d = idx % D;
+    const int ncols = MR ? min(CW, nq * G - cg * CW) : G;
+    for (int idx = threadIdx.x; idx < ncols * D; idx += THREADS) {
+        const int hl = idx / D, d = idx % D;      // column of this CTA
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < WARPS; ++w) M = fmaxf(M, sm_m[w * HL + hl]);
@@ -486,11 +538,14 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
                 O += f * sm_o[(w * HL + hl) * D + d];
             }
         }
-        const int h = g * G + hl;
+        // MR: column -> (row of the chunk, head); partials are per row
+        const int gc = cg * CW + hl;
+        const int orow = MR ? row + gc / G : row, owi = MR ? orow : wi;
+        const int h = g * G + (MR ? gc % G : hl);
         if (nsplit_s == 1) {
-            p.out[((size_t)row * p.hq + h) * D + d] = Ls > 0.f ? O * vsc / Ls : 0.f;
+            p.out[((size_t)orow * p.hq + h) * D + d] = Ls > 0.f ? O * vsc / Ls : 0.f;
         } else {
-            const size_t pi = ((size_t)wi * p.hq + h) * p.num_splits + split;
+            const size_t pi = ((size_t)owi * p.hq + h) * p.num_splits + split;
             p.part_o[pi * D + d] = O * vsc;
             if (d == 0) {
                 p.part_ml[pi * 2] = (Ls > 0.f) ? M : -INFINITY;
@@ -500,18 +555,24 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
     }
 }
 
-// Log-sum-exp merge of the split partitions: one warp per (sequence, q head).
+// Log-sum-exp merge of the split partitions: one warp per (sequence, q head),
+// or per (row, q head) in the row and multi-row modes.
 __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p)
 {
     griddep_wait();   // the partials come from the decode kernel just before
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (wid >= (p.row_mode ? p.total_rows : p.num_seqs) * p.hq) return;
-    const int wi = wid / p.hq, h = wid % p.hq;   // wi: sequence, or row in row mode
+    const bool per_row = p.row_mode || p.col_groups > 0;
+    if (wid >= (per_row ? p.total_rows : p.num_seqs) * p.hq) return;
+    const int wi = wid / p.hq, h = wid % p.hq;   // wi: sequence, or row
     int row = wi, L;
     if (p.row_mode) {
+        int seq, Lseq;
+        L = row_keys(p, row, seq, Lseq);
+    } else if (p.col_groups > 0) {
+        // multi-row: the row's partitions are those of its sequence's whole context
         int seq;
-        L = row_keys(p, row, seq);
+        (void)row_keys(p, row, seq, L);
     } else {
         if (p.cu_q_lens) {
             int a = p.cu_q_lens[wi], b = p.cu_q_lens[wi + 1];
@@ -547,20 +608,29 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p)
 }
 
 // ---- device code end (hashed with the ncu counters of profiles/)
-template <bool FP8, int NT>
+template <bool FP8, int NT, bool MR>
 cudaError_t launch_one(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &p,
                        cudaStream_t st)
 {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP8, NT>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP8, NT, MR>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Geo<FP8>::SMEM);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    dim3 grid(p.num_splits, p.hkv, p.row_mode ? p.total_rows : p.num_seqs);
-    return pkv_host::launch_pdl(decode_kernel<FP8, NT>, grid, dim3(THREADS), Geo<FP8>::SMEM, st, km, vm, p);
+    dim3 grid(p.num_splits * (MR ? p.col_groups : 1), p.hkv, p.row_mode ? p.total_rows : p.num_seqs);
+    return pkv_host::launch_pdl(decode_kernel<FP8, NT, MR>, grid, dim3(THREADS), Geo<FP8>::SMEM, st, km, vm, p);
+}
+
+template <bool FP8>
+cudaError_t launch_for(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &p, int nt,
+                       cudaStream_t st)
+{
+    if (p.col_groups > 0)
+        return nt == 2 ? launch_one<FP8, 2, true>(km, vm, p, st) : launch_one<FP8, 1, true>(km, vm, p, st);
+    return nt == 2 ? launch_one<FP8, 2, false>(km, vm, p, st) : launch_one<FP8, 1, false>(km, vm, p, st);
 }
 
 }  // namespace
@@ -618,6 +688,15 @@ size_t workspace_bytes_rows(int32_t total_rows, int32_t hq, int32_t max_blocks)
     return partial_bytes(total_rows, hq, s);
 }
 
+// Multi-row mode: the decode partitioning, partials per row.
+size_t workspace_bytes_multi(int32_t total_rows, int32_t hq, int32_t max_blocks, int32_t num_splits)
+{
+    if (total_rows < 1 || hq < 1 || max_blocks < 1) return 0;
+    int32_t pb, s;
+    plan_splits(max_blocks, num_splits, &pb, &s);
+    return partial_bytes(total_rows, hq, s);
+}
+
 bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int32_t hkv,
                kv_dtype dt, CUtensorMap *km, CUtensorMap *vm)
 {
@@ -634,19 +713,23 @@ bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int
 }
 
 // Validates host-visible arguments shared by decode and the decode rows of a
-// mixed batch, then launches decode (+ reduce).  row_mode (needs cu_q_lens):
-// every row of the batch, chunk rows included, is a decode problem over the
-// keys it may see.
+// mixed batch, then launches decode (+ reduce).  Needing cu_q_lens:
+//  row_mode        every row of the batch, chunk rows included, is a decode
+//                  problem over the keys it may see;
+//  multi_q_len > 0 multi-row mode: every sequence's rows (at most multi_q_len)
+//                  are covered by column groups of one CTA per KV tile stream.
 kv_status run(float *out, const void *q, const void *k_cache, const void *v_cache,
               const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
               const int32_t *cu_q_lens, int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t hkv,
               int32_t num_blocks, float scale, kv_dtype dt, const float *k_scale, const float *v_scale,
               int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st,
-              bool row_mode)
+              bool row_mode, int32_t multi_q_len)
 {
-    if (row_mode && (!cu_q_lens || total_rows < 0)) return KV_ERR_INVALID;
-    if (row_mode && total_rows == 0) return KV_OK;
+    const bool multi = multi_q_len > 0;
+    if ((row_mode || multi) && (!cu_q_lens || total_rows < 0)) return KV_ERR_INVALID;
+    if ((row_mode || multi) && total_rows == 0) return KV_OK;
     if (row_mode && total_rows > 65535) return KV_ERR_UNSUPPORTED;
+    if (row_mode && multi) return KV_ERR_INVALID;
     if (num_seqs == 0) return KV_OK;
     if (num_seqs < 0 || hq < 1 || hkv < 1 || num_blocks < 1 || max_blocks < 1) return KV_ERR_INVALID;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return KV_ERR_INVALID;
@@ -679,10 +762,19 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     p.scale_log2 = scale * LOG2E;
     if (row_mode) plan_rows(max_blocks, &p.part_blocks, &p.num_splits);
     else plan_splits(max_blocks, num_splits, &p.part_blocks, &p.num_splits);
+    // columns of one sequence and KV head: its rows x the group's heads
+    const int64_t cols = multi ? (int64_t)multi_q_len * G : G;
+    const int nt = cols > 8 ? 2 : 1;
+    if (multi) {
+        const int64_t groups = (cols + 8 * nt - 1) / (8 * nt);
+        if (groups * p.num_splits > INT32_MAX) return KV_ERR_UNSUPPORTED;
+        p.col_groups = (int)groups;
+    }
     if (p.num_splits > 65535) return KV_ERR_UNSUPPORTED;
-    const int32_t problems = row_mode ? total_rows : num_seqs;
+    const int32_t problems = (row_mode || multi) ? total_rows : num_seqs;
     const size_t need = row_mode ? workspace_bytes_rows(total_rows, hq, max_blocks)
-                                 : workspace_bytes(num_seqs, hq, max_blocks, num_splits);
+                                 : multi ? workspace_bytes_multi(total_rows, hq, max_blocks, num_splits)
+                                         : workspace_bytes(num_seqs, hq, max_blocks, num_splits);
     if (need) {
         if (!workspace || workspace_bytes_given < need || !pkv_host::aligned(workspace, 256))
             return KV_ERR_INVALID;
@@ -692,9 +784,7 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     }
     CUtensorMap km, vm;
     if (!make_maps(k_cache, v_cache, num_blocks, hkv, dt, &km, &vm)) return KV_ERR_CUDA;
-    cudaError_t e;
-    if (dt == KV_BF16) e = G == 16 ? launch_one<false, 2>(km, vm, p, st) : launch_one<false, 1>(km, vm, p, st);
-    else e = G == 16 ? launch_one<true, 2>(km, vm, p, st) : launch_one<true, 1>(km, vm, p, st);
+    const cudaError_t e = dt == KV_BF16 ? launch_for<false>(km, vm, p, nt, st) : launch_for<true>(km, vm, p, nt, st);
     if (e != cudaSuccess) return KV_ERR_CUDA;
     if (p.num_splits > 1) {
         const int64_t warps = (int64_t)problems * hq;
@@ -734,7 +824,7 @@ kv_status paged_attention_decode(float *out, const void *q, const void *k_cache,
     return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            nullptr, num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                            k_scale, v_scale, num_splits, workspace, workspace_bytes,
-                           static_cast<cudaStream_t>(stream), false);
+                           static_cast<cudaStream_t>(stream), false, 0);
 }
 
 }  // extern "C"
@@ -800,7 +890,7 @@ kv_status paged_attention_decode_static_scratch(float *out, const void *q, const
     return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            nullptr, num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                            k_scale, v_scale, num_splits, scratch, need ? STATIC_SCRATCH_BYTES : 0,
-                           static_cast<cudaStream_t>(stream), false);
+                           static_cast<cudaStream_t>(stream), false, 0);
 }
 
 }  // extern "C"

@@ -561,9 +561,10 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
               const int32_t *cu_q_lens, int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t hkv,
               int32_t num_blocks, float scale, kv_dtype dt, const float *k_scale, const float *v_scale,
               int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st,
-              bool row_mode);
+              bool row_mode, int32_t multi_q_len);
 size_t workspace_bytes(int32_t num_seqs, int32_t hq, int32_t max_blocks, int32_t num_splits);
 size_t workspace_bytes_rows(int32_t total_rows, int32_t hq, int32_t max_blocks);
+size_t workspace_bytes_multi(int32_t total_rows, int32_t hq, int32_t max_blocks, int32_t num_splits);
 bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int32_t hkv, kv_dtype dt,
                CUtensorMap *km, CUtensorMap *vm);
 }  // namespace pkv_decode
@@ -595,6 +596,18 @@ Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq,
 size_t rows_bytes(int32_t total_q, int32_t hq, int32_t max_blocks)
 {
     return pkv_decode::workspace_bytes_rows(total_q, hq, max_blocks);
+}
+
+// Short chunks (a speculative draft being verified, a few rows per sequence)
+// are memory-bound like decode: when every sequence's rows x the group's heads
+// fit in MULTI_MAX_COLS columns, the whole batch runs in the decode kernel's
+// multi-row mode, which streams each K/V tile once for all the rows of its
+// sequence (column groups of 16 share it through L2).
+constexpr int64_t MULTI_MAX_COLS = 64;
+
+bool use_multi(int32_t max_q_len, int32_t hq, int32_t hkv)
+{
+    return max_q_len >= 2 && hkv >= 1 && (int64_t)max_q_len * (hq / hkv) <= MULTI_MAX_COLS;
 }
 }  // namespace
 
@@ -643,11 +656,14 @@ size_t paged_attention_chunked_prefill_workspace_size(int32_t num_seqs, int32_t 
                                                       int32_t max_blocks_per_seq,
                                                       int32_t num_splits)
 {
-    (void)num_kv_heads;
-    if (num_seqs < 1 || total_q_tokens < 1 || max_q_len < 1 || num_q_heads < 1 || max_blocks_per_seq < 1)
+    if (num_seqs < 1 || total_q_tokens < 1 || max_q_len < 1 || num_q_heads < 1 || max_blocks_per_seq < 1 ||
+        num_kv_heads < 1)
         return 0;
-    const size_t t = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, max_blocks_per_seq, num_splits).total;
-    return max_q_len >= 2 ? std::max(t, rows_bytes(total_q_tokens, num_q_heads, max_blocks_per_seq)) : t;
+    size_t t = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, max_blocks_per_seq, num_splits).total;
+    if (max_q_len >= 2) t = std::max(t, rows_bytes(total_q_tokens, num_q_heads, max_blocks_per_seq));
+    if (use_multi(max_q_len, num_q_heads, num_kv_heads))
+        t = std::max(t, pkv_decode::workspace_bytes_multi(total_q_tokens, num_q_heads, max_blocks_per_seq, num_splits));
+    return t;
 }
 
 kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32_t *cu_q_lens,
@@ -672,12 +688,18 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     if (!(scale > 0.f) || num_seqs > 65535 || num_kv_heads > 65535) return KV_ERR_INVALID;
     if (!pkv_host::aligned(out, 16) || !pkv_host::aligned(q, 16)) return KV_ERR_INVALID;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (use_multi(max_q_len, num_q_heads, num_kv_heads)) {
+        // short chunks: the decode kernel's multi-row mode for the whole batch
+        return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
+                               total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
+                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, false, max_q_len);
+    }
     if (max_q_len >= 2 && dtype == KV_FP8_E4M3) {
         // fp8 cache with chunks: every row (chunk or decode) goes through the
         // decode kernel as a problem of its own, over the keys it may see
         return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
-                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, true);
+                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, true, 0);
     }
     const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, max_blocks_per_seq, num_splits);
     if (pl.total && (!workspace || workspace_bytes < pl.total || !pkv_host::aligned(workspace, 256)))
@@ -687,7 +709,7 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
         return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                                k_scale, v_scale, num_splits, pl.decode_bytes ? ws : nullptr, pl.decode_bytes, on,
-                               false);
+                               false, 0);
     };
     if (max_q_len < 2) return decode_rows(st);   // decode rows only
     // decode rows (n = 1) on the side stream, forked from and joined into the
