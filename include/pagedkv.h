@@ -306,7 +306,11 @@ PAGEDKV_API kv_status paged_attention_decode_static_scratch(
  * (n_s >= 2) take the tensor-core (tcgen05) kernel, and the decode rows run on
  * a stream the library owns (one per device), forked from `stream` with an
  * event and joined back into it before the call returns: work enqueued on
- * `stream` afterwards sees the whole output.  With an fp8 cache and chunks,
+ * `stream` afterwards sees the whole output.  Short chunks -- max_q_len x
+ * (num_q_heads / num_kv_heads) <= 16, e.g. a speculative draft of 4 tokens
+ * under a GQA group of 4 ([P3] speculative decoding, N = 4-8) -- run instead
+ * with the whole batch in the decode kernel, whose CTA then covers all rows of
+ * a sequence so each K/V tile is read once.  With an fp8 cache and longer chunks,
  * every row of the batch (chunk rows included) is a decode problem of its own
  * over the keys it may see, on `stream`: total_q_tokens <= 65535 (else
  * KV_ERR_UNSUPPORTED), partitions of 16,384 keys, num_splits ignored.

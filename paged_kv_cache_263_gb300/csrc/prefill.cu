@@ -10,7 +10,7 @@
 // prefill.  Rows with n = 1 are decode rows and go to the decode kernel.
 //
 // Tensor-core kernel (bf16 cache), one CTA per (pair of 128-row query tiles,
-// KV head, 16,384-key partition):
+// KV head, KV partition):
 //  * A query tile packs 128/G chunk tokens x the G query heads of one KV head
 //    (row = token * G + head), so every K/V tile is shared by the whole GQA
 //    group; the two tiles of a pair share every K/V tile as well.  Both Q tiles
@@ -35,8 +35,9 @@
 //  * Keys at or past the context end inside the last tile are masked in S; the
 //    producer zeroes their V rows after the load lands (0 x garbage could be
 //    NaN), signalled on its own barrier.
-//  * Long contexts are cut into 16,384-key partitions of whole tiles, merged
-//    by a fixed-order log-sum-exp kernel (no atomics).
+//  * Long contexts are cut into partitions of whole tiles (16,384 keys, less
+//    when the grid would be too small to fill the GPU), merged by a
+//    fixed-order log-sum-exp kernel (no atomics).
 //  * Decode rows (n = 1) of the batch run on a library-owned side stream in
 //    the decode kernel, concurrently with the chunk tiles.
 //
@@ -546,7 +547,9 @@ __global__ void __launch_bounds__(128) prefill_reduce_kernel(const PrefillParams
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
-constexpr int TILES_PER_SPLIT = 16384 / BN;   // 16,384 keys per partition
+constexpr int TILES_PER_SPLIT = 16384 / BN;   // 16,384 keys per partition at most
+constexpr int MIN_TILES_PER_SPLIT = 1024 / BN; // 1,024 keys at least
+constexpr int64_t TARGET_CTAS = 4 * 152;       // four CTAs per SM of the grid, at least
 
 struct Plan {
     size_t decode_bytes, part_o_off, part_ml_off, tile_off_off, total;
@@ -570,14 +573,29 @@ bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int
 }  // namespace pkv_decode
 
 namespace {
-Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq, int32_t max_blocks,
+// KV partition length: 16,384 keys, halved (down to 1,024) while the grid
+// would hold fewer than TARGET_CTAS CTAs -- short chunks over a few thousand
+// keys otherwise leave most SMs idle (one CTA per SM fits).  The CTA count is
+// estimated from the host-visible sizes only: chunk sequences ~ total_q /
+// max_q_len, each with ceil(ceil(max_q_len / tpt) / 2) pairs of query tiles.
+int plan_tiles_per_split(int32_t total_q, int32_t max_q_len, int32_t hq, int32_t hkv, int max_kv_tiles)
+{
+    const int G = std::max(1, hq / std::max(1, hkv)), tpt = std::max(1, BM / G);
+    const int64_t chunks = std::max<int64_t>(1, (int64_t)total_q / std::max(1, max_q_len));
+    const int64_t pairs = chunks * (((int64_t)max_q_len + tpt - 1) / tpt + 1) / 2;
+    int tps = TILES_PER_SPLIT;
+    while (tps > MIN_TILES_PER_SPLIT && pairs * hkv * ((max_kv_tiles + tps - 1) / tps) < TARGET_CTAS) tps /= 2;
+    return tps;
+}
+
+Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq, int32_t hkv, int32_t max_blocks,
                int32_t num_splits)
 {
     Plan pl{};
     auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
     pl.decode_bytes = up(pkv_decode::workspace_bytes(num_seqs, hq, max_blocks, num_splits));
-    pl.tiles_per_split = TILES_PER_SPLIT;
     const int max_kv_tiles = (max_blocks * BS + BN - 1) / BN;
+    pl.tiles_per_split = plan_tiles_per_split(total_q, max_q_len, hq, hkv, max_kv_tiles);
     pl.max_splits = max_q_len >= 2 ? (max_kv_tiles + pl.tiles_per_split - 1) / pl.tiles_per_split : 0;
     size_t off = pl.decode_bytes;
     pl.part_o_off = off;
@@ -602,8 +620,12 @@ size_t rows_bytes(int32_t total_q, int32_t hq, int32_t max_blocks)
 // are memory-bound like decode: when every sequence's rows x the group's heads
 // fit in MULTI_MAX_COLS columns, the whole batch runs in the decode kernel's
 // multi-row mode, which streams each K/V tile once for all the rows of its
-// sequence (column groups of 16 share it through L2).
-constexpr int64_t MULTI_MAX_COLS = 64;
+// sequence.  Measured on GB300: one column group (16 columns) beats the
+// tensor-core kernel; several groups sharing tiles through L2 do not.
+#ifndef PKV_MULTI_MAX_COLS
+#define PKV_MULTI_MAX_COLS 16
+#endif
+constexpr int64_t MULTI_MAX_COLS = PKV_MULTI_MAX_COLS;
 
 bool use_multi(int32_t max_q_len, int32_t hq, int32_t hkv)
 {
@@ -659,7 +681,8 @@ size_t paged_attention_chunked_prefill_workspace_size(int32_t num_seqs, int32_t 
     if (num_seqs < 1 || total_q_tokens < 1 || max_q_len < 1 || num_q_heads < 1 || max_blocks_per_seq < 1 ||
         num_kv_heads < 1)
         return 0;
-    size_t t = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, max_blocks_per_seq, num_splits).total;
+    size_t t = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq,
+                         num_splits).total;
     if (max_q_len >= 2) t = std::max(t, rows_bytes(total_q_tokens, num_q_heads, max_blocks_per_seq));
     if (use_multi(max_q_len, num_q_heads, num_kv_heads))
         t = std::max(t, pkv_decode::workspace_bytes_multi(total_q_tokens, num_q_heads, max_blocks_per_seq, num_splits));
@@ -701,7 +724,8 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                                k_scale, v_scale, num_splits, workspace, workspace_bytes, st, true, 0);
     }
-    const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, max_blocks_per_seq, num_splits);
+    const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq,
+                              num_splits);
     if (pl.total && (!workspace || workspace_bytes < pl.total || !pkv_host::aligned(workspace, 256)))
         return KV_ERR_INVALID;
     uint8_t *ws = static_cast<uint8_t *>(workspace);

@@ -37,7 +37,7 @@ def test_mixed_batch_small(hq, hkv):
 
 
 def test_chunk_spanning_several_partitions():
-    """A 40-row chunk over 40,000 keys: three 16,384-key partitions merged by LSE."""
+    """A 40-row chunk over 40,000 keys: several KV partitions merged by LSE."""
     wl = small_workload(800, lens=[40000, 33], q_lens=[40, 1], hq=16, hkv=2)
     _, got = _run(wl)
     cu = wl.cu_q_lens
