@@ -15,17 +15,16 @@
 //    (row = token * G + head), so every K/V tile is shared by the whole GQA
 //    group; the two tiles of a pair share every K/V tile as well.  Both Q tiles
 //    land in shared memory with one 3-D TMA load each.
-//  * K/V tiles of 128 keys = 8 physical blocks, gathered through the block
-//    table by 2-D TMA loads (128-byte swizzle) into a 2-stage ring (warp 8).
-//  * S[128x128] = Q K^T and O[128x128] += P V run as tcgen05.mma (K=16 steps,
-//    N = 128: the full tensor rate), one issuing warp per query tile (warps 9
-//    and 10).  P (bf16) is written over S's first 64 columns and read by the
-//    second product as the A operand straight from tensor memory, so S(j+1)
-//    follows PV(j) in issue order; while one tile's softmax runs, the tensor
-//    pipe works on the other tile's products.  K is the K-major B operand of
-//    the first product, V the MN-major B operand of the second, both from the
-//    same shared-memory stage.  Tensor memory: S 128 columns and O 128 columns
-//    per query tile, 512 in all.
+//  * K/V tiles of 64 keys = 4 physical blocks, gathered through the block
+//    table by 2-D TMA loads (128-byte swizzle) into a 4-stage ring (warp 8).
+//  * S[128x64] = Q K^T and O[128x128] += P V run as tcgen05.mma (K=16 steps),
+//    one issuing warp per query tile (warps 9 and 10).  S is double-buffered
+//    per tile in tensor memory, so QK^T of tile j+2 runs while the softmax
+//    works on tile j.  P (bf16) is written over its S buffer and read by the
+//    second product as the A operand straight from tensor memory; K is the
+//    K-major B operand of the first product, V the MN-major B operand of the
+//    second, both from the same shared-memory stage.  Tensor memory: S 2 x 64
+//    columns and O 128 columns per query tile, 512 in all.
 //  * Two softmax warpgroups (warps 0-7), one per query tile, own one TMEM lane
 //    (= one query row) per thread.  They read S with tcgen05.ld, apply the
 //    causal mask on diagonal tiles, keep the online max / normaliser
@@ -271,7 +270,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int st = jj % KV_STAGES;
             if (jj >= KV_STAGES && !wait_w(bar(B_KVE + st), ((jj - KV_STAGES) / KV_STAGES) & 1)) break;
             const int j = j0 + jj;
-            const int b = j * (BN / BS) + lane;       // lanes 0..7: the tile's 8 blocks
+            const int b = j * (BN / BS) + (lane & 3);
             int32_t id = -1;
             if (lane < BN / BS && b < nblk) id = __ldg(bt + b);
             const bool valid = lane < BN / BS && b < nblk && id >= 0 && id < p.num_blocks;
