@@ -55,17 +55,17 @@ __device__ uint32_t g_status;
 
 using namespace pkv;
 
-constexpr int BM = 128, BN = 128;              // 128 query rows x 128 keys (8 blocks) per tile
+constexpr int BM = 128, BN = 64;               // 128 query rows x 64 keys (4 blocks) per tile
 // warps 0-3 softmax of query tile 0, 4-7 softmax of query tile 1, 8 TMA producer,
 // 9 and 10 MMA issuers of query tile 0 and 1
 constexpr int THREADS = 352;
-constexpr int KV_STAGES = 2;
+constexpr int KV_STAGES = 4;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
-// shared memory: Q 2 x 32 KiB | 2 stages of (K 32 KiB, V 32 KiB) | barriers.  P lives
-// in tensor memory.  A K or V tile is two 64-column halves of [128 keys][128 B].
+// shared memory: Q 2 x 32 KiB | 4 stages of (K 16 KiB, V 16 KiB) | barriers.  P lives
+// in tensor memory.
 constexpr uint32_t SQ = 0, Q_TILE = 32768;
-constexpr uint32_t SKV = 65536, KV_STAGE_BYTES = 65536, V_OFF = 32768, KV_HALF = 16384;
+constexpr uint32_t SKV = 65536, KV_STAGE_BYTES = 32768, V_OFF = 16384, KV_HALF = 8192;
 constexpr uint32_t SBAR = SKV + KV_STAGES * KV_STAGE_BYTES;
 constexpr int SMEM_BYTES = SBAR + 256;
 static_assert(SKV >= 2 * 32768 && SBAR == SKV + KV_STAGES * KV_STAGE_BYTES, "shared-memory layout overlaps");
@@ -75,8 +75,8 @@ enum {
     B_KVF = 0,                      // + stage: K and V of a tile landed
     B_KVE = B_KVF + KV_STAGES,      // + stage: every MMA reading the stage is done
     B_Q = B_KVE + KV_STAGES,        // both Q tiles landed
-    B_S = B_Q + 1,                  // + group: the group's S tile is in TMEM
-    B_P = B_S + 2,                  // + group: the group's P is in TMEM (128 arrivals)
+    B_S = B_Q + 1,                  // + 2*group + buffer: an S tile of the group is in TMEM
+    B_P = B_S + 4,                  // + group: the group's P is in TMEM (128 arrivals)
     B_PVD = B_P + 2,                // + group: the group's latest PV product finished
     B_DRAIN = B_PVD + 2,            // + group: every MMA of the group's issuer finished
     B_TAIL = B_DRAIN + 2,           // the V rows past the context are zeroed
@@ -90,7 +90,7 @@ constexpr uint32_t idesc(int n, bool b_mn_major)
     return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(BM >> 4) << 24);
 }
-constexpr uint32_t IDESC_S = idesc(BN, false);    // S[128 x 128] = Q K^T, K K-major
+constexpr uint32_t IDESC_S = idesc(BN, false);    // S[128 x 64] = Q K^T, K K-major
 constexpr uint32_t IDESC_PV = idesc(D, true);     // O[128 x 128] += P V, V MN-major
 
 struct PrefillParams {
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bar(B_KVE + i), has1 ? 2 : 1);   // one release per MMA issuer
         }
         mbar_init(bar(B_Q), 1);
-        for (int i = 0; i < 2; ++i) mbar_init(bar(B_S + i), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bar(B_S + i), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_P + i), 128);
             mbar_init(bar(B_PVD + i), 1);
@@ -248,9 +248,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // TMEM columns per query tile gi: S at 128 gi (128 fp32 columns; P overwrites
-    // the first 64 with bf16 pairs once S has been read), O at 256 + 128 gi
-    auto tS = [&](int gi) -> uint32_t { return tmem + gi * BN; };
+    // TMEM columns per query tile gi: two S buffers of 64 fp32 columns at
+    // 128 gi + 64 b (P overwrites the first 32 of a buffer with bf16 pairs once its
+    // S has been read), O at 256 + 128 gi
+    auto tS = [&](int gi, int b) -> uint32_t { return tmem + gi * 128 + b * BN; };
     auto tO = [&](int gi) -> uint32_t { return tmem + 256 + gi * D; };
 
     if (warp == 8) {
@@ -323,17 +324,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t kdesc0 = sdesc_sw128(sbase + SKV, 16, 1024);
             const uint64_t vdesc0 = sdesc_sw128(sbase + SKV + V_OFF, KV_HALF, 1024);
             const uint32_t to = tO(gi);
-            // S = Q K^T for KV tile jj: A = Q, B = K (K-major)
+            // S = Q K^T for KV tile jj into S buffer jj % 2: A = Q, B = K (K-major)
             auto issue_s = [&](int jj) {
                 if (lane == 0) {
                     tc_fence_after();
                     const uint64_t kd = kdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
-                    const uint32_t ts = tS(gi);
+                    const uint32_t ts = tS(gi, jj & 1);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)   // D = 128 in steps of 16: 4 per 64-wide half
                         umma_f16(ts, qdesc + (uint64_t)((((kk >> 2) * 16384) + (kk & 3) * 32) >> 4),
                                  kd + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4), IDESC_S, kk > 0);
-                    umma_commit(bar(B_S + gi));
+                    umma_commit(bar(B_S + 2 * gi + (jj & 1)));
                 }
                 __syncwarp();
             };
@@ -342,9 +343,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) {
                     tc_fence_after();
                     const uint64_t vd = vdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
-                    const uint32_t ts = tS(gi);
+                    const uint32_t ts = tS(gi, jj & 1);
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)   // 128 keys in steps of 16
+                    for (int kk = 0; kk < BN / 16; ++kk)   // 64 keys in steps of 16
                         umma_f16_ts(to, ts + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), IDESC_PV,
                                     (jj > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(bar(B_PVD + gi));
@@ -357,19 +358,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             auto tail_ready = [&](int jj) -> bool {
                 return (j0 + jj + 1) * BN <= L || wait_w(bar(B_TAIL), 0);
             };
-            // S(jj+1) follows PV(jj) in issue order (P aliases S); the other query
-            // tile's products keep the tensor pipe busy while this tile's softmax runs
-            bool ok = wait_w(bar(B_Q), 0) && wait_w(bar(B_KVF), 0);
-            if (ok) issue_s(0);
+            // S of the first two tiles up front; afterwards S(jj+2) follows PV(jj), so
+            // each softmax finds its S computed while it worked on the tile before
+            bool ok = wait_w(bar(B_Q), 0);
+            for (int jj = 0; ok && jj < min(2, T); ++jj) {
+                if (!wait_w(bar(B_KVF + jj), 0)) { ok = false; break; }
+                issue_s(jj);
+            }
             for (int jj = 0; jj < T && ok; ++jj) {
                 if (!wait_w(bar(B_P + gi), jj & 1) || !tail_ready(jj)) { ok = false; break; }
-                // in issue order: PV(jj) reads P from the S columns before S(jj+1)
-                // overwrites them
+                // in issue order: PV(jj) reads P from S buffer jj % 2 before S(jj+2)
+                // overwrites it
                 issue_pv(jj);
-                if (jj + 1 < T) {
-                    const int sn = (jj + 1) % KV_STAGES;
-                    if (!wait_w(bar(B_KVF + sn), ((jj + 1) / KV_STAGES) & 1)) { ok = false; break; }
-                    issue_s(jj + 1);
+                if (jj + 2 < T) {
+                    const int sn = (jj + 2) % KV_STAGES;
+                    if (!wait_w(bar(B_KVF + sn), ((jj + 2) / KV_STAGES) & 1)) { ok = false; break; }
+                    issue_s(jj + 2);
                 }
             }
             // every MMA this issuer started has finished before TMEM is released
@@ -396,28 +400,25 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool ok = true;
             for (int jj = 0; jj < T && ok; ++jj) {
                 const int t0 = (j0 + jj) * BN;
-                if (!wait_w(bar(B_S + gi), jj & 1)) { ok = false; break; }
+                if (!wait_w(bar(B_S + 2 * gi + (jj & 1)), (jj >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                // two passes over S, 64 columns at a time (registers): the row max,
-                // then the exponentials; raw scores -- the scale (> 0) is applied
-                // inside the exponent's FFMA, so the max is taken on raw values
-                const bool diag = t0 + BN - 1 > pos_min;   // causal mask needed
-                float mk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    float sv[64];
-                    tmem_ld64(tS(gi) + lane_base + hh * 64, sv);
-                    if (diag) {
+                float sv[BN];
+                tmem_ld64(tS(gi, jj & 1) + lane_base, sv);
+                // raw scores; the scale (> 0) is applied inside the exponent's FFMA,
+                // so the max is taken on the raw values
+                if (t0 + BN - 1 > pos_min) {             // diagonal tile: causal mask
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (t0 + hh * 64 + c > pos) sv[c] = -INFINITY;
-                    }
-                    // four independent chains of 3-input maxima
+                    for (int c = 0; c < BN; ++c)
+                        if (t0 + c > pos) sv[c] = -INFINITY;
+                }
+                // max over the 64 scores: four independent chains of 3-input maxima
+                float mk[4];
 #pragma unroll
-                    for (int c = 0; c < 64; c += 8) {
+                for (int k = 0; k < 4; ++k) mk[k] = fmaxf(sv[k], sv[4 + k]);        // elements 0..7
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) mk[k] = max3(mk[k], sv[c + k], sv[c + 4 + k]);
-                    }
+                for (int c = 8; c < BN; c += 8) {                                      // elements c..c+7
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) mk[k] = max3(mk[k], sv[c + k], sv[c + 4 + k]);
                 }
                 const float mraw = max3(mk[0], mk[1], fmaxf(mk[2], mk[3]));
                 const float mx = mraw * p.scale_log2;
@@ -429,30 +430,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // With no visible key yet (m_ref = -inf) every score is -inf and the
                 // reference 0 keeps the exponent at -inf, i.e. p = 0.
                 const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;
-                // exponent argument and running sum on packed fp32 pairs; P as bf16
-                // pairs over the first 64 columns of S (the A operand of PV) -- S(jj)
-                // columns 64h.. are read before P's columns 32h.. are written
+                // exponent argument and running sum on packed fp32 pairs
                 const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2), mn2 = f2_pack(mneg, mneg);
                 uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    float sv[64];
-                    tmem_ld64(tS(gi) + lane_base + hh * 64, sv);
-                    if (diag) {
+                uint32_t pw[BN / 2];
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (t0 + hh * 64 + c > pos) sv[c] = -INFINITY;
-                    }
-                    uint32_t pw[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float y0, y1;
-                        f2_unpack(f2_fma(f2_pack(sv[2 * e], sv[2 * e + 1]), sl2, mn2), y0, y1);
-                        const float p0 = ex2(y0), p1 = ex2(y1);
-                        acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
-                        pw[e] = pack_bf16(p0, p1);
-                    }
-                    tmem_st32u(tS(gi) + lane_base + hh * 32, pw);
+                for (int e = 0; e < BN / 2; ++e) {
+                    float y0, y1;
+                    f2_unpack(f2_fma(f2_pack(sv[2 * e], sv[2 * e + 1]), sl2, mn2), y0, y1);
+                    const float p0 = ex2(y0), p1 = ex2(y1);
+                    acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
+                    pw[e] = pack_bf16(p0, p1);
                 }
                 const uint64_t a2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
                 float s0, s1;
@@ -460,7 +448,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const float sum = s0 + s1;
                 l = l * alpha + sum;
                 if (jj > 0) {
-                    // PV(jj-1) finished (it ran before S(jj)): O holds every earlier tile
+                    // PV(jj-1) finished: O holds every earlier tile, and PV(jj-2), which
+                    // read the P columns about to be overwritten, finished before it
                     if (!wait_w(bar(B_PVD + gi), (jj - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
                 }
@@ -474,6 +463,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         tmem_st32(tO(gi) + lane_base + c * 32, o);
                     }
                 }
+                // P in bf16 pairs over the first 32 columns of the S buffer (the A
+                // operand of PV)
+                tmem_st32u(tS(gi, jj & 1) + lane_base, pw);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(B_P + gi));
