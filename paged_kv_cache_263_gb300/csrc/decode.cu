@@ -642,10 +642,19 @@ namespace pkv_decode {
 // mode lengthens partitions with the longest context (64 blocks up to 8K
 // tokens, 128 up to 64K, 256 beyond): measured on GB300 this keeps enough
 // CTAs for the short batches while long ones pay less per-CTA ramp-up and
-// partial-merge traffic.
-void plan_splits(int32_t max_blocks, int32_t num_splits, int32_t *part_blocks, int32_t *splits)
+// partial-merge traffic.  A batch with few (sequence, KV head) pairs --
+// estimated as num_seqs x hq / 8 -- gets shorter partitions (down to 4
+// blocks, one per warp) so that the grid still holds about SMALL_TARGET CTAs:
+// a handful of sequences is otherwise latency-bound on a few warps each.
+constexpr int64_t SMALL_TARGET = 2 * 3 * 152;
+
+void plan_splits(int32_t max_blocks, int32_t num_splits, int32_t num_seqs, int32_t hq, int32_t *part_blocks,
+                 int32_t *splits)
 {
-    const int32_t auto_part = max_blocks <= 512 ? 64 : (max_blocks <= 4096 ? 128 : 256);
+    int32_t auto_part = max_blocks <= 512 ? 64 : (max_blocks <= 4096 ? 128 : 256);
+    const int64_t pairs = (int64_t)std::max(1, num_seqs) * std::max(1, hq / 8);
+    const int64_t want = ((int64_t)max_blocks * pairs + SMALL_TARGET - 1) / SMALL_TARGET;
+    auto_part = (int32_t)std::min<int64_t>(auto_part, std::max<int64_t>(4, want));
     int32_t s = num_splits > 0 ? num_splits : (max_blocks + auto_part - 1) / auto_part;
     s = std::max(1, std::min(s, max_blocks));
     int32_t pb = (max_blocks + s - 1) / s;
@@ -676,7 +685,7 @@ size_t workspace_bytes(int32_t num_seqs, int32_t hq, int32_t max_blocks, int32_t
 {
     if (num_seqs < 1 || hq < 1 || max_blocks < 1) return 0;
     int32_t pb, s;
-    plan_splits(max_blocks, num_splits, &pb, &s);
+    plan_splits(max_blocks, num_splits, num_seqs, hq, &pb, &s);
     return partial_bytes(num_seqs, hq, s);
 }
 
@@ -689,11 +698,12 @@ size_t workspace_bytes_rows(int32_t total_rows, int32_t hq, int32_t max_blocks)
 }
 
 // Multi-row mode: the decode partitioning, partials per row.
-size_t workspace_bytes_multi(int32_t total_rows, int32_t hq, int32_t max_blocks, int32_t num_splits)
+size_t workspace_bytes_multi(int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t max_blocks,
+                             int32_t num_splits)
 {
     if (total_rows < 1 || hq < 1 || max_blocks < 1) return 0;
     int32_t pb, s;
-    plan_splits(max_blocks, num_splits, &pb, &s);
+    plan_splits(max_blocks, num_splits, num_seqs, hq, &pb, &s);
     return partial_bytes(total_rows, hq, s);
 }
 
@@ -761,7 +771,7 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     p.num_blocks = num_blocks;
     p.scale_log2 = scale * LOG2E;
     if (row_mode) plan_rows(max_blocks, &p.part_blocks, &p.num_splits);
-    else plan_splits(max_blocks, num_splits, &p.part_blocks, &p.num_splits);
+    else plan_splits(max_blocks, num_splits, num_seqs, hq, &p.part_blocks, &p.num_splits);
     // columns of one sequence and KV head: its rows x the group's heads
     const int64_t cols = multi ? (int64_t)multi_q_len * G : G;
     const int nt = cols > 8 ? 2 : 1;
@@ -773,7 +783,7 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     if (p.num_splits > 65535) return KV_ERR_UNSUPPORTED;
     const int32_t problems = (row_mode || multi) ? total_rows : num_seqs;
     const size_t need = row_mode ? workspace_bytes_rows(total_rows, hq, max_blocks)
-                                 : multi ? workspace_bytes_multi(total_rows, hq, max_blocks, num_splits)
+                                 : multi ? workspace_bytes_multi(total_rows, num_seqs, hq, max_blocks, num_splits)
                                          : workspace_bytes(num_seqs, hq, max_blocks, num_splits);
     if (need) {
         if (!workspace || workspace_bytes_given < need || !pkv_host::aligned(workspace, 256))

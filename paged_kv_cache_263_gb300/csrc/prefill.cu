@@ -571,7 +571,8 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
               bool row_mode, int32_t multi_q_len);
 size_t workspace_bytes(int32_t num_seqs, int32_t hq, int32_t max_blocks, int32_t num_splits);
 size_t workspace_bytes_rows(int32_t total_rows, int32_t hq, int32_t max_blocks);
-size_t workspace_bytes_multi(int32_t total_rows, int32_t hq, int32_t max_blocks, int32_t num_splits);
+size_t workspace_bytes_multi(int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t max_blocks,
+                             int32_t num_splits);
 bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int32_t hkv, kv_dtype dt,
                CUtensorMap *km, CUtensorMap *vm);
 }  // namespace pkv_decode
@@ -689,7 +690,8 @@ size_t paged_attention_chunked_prefill_workspace_size(int32_t num_seqs, int32_t 
                          num_splits).total;
     if (max_q_len >= 2) t = std::max(t, rows_bytes(total_q_tokens, num_q_heads, max_blocks_per_seq));
     if (use_multi(max_q_len, num_q_heads, num_kv_heads))
-        t = std::max(t, pkv_decode::workspace_bytes_multi(total_q_tokens, num_q_heads, max_blocks_per_seq, num_splits));
+        t = std::max(t, pkv_decode::workspace_bytes_multi(total_q_tokens, num_seqs, num_q_heads, max_blocks_per_seq,
+                                                          num_splits));
     return t;
 }
 
