@@ -364,6 +364,10 @@ def run_ours(args):
         a1.record(stream)
         torch.cuda.synchronize(dev)
         attn_avg_graph = a0.elapsed_time(a1) / K
+        st = pkv.kv_last_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} after the graph replays "
+                               f"(flags {pkv.kv_last_device_status_flags()})")
     # eager: the same step issued call by call (host launch overhead included),
     # with events around each call
     KE = min(K, 1000)
@@ -390,7 +394,7 @@ def run_ours(args):
         ms_per_step = eager_ms
     st = pkv.kv_last_device_status()
     if st != 0:
-        raise RuntimeError(f"device status {st} after timing")
+        raise RuntimeError(f"device status {st} after timing (flags {pkv.kv_last_device_status_flags()})")
 
     # ---- end to end through the public API with pinned host buffers
     h_q = dw.q.cpu().pin_memory()
