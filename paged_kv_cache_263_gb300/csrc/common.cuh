@@ -358,11 +358,16 @@ __device__ __forceinline__ void griddep_launch_dependents()
 
 #if defined(__CUDACC__)
 namespace pkv_host {
-// Launch with programmatic stream serialisation (the kernel calls
-// pkv::griddep_wait() before it reads what earlier kernels produced).
+// Launch, with programmatic stream serialisation when pdl is set (the kernel
+// calls pkv::griddep_wait() before it reads what earlier kernels produced).
+// Only for a kernel whose predecessor on the stream is a kernel: on a stream
+// fed through an event from another stream it is not used (measured on GB300:
+// decode kernels launched that way on the library's side stream, after calls
+// from a second caller stream, left the concurrent tcgen05 chunk kernel's
+// CTAs waiting past their time limit).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args &&...args)
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                      Args &&...args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -373,7 +378,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 }  // namespace pkv_host

@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p)
 // ---- device code end (hashed with the ncu counters of profiles/)
 template <bool FP8, int NT, bool MR>
 cudaError_t launch_one(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &p,
-                       cudaStream_t st)
+                       cudaStream_t st, bool pdl)
 {
     static bool configured = false;
     if (!configured) {
@@ -621,16 +621,16 @@ cudaError_t launch_one(const CUtensorMap &km, const CUtensorMap &vm, const Decod
         configured = true;
     }
     dim3 grid(p.num_splits * (MR ? p.col_groups : 1), p.hkv, p.row_mode ? p.total_rows : p.num_seqs);
-    return pkv_host::launch_pdl(decode_kernel<FP8, NT, MR>, grid, dim3(THREADS), Geo<FP8>::SMEM, st, km, vm, p);
+    return pkv_host::launch_ex(decode_kernel<FP8, NT, MR>, grid, dim3(THREADS), Geo<FP8>::SMEM, st, pdl, km, vm, p);
 }
 
 template <bool FP8>
 cudaError_t launch_for(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &p, int nt,
-                       cudaStream_t st)
+                       cudaStream_t st, bool pdl)
 {
     if (p.col_groups > 0)
-        return nt == 2 ? launch_one<FP8, 2, true>(km, vm, p, st) : launch_one<FP8, 1, true>(km, vm, p, st);
-    return nt == 2 ? launch_one<FP8, 2, false>(km, vm, p, st) : launch_one<FP8, 1, false>(km, vm, p, st);
+        return nt == 2 ? launch_one<FP8, 2, true>(km, vm, p, st, pdl) : launch_one<FP8, 1, true>(km, vm, p, st, pdl);
+    return nt == 2 ? launch_one<FP8, 2, false>(km, vm, p, st, pdl) : launch_one<FP8, 1, false>(km, vm, p, st, pdl);
 }
 
 }  // namespace
@@ -726,7 +726,8 @@ bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int
 }
 
 // Validates host-visible arguments shared by decode and the decode rows of a
-// mixed batch, then launches decode (+ reduce).  Needing cu_q_lens:
+// mixed batch, then launches decode (+ reduce), with programmatic dependent
+// launch when pdl is set (see pkv_host::launch_ex).  Needing cu_q_lens:
 //  row_mode        every row of the batch, chunk rows included, is a decode
 //                  problem over the keys it may see;
 //  multi_q_len > 0 multi-row mode: every sequence's rows (at most multi_q_len)
@@ -736,7 +737,7 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
               const int32_t *cu_q_lens, int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t hkv,
               int32_t num_blocks, float scale, kv_dtype dt, const float *k_scale, const float *v_scale,
               int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st,
-              bool row_mode, int32_t multi_q_len)
+              bool row_mode, int32_t multi_q_len, bool pdl)
 {
     const bool multi = multi_q_len > 0;
     if ((row_mode || multi) && (!cu_q_lens || total_rows < 0)) return KV_ERR_INVALID;
@@ -797,11 +798,12 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     }
     CUtensorMap km, vm;
     if (!make_maps(k_cache, v_cache, num_blocks, hkv, dt, &km, &vm)) return KV_ERR_CUDA;
-    const cudaError_t e = dt == KV_BF16 ? launch_for<false>(km, vm, p, nt, st) : launch_for<true>(km, vm, p, nt, st);
+    const cudaError_t e =
+        dt == KV_BF16 ? launch_for<false>(km, vm, p, nt, st, pdl) : launch_for<true>(km, vm, p, nt, st, pdl);
     if (e != cudaSuccess) return KV_ERR_CUDA;
     if (p.num_splits > 1) {
         const int64_t warps = (int64_t)problems * hq;
-        if (pkv_host::launch_pdl(reduce_kernel, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, st, p) !=
+        if (pkv_host::launch_ex(reduce_kernel, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, st, pdl, p) !=
             cudaSuccess)
             return KV_ERR_CUDA;
     }
@@ -837,7 +839,7 @@ kv_status paged_attention_decode(float *out, const void *q, const void *k_cache,
     return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            nullptr, num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                            k_scale, v_scale, num_splits, workspace, workspace_bytes,
-                           static_cast<cudaStream_t>(stream), false, 0);
+                           static_cast<cudaStream_t>(stream), false, 0, true);
 }
 
 }  // extern "C"
@@ -903,7 +905,7 @@ kv_status paged_attention_decode_static_scratch(float *out, const void *q, const
     return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            nullptr, num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                            k_scale, v_scale, num_splits, scratch, need ? STATIC_SCRATCH_BYTES : 0,
-                           static_cast<cudaStream_t>(stream), false, 0);
+                           static_cast<cudaStream_t>(stream), false, 0, true);
 }
 
 }  // extern "C"

@@ -568,7 +568,7 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
               const int32_t *cu_q_lens, int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t hkv,
               int32_t num_blocks, float scale, kv_dtype dt, const float *k_scale, const float *v_scale,
               int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st,
-              bool row_mode, int32_t multi_q_len);
+              bool row_mode, int32_t multi_q_len, bool pdl);
 size_t workspace_bytes(int32_t num_seqs, int32_t hq, int32_t max_blocks, int32_t num_splits);
 size_t workspace_bytes_rows(int32_t total_rows, int32_t hq, int32_t max_blocks);
 size_t workspace_bytes_multi(int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t max_blocks,
@@ -721,27 +721,27 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
         // short chunks: the decode kernel's multi-row mode for the whole batch
         return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
-                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, false, max_q_len);
+                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, false, max_q_len, true);
     }
     if (max_q_len >= 2 && dtype == KV_FP8_E4M3) {
         // fp8 cache with chunks: every row (chunk or decode) goes through the
         // decode kernel as a problem of its own, over the keys it may see
         return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
-                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, true, 0);
+                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, true, 0, true);
     }
     const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq,
                               num_splits);
     if (pl.total && (!workspace || workspace_bytes < pl.total || !pkv_host::aligned(workspace, 256)))
         return KV_ERR_INVALID;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    auto decode_rows = [&](cudaStream_t on) {
+    auto decode_rows = [&](cudaStream_t on, bool pdl) {
         return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                                k_scale, v_scale, num_splits, pl.decode_bytes ? ws : nullptr, pl.decode_bytes, on,
-                               false, 0);
+                               false, 0, pdl);
     };
-    if (max_q_len < 2) return decode_rows(st);   // decode rows only
+    if (max_q_len < 2) return decode_rows(st, true);   // decode rows only
     // decode rows (n = 1) on the side stream, forked from and joined into the
     // caller's stream; the chunk tiles run on the caller's stream meanwhile
     std::lock_guard<std::mutex> side_lock(g_side_mu);
@@ -749,7 +749,7 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     if (!side) return KV_ERR_CUDA;
     if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
         return KV_ERR_CUDA;
-    kv_status rs = decode_rows(side->stream);
+    kv_status rs = decode_rows(side->stream, false);   // fed by an event, not a kernel
     if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return KV_ERR_CUDA;
     struct Join {   // the caller's stream waits for the decode rows however this call ends
         cudaStream_t st;

@@ -139,3 +139,33 @@ def test_spec_verify_workloads_sampled(name):
     for s in (0, 1, wl.num_seqs // 2, wl.num_seqs - 1):
         err = max_abs(out[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s))
         assert err <= TOL["bf16"], (s, err)
+
+
+def test_calls_from_several_streams_and_a_captured_graph():
+    """The mixed call issued from a second stream, captured into a CUDA graph and
+    replayed, then eagerly again from the default stream: every call completes
+    within its time limits (status 0) and gives bitwise the same output."""
+    import torch
+    wl = make_workload("spec_verify8")
+    dw = DeviceWorkload(wl)
+    dw.step()
+    assert pkv.kv_last_device_status() == 0
+    ref = dw.out.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            dw.attention()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dw.attention()
+    for _ in range(20):
+        g.replay()
+    torch.cuda.synchronize()
+    assert pkv.kv_last_device_status() == 0
+    assert torch.equal(dw.out, ref)
+    for _ in range(60):
+        dw.attention()
+    assert pkv.kv_last_device_status() == 0, pkv.kv_last_device_status_flags()
+    assert torch.equal(dw.out, ref)
