@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int st = jj % KV_STAGES;
             if (jj >= KV_STAGES && !wait_w(bar(B_KVE + st), ((jj - KV_STAGES) / KV_STAGES) & 1)) break;
             const int j = j0 + jj;
-            const int b = j * (BN / BS) + lane;       // lanes 0..3: the tile's 4 blocks
+            const int b = j * (BN / BS) + (lane & 3);
             int32_t id = -1;
             if (lane < BN / BS && b < nblk) id = __ldg(bt + b);
             const bool valid = lane < BN / BS && b < nblk && id >= 0 && id < p.num_blocks;
@@ -447,14 +447,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 f2_unpack(a2, s0, s1);
                 const float sum = s0 + s1;
                 l = l * alpha + sum;
-                // P(jj) overwrites the S buffer PV(jj-2) read: S(jj) was issued after
-                // PV(jj-2) by the same thread and has completed, so PV(jj-2) has too.
-                // Only a rescale of O has to wait for PV(jj-1) (it accumulates into
-                // O); with the lazy rescale most tiles skip both.  PVD is then at
-                // most one phase behind jj - 1, so its parity wait is unambiguous.
-                if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                if (jj > 0) {
+                    // PV(jj-1) finished: O holds every earlier tile, and PV(jj-2), which
+                    // read the P columns about to be overwritten, finished before it
                     if (!wait_w(bar(B_PVD + gi), (jj - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
+                }
+                if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float o[32];
@@ -471,10 +470,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_before();
                 mbar_arrive(bar(B_P + gi));
             }
-            // every product of this tile's issuer, the last PV included, is done;
-            // B_DRAIN's single phase is unambiguous however many PVD phases this
-            // warp skipped above
-            if (ok && wait_w(bar(B_DRAIN + gi), 0)) {
+            if (ok && wait_w(bar(B_PVD + gi), (T - 1) & 1)) {
                 tc_fence_after();
                 const size_t rh = (size_t)(row0 + (row_valid ? i : i0)) * p.hq + head;
                 const size_t pi = rh * p.max_splits + split;
