@@ -360,11 +360,9 @@ __device__ __forceinline__ void griddep_launch_dependents()
 namespace pkv_host {
 // Launch, with programmatic stream serialisation when pdl is set (the kernel
 // calls pkv::griddep_wait() before it reads what earlier kernels produced).
-// Only for a kernel whose predecessor on the stream is a kernel: on a stream
-// fed through an event from another stream it is not used (measured on GB300:
-// decode kernels launched that way on the library's side stream, after calls
-// from a second caller stream, left the concurrent tcgen05 chunk kernel's
-// CTAs waiting past their time limit).
+// Used where the kernel's predecessor on the stream is a kernel (typically the
+// cache write); work on a stream that is fed through an event from another
+// stream launches plainly.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
                       Args &&...args)
