@@ -82,8 +82,7 @@ enum {
     B_SFREE = B_S + 4,              // + 2*group + buffer: the PV reading that buffer's P finished
     B_P = B_SFREE + 4,              // + group: the group's P is in TMEM (128 arrivals)
     B_PVD = B_P + 2,                // + group: the group's latest PV product finished
-    B_PVI = B_PVD + 2,              // + group: the group's latest PV product was issued
-    B_DRAIN = B_PVI + 2,            // + issuer warp - 9: every MMA of that issuer finished
+    B_DRAIN = B_PVD + 2,            // + issuer warp - 9: every MMA of that issuer finished
     B_TAIL = B_DRAIN + 4,           // the V rows past the context are zeroed
     NBAR
 };
@@ -243,7 +242,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bar(B_QR + i), 128);
             mbar_init(bar(B_P + i), 128);
             mbar_init(bar(B_PVD + i), 1);
-            mbar_init(bar(B_PVI + i), 1);
         }
         mbar_init(bar(B_TAIL), 1);
         *abort_flag = 0;
@@ -372,7 +370,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // the stage is released once both tiles' PV products are done
                         // (its K was read by S(jj), which finished before P(jj) existed)
                         umma_commit(bar(B_KVE + jj % KV_STAGES));
-                        mbar_arrive(bar(B_PVI + gi));   // PV(jj) is issued
                     }
                     __syncwarp();
                 }
@@ -467,17 +464,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 f2_unpack(a2, s0, s1);
                 const float sum = s0 + s1;
                 l = l * alpha + sum;
-                // Before arriving for tile jj every warp of the group waits until
-                // PV(jj-1) has been issued -- which needed all 128 arrivals for tile
-                // jj-1 -- so no warp's arrival can count toward another tile's
-                // phase.  P(jj) overwrites the buffer PV(jj-2) read: S(jj) was
-                // written there only after PV(jj-2) had finished (B_SFREE).  Only a
-                // rescale of O waits for PV(jj-1) to finish (PVD is then at most
-                // one phase behind, as PV(jj-2) has finished).
-                if (jj > 0 && !wait_w(bar(B_PVI + gi), (jj - 1) & 1)) { ok = false; break; }
-                if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                if (jj > 0) {
+                    // PV(jj-1) finished: O holds every earlier tile, and PV(jj-2), which
+                    // read the P columns about to be overwritten, finished before it
                     if (!wait_w(bar(B_PVD + gi), (jj - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
+                }
+                if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float o[32];
@@ -494,9 +487,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_before();
                 mbar_arrive(bar(B_P + gi));
             }
-            // every PV of this tile has finished (its issuer's drain barrier has
-            // one phase, unambiguous however many PVD phases were skipped)
-            if (ok && wait_w(bar(B_DRAIN + 2 + gi), 0)) {
+            if (ok && wait_w(bar(B_PVD + gi), (T - 1) & 1)) {
                 tc_fence_after();
                 const size_t rh = (size_t)(row0 + (row_valid ? i : i0)) * p.hq + head;
                 const size_t pi = rh * p.max_splits + split;
