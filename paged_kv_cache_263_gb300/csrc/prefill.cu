@@ -57,10 +57,8 @@ using namespace pkv;
 
 constexpr int BM = 128, BN = 32;               // 128 query rows x 32 keys (2 blocks) per tile
 // warps 0-3 softmax of query tile 0, 4-7 softmax of query tile 1, 8 TMA producer,
-// 9 and 10 issue QK^T of query tile 0 and 1, 11 and 12 issue PV of tile 0 and 1
-// (a thread issues one tcgen05.mma per ~50 cycles; four issuers keep the
-// tensor pipe fed with these narrow products)
-constexpr int THREADS = 416;
+// 9 and 10 MMA issuers of query tile 0 and 1
+constexpr int THREADS = 352;
 constexpr int KV_STAGES = 8;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -69,7 +67,7 @@ constexpr float RESCALE_LOG2 = 8.0f;
 // halves of [32 keys][128 B].
 constexpr uint32_t SKV = 0, KV_STAGE_BYTES = 16384, V_OFF = 8192, KV_HALF = 4096;
 constexpr uint32_t SBAR = SKV + KV_STAGES * KV_STAGE_BYTES;
-constexpr int SMEM_BYTES = SBAR + 512;
+constexpr int SMEM_BYTES = SBAR + 256;
 static_assert(KV_HALF == BN * 128 && V_OFF == 2 * KV_HALF && KV_STAGE_BYTES == 2 * V_OFF, "K/V stage layout");
 static_assert(SBAR == SKV + KV_STAGES * KV_STAGE_BYTES, "shared-memory layout overlaps");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
@@ -79,14 +77,13 @@ enum {
     B_KVE = B_KVF + KV_STAGES,      // + stage: every MMA reading the stage is done
     B_QR = B_KVE + KV_STAGES,       // + group: the group's Q rows are in TMEM (128 arrivals)
     B_S = B_QR + 2,                 // + 2*group + buffer: an S tile of the group is in TMEM
-    B_SFREE = B_S + 4,              // + 2*group + buffer: the PV reading that buffer's P finished
-    B_P = B_SFREE + 4,              // + group: the group's P is in TMEM (128 arrivals)
+    B_P = B_S + 4,                  // + group: the group's P is in TMEM (128 arrivals)
     B_PVD = B_P + 2,                // + group: the group's latest PV product finished
-    B_DRAIN = B_PVD + 2,            // + issuer warp - 9: every MMA of that issuer finished
-    B_TAIL = B_DRAIN + 4,           // the V rows past the context are zeroed
+    B_DRAIN = B_PVD + 2,            // + group: every MMA of the group's issuer finished
+    B_TAIL = B_DRAIN + 2,           // the V rows past the context are zeroed
     NBAR
 };
-static_assert(NBAR * 8 + 8 <= 512, "barrier area");
+static_assert(NBAR * 8 + 8 <= 256, "barrier area");
 
 // instruction descriptors, kind::f16: fp32 accumulate, bf16 A and B, M=128
 constexpr uint32_t idesc(int n, bool b_mn_major)
@@ -233,15 +230,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bar(B_KVF + i), 1);
             mbar_init(bar(B_KVE + i), has1 ? 2 : 1);   // one release per MMA issuer
         }
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(bar(B_S + i), 1);
-            mbar_init(bar(B_SFREE + i), 1);
-            mbar_init(bar(B_DRAIN + i), 1);
-        }
+        for (int i = 0; i < 4; ++i) mbar_init(bar(B_S + i), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_QR + i), 128);
             mbar_init(bar(B_P + i), 128);
             mbar_init(bar(B_PVD + i), 1);
+            mbar_init(bar(B_DRAIN + i), 1);
         }
         mbar_init(bar(B_TAIL), 1);
         *abort_flag = 0;
@@ -313,14 +307,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int jj = max(0, issued - KV_STAGES); jj < issued; ++jj)
                 (void)mbar_wait_bounded(bar(B_KVF + jj % KV_STAGES), (jj / KV_STAGES) & 1);
         }
-    } else if (warp >= 9 && warp <= 12) {
-        // ======================= MMA issuers: QK^T (warps 9, 10) and PV (warps 11, 12)
-        // of query tile gi.  Each thread's products run in its issue order; across
-        // the two threads of a tile the S buffers are handed over by barriers:
-        // S(jj) is read by the softmax, which writes P(jj) over it and arrives on
-        // B_P; PV(jj) then reads P(jj) and frees the buffer (B_SFREE) for S(jj+2).
-        const int gi = (warp - 9) & 1;
-        const bool is_qk = warp <= 10;
+    } else if (warp == 9 || warp == 10) {
+        // ======================= MMA issuers: warp 9 for query tile 0, warp 10 for tile 1
+        const int gi = warp - 9;
         if (gi == 0 || has1) {
             // shared-memory descriptors of stage 0; other stages and K steps are
             // constant byte offsets added to the start-address field (in 16-byte
@@ -329,57 +318,65 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t kdesc0 = sdesc_sw128(sbase + SKV, 16, 1024);
             const uint64_t vdesc0 = sdesc_sw128(sbase + SKV + V_OFF, KV_HALF, 1024);
             const uint32_t to = tO(gi);
-            bool ok = true;
-            if (is_qk) {
-                // S = Q K^T for KV tile jj into S buffer jj % 2: A = Q from TMEM, B = K
-                // (K-major) from smem
-                ok = wait_w(bar(B_QR + gi), 0);
-                for (int jj = 0; jj < T && ok; ++jj) {
-                    const int b = jj & 1;
-                    if (jj >= 2 && !wait_w(bar(B_SFREE + 2 * gi + b), ((jj - 2) >> 1) & 1)) { ok = false; break; }
-                    if (!wait_w(bar(B_KVF + jj % KV_STAGES), (jj / KV_STAGES) & 1)) { ok = false; break; }
-                    if (lane == 0) {
-                        tc_fence_after();
-                        const uint64_t kd = kdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
-                        const uint32_t ts = tS(gi, b);
+            // S = Q K^T for KV tile jj into S buffer jj % 2: A = Q from TMEM, B = K
+            // (K-major) from smem
+            auto issue_s = [&](int jj) {
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint64_t kd = kdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
+                    const uint32_t ts = tS(gi, jj & 1);
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)   // D = 128 in steps of 16: 4 per 64-wide half
-                            umma_f16_ts(ts, tq + kk * 8,
-                                        kd + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4), IDESC_S,
-                                        kk > 0 ? 1u : 0u);
-                        umma_commit(bar(B_S + 2 * gi + b));
-                    }
-                    __syncwarp();
+                    for (int kk = 0; kk < 8; ++kk)   // D = 128 in steps of 16: 4 per 64-wide half
+                        umma_f16_ts(ts, tq + kk * 8, kd + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4),
+                                    IDESC_S, kk > 0 ? 1u : 0u);
+                    umma_commit(bar(B_S + 2 * gi + (jj & 1)));
                 }
-            } else {
-                // O += P V for KV tile jj: A = P from TMEM, B = V (MN-major) from smem;
-                // a tile holding keys >= L is read only after the producer zeroed them
-                for (int jj = 0; jj < T && ok; ++jj) {
-                    if (!wait_w(bar(B_P + gi), jj & 1)) { ok = false; break; }
-                    if ((j0 + jj + 1) * BN > L && !wait_w(bar(B_TAIL), 0)) { ok = false; break; }
-                    if (lane == 0) {
-                        tc_fence_after();
-                        const uint64_t vd = vdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
-                        const uint32_t ts = tS(gi, jj & 1);
+                __syncwarp();
+            };
+            // O += P V for KV tile jj: A = P from TMEM, B = V (MN-major) from smem
+            auto issue_pv = [&](int jj) {
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint64_t vd = vdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
+                    const uint32_t ts = tS(gi, jj & 1);
 #pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)   // 32 keys in steps of 16
-                            umma_f16_ts(to, ts + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), IDESC_PV,
-                                        (jj > 0 || kk > 0) ? 1u : 0u);
-                        umma_commit(bar(B_PVD + gi));
-                        umma_commit(bar(B_SFREE + 2 * gi + (jj & 1)));
-                        // the stage is released once both tiles' PV products are done
-                        // (its K was read by S(jj), which finished before P(jj) existed)
-                        umma_commit(bar(B_KVE + jj % KV_STAGES));
-                    }
-                    __syncwarp();
+                    for (int kk = 0; kk < BN / 16; ++kk)   // 32 keys in steps of 16
+                        umma_f16_ts(to, ts + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), IDESC_PV,
+                                    (jj > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(bar(B_PVD + gi));
+                    // the stage is released once both issuers' MMAs reading it are done
+                    umma_commit(bar(B_KVE + jj % KV_STAGES));
+                }
+                __syncwarp();
+            };
+            // a tile holding keys >= L is read by PV only after the producer zeroed them
+            auto tail_ready = [&](int jj) -> bool {
+                return (j0 + jj + 1) * BN <= L || wait_w(bar(B_TAIL), 0);
+            };
+            // S of the first two tiles up front; afterwards S(jj+2) follows PV(jj), so
+            // each softmax finds its S computed while it worked on the tile before
+            bool ok = wait_w(bar(B_QR + gi), 0);
+            for (int jj = 0; ok && jj < min(2, T); ++jj) {
+                if (!wait_w(bar(B_KVF + jj), 0)) { ok = false; break; }
+                issue_s(jj);
+            }
+            for (int jj = 0; jj < T && ok; ++jj) {
+                if (!wait_w(bar(B_P + gi), jj & 1) || !tail_ready(jj)) { ok = false; break; }
+                // in issue order: PV(jj) reads P from S buffer jj % 2 before S(jj+2)
+                // overwrites it
+                issue_pv(jj);
+                if (jj + 2 < T) {
+                    const int sn = (jj + 2) % KV_STAGES;
+                    if (!wait_w(bar(B_KVF + sn), ((jj + 2) / KV_STAGES) & 1)) { ok = false; break; }
+                    issue_s(jj + 2);
                 }
             }
             // every MMA this issuer started has finished before TMEM is released
-            if (lane == 0) umma_commit(bar(B_DRAIN + warp - 9));
+            if (lane == 0) umma_commit(bar(B_DRAIN + gi));
             __syncwarp();
-            (void)mbar_wait_bounded(bar(B_DRAIN + warp - 9), 0);
+            (void)mbar_wait_bounded(bar(B_DRAIN + gi), 0);
         }
-    } else if (warp < 8) {
+    } else {
         // ======================= softmax warpgroups: thread = query row = TMEM lane
         const int gi = warp >> 2;                  // which query tile of the pair
         if (gi == 0 || has1) {
