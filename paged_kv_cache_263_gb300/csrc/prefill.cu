@@ -55,28 +55,27 @@ __device__ uint32_t g_status;
 
 using namespace pkv;
 
-constexpr int BM = 128, BN = 32;               // 128 query rows x 32 keys (2 blocks) per tile
+constexpr int BM = 128, BN = 64;               // 128 query rows x 64 keys (4 blocks) per tile
 // warps 0-3 softmax of query tile 0, 4-7 softmax of query tile 1, 8 TMA producer,
 // 9 and 10 MMA issuers of query tile 0 and 1
 constexpr int THREADS = 352;
-constexpr int KV_STAGES = 8;
+constexpr int KV_STAGES = 4;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
-// shared memory: 8 stages of (K 8 KiB, V 8 KiB) | barriers.  Q and P live in tensor
-// memory, so shared memory streams only K and V.  A K or V tile is two 64-column
-// halves of [32 keys][128 B].
-constexpr uint32_t SKV = 0, KV_STAGE_BYTES = 16384, V_OFF = 8192, KV_HALF = 4096;
+// shared memory: Q 2 x 32 KiB | 4 stages of (K 16 KiB, V 16 KiB) | barriers.  P lives
+// in tensor memory.
+constexpr uint32_t SQ = 0, Q_TILE = 32768;
+constexpr uint32_t SKV = 65536, KV_STAGE_BYTES = 32768, V_OFF = 16384, KV_HALF = 8192;
 constexpr uint32_t SBAR = SKV + KV_STAGES * KV_STAGE_BYTES;
 constexpr int SMEM_BYTES = SBAR + 256;
-static_assert(KV_HALF == BN * 128 && V_OFF == 2 * KV_HALF && KV_STAGE_BYTES == 2 * V_OFF, "K/V stage layout");
-static_assert(SBAR == SKV + KV_STAGES * KV_STAGE_BYTES, "shared-memory layout overlaps");
+static_assert(SKV >= 2 * 32768 && SBAR == SKV + KV_STAGES * KV_STAGE_BYTES, "shared-memory layout overlaps");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 // barriers
 enum {
     B_KVF = 0,                      // + stage: K and V of a tile landed
     B_KVE = B_KVF + KV_STAGES,      // + stage: every MMA reading the stage is done
-    B_QR = B_KVE + KV_STAGES,       // + group: the group's Q rows are in TMEM (128 arrivals)
-    B_S = B_QR + 2,                 // + 2*group + buffer: an S tile of the group is in TMEM
+    B_Q = B_KVE + KV_STAGES,        // both Q tiles landed
+    B_S = B_Q + 1,                  // + 2*group + buffer: an S tile of the group is in TMEM
     B_P = B_S + 4,                  // + group: the group's P is in TMEM (128 arrivals)
     B_PVD = B_P + 2,                // + group: the group's latest PV product finished
     B_DRAIN = B_PVD + 2,            // + group: every MMA of the group's issuer finished
@@ -91,7 +90,7 @@ constexpr uint32_t idesc(int n, bool b_mn_major)
     return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(BM >> 4) << 24);
 }
-constexpr uint32_t IDESC_S = idesc(BN, false);    // S[128 x 32] = Q K^T, K K-major
+constexpr uint32_t IDESC_S = idesc(BN, false);    // S[128 x 64] = Q K^T, K K-major
 constexpr uint32_t IDESC_PV = idesc(D, true);     // O[128 x 128] += P V, V MN-major
 
 struct PrefillParams {
@@ -179,7 +178,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap kmap,
+    prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -230,9 +229,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bar(B_KVF + i), 1);
             mbar_init(bar(B_KVE + i), has1 ? 2 : 1);   // one release per MMA issuer
         }
+        mbar_init(bar(B_Q), 1);
         for (int i = 0; i < 4; ++i) mbar_init(bar(B_S + i), 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_QR + i), 128);
             mbar_init(bar(B_P + i), 128);
             mbar_init(bar(B_PVD + i), 1);
             mbar_init(bar(B_DRAIN + i), 1);
@@ -249,17 +248,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // TMEM columns per query tile gi, 256 gi + : Q 0..63 (bf16 pairs, the A operand
-    // of QK^T), two S buffers of 32 fp32 columns at 64 and 96 (P overwrites the
-    // first 16 of a buffer with bf16 pairs once its S has been read), O 128..255
-    auto tQ = [&](int gi) -> uint32_t { return tmem + gi * 256; };
-    auto tS = [&](int gi, int b) -> uint32_t { return tmem + gi * 256 + 64 + b * BN; };
-    auto tO = [&](int gi) -> uint32_t { return tmem + gi * 256 + 128; };
+    // TMEM columns per query tile gi: two S buffers of 64 fp32 columns at
+    // 128 gi + 64 b (P overwrites the first 32 of a buffer with bf16 pairs once its
+    // S has been read), O at 256 + 128 gi
+    auto tS = [&](int gi, int b) -> uint32_t { return tmem + gi * 128 + b * BN; };
+    auto tO = [&](int gi) -> uint32_t { return tmem + 256 + gi * D; };
 
     if (warp == 8) {
         // ======================= TMA producer
         const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks;
         const int nblk = (L + BS - 1) / BS;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(B_Q), (has1 ? 4 : 2) * 16384);
+            for (int gi = 0; gi < (has1 ? 2 : 1); ++gi) {
+                const int zq = row0 + (2 * pair + gi) * tpt;
+                tma_load_3d(sbase + SQ + gi * Q_TILE, &qmap, 0, g * G, zq, bar(B_Q));
+                tma_load_3d(sbase + SQ + gi * Q_TILE + 16384, &qmap, 64, g * G, zq, bar(B_Q));
+            }
+        }
         int issued = 0;
         for (int jj = 0; jj < T; ++jj) {
             const int st = jj % KV_STAGES;
@@ -314,12 +320,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             // shared-memory descriptors of stage 0; other stages and K steps are
             // constant byte offsets added to the start-address field (in 16-byte
             // units; shared memory is < 256 KiB, so the 14-bit field never carries)
-            const uint32_t tq = tQ(gi);
+            const uint64_t qdesc = sdesc_sw128(sbase + SQ + gi * Q_TILE, 16, 1024);
             const uint64_t kdesc0 = sdesc_sw128(sbase + SKV, 16, 1024);
             const uint64_t vdesc0 = sdesc_sw128(sbase + SKV + V_OFF, KV_HALF, 1024);
             const uint32_t to = tO(gi);
-            // S = Q K^T for KV tile jj into S buffer jj % 2: A = Q from TMEM, B = K
-            // (K-major) from smem
+            // S = Q K^T for KV tile jj into S buffer jj % 2: A = Q, B = K (K-major)
             auto issue_s = [&](int jj) {
                 if (lane == 0) {
                     tc_fence_after();
@@ -327,8 +332,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t ts = tS(gi, jj & 1);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)   // D = 128 in steps of 16: 4 per 64-wide half
-                        umma_f16_ts(ts, tq + kk * 8, kd + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4),
-                                    IDESC_S, kk > 0 ? 1u : 0u);
+                        umma_f16(ts, qdesc + (uint64_t)((((kk >> 2) * 16384) + (kk & 3) * 32) >> 4),
+                                 kd + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4), IDESC_S, kk > 0);
                     umma_commit(bar(B_S + 2 * gi + (jj & 1)));
                 }
                 __syncwarp();
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint64_t vd = vdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
                     const uint32_t ts = tS(gi, jj & 1);
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)   // 32 keys in steps of 16
+                    for (int kk = 0; kk < BN / 16; ++kk)   // 64 keys in steps of 16
                         umma_f16_ts(to, ts + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), IDESC_PV,
                                     (jj > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(bar(B_PVD + gi));
@@ -355,7 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             };
             // S of the first two tiles up front; afterwards S(jj+2) follows PV(jj), so
             // each softmax finds its S computed while it worked on the tile before
-            bool ok = wait_w(bar(B_QR + gi), 0);
+            bool ok = wait_w(bar(B_Q), 0);
             for (int jj = 0; ok && jj < min(2, T); ++jj) {
                 if (!wait_w(bar(B_KVF + jj), 0)) { ok = false; break; }
                 issue_s(jj);
@@ -391,25 +396,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int pos = row_valid ? L - n + i : L - n + i1 - 1;
             const int pos_min = L - n + i0;
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-            {
-                // this row of Q into the tile's Q columns (bf16 pairs: column c holds
-                // d = 2c, 2c + 1), once; rows past the chunk are zero
-                uint32_t qw[64];
-                const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + ((size_t)(row0 + i) * p.hq + head) * D);
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const uint4 v = row_valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
-                    qw[4 * c] = v.x;
-                    qw[4 * c + 1] = v.y;
-                    qw[4 * c + 2] = v.z;
-                    qw[4 * c + 3] = v.w;
-                }
-                tmem_st32u(tQ(gi) + lane_base, *reinterpret_cast<const uint32_t(*)[32]>(qw));
-                tmem_st32u(tQ(gi) + lane_base + 32, *reinterpret_cast<const uint32_t(*)[32]>(qw + 32));
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(bar(B_QR + gi));
-            }
             float m_ref = -INFINITY, l = 0.f;
             bool ok = true;
             for (int jj = 0; jj < T && ok; ++jj) {
@@ -417,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!wait_w(bar(B_S + 2 * gi + (jj & 1)), (jj >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 float sv[BN];
-                tmem_ld32(tS(gi, jj & 1) + lane_base, sv);
+                tmem_ld64(tS(gi, jj & 1) + lane_base, sv);
                 // raw scores; the scale (> 0) is applied inside the exponent's FFMA,
                 // so the max is taken on the raw values
                 if (t0 + BN - 1 > pos_min) {             // diagonal tile: causal mask
@@ -425,7 +411,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int c = 0; c < BN; ++c)
                         if (t0 + c > pos) sv[c] = -INFINITY;
                 }
-                // max over the 32 scores: four independent chains of 3-input maxima
+                // max over the 64 scores: four independent chains of 3-input maxima
                 float mk[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) mk[k] = fmaxf(sv[k], sv[4 + k]);        // elements 0..7
@@ -477,9 +463,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         tmem_st32(tO(gi) + lane_base + c * 32, o);
                     }
                 }
-                // P in bf16 pairs over the first 16 columns of the S buffer (the A
+                // P in bf16 pairs over the first 32 columns of the S buffer (the A
                 // operand of PV)
-                tmem_st16u(tS(gi, jj & 1) + lane_base, pw);
+                tmem_st32u(tS(gi, jj & 1) + lane_base, pw);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(B_P + gi));
@@ -787,8 +773,12 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     p.tiles_per_split = pl.tiles_per_split;
     p.max_splits = std::max(1, pl.max_splits);
     p.scale_log2 = scale * LOG2E;
-    CUtensorMap km, vm;
+    CUtensorMap qm, km, vm;
     const int tpt = BM / G;
+    if (!pkv_host::encode_tmap_3d(&qm, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, num_q_heads, total_q_tokens,
+                                  (uint64_t)D * 2, (uint64_t)num_q_heads * D * 2, 64, G, tpt,
+                                  CU_TENSOR_MAP_SWIZZLE_128B))
+        return KV_ERR_CUDA;
     if (!pkv_decode::make_maps(k_cache, v_cache, num_blocks, num_kv_heads, dtype, &km, &vm)) return KV_ERR_CUDA;
     static bool configured = false;
     if (!configured) {
@@ -802,7 +792,7 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     const int64_t tiles_ub = (total_q_tokens + tpt - 1) / tpt + std::min<int64_t>(num_seqs, total_q_tokens / 2);
     if (tiles_ub > INT32_MAX || p.max_splits > 65535) return KV_ERR_UNSUPPORTED;
     dim3 grid((unsigned)tiles_ub, num_kv_heads, p.max_splits);
-    prefill_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(km, vm, p);
+    prefill_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(qm, km, vm, p);
     if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
     if (p.max_splits > 1) {
         const int64_t warps = (int64_t)total_q_tokens * num_q_heads;
