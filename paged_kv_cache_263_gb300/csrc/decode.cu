@@ -48,7 +48,6 @@ using namespace pkv;
 constexpr int WARPS = 4;
 constexpr int THREADS = WARPS * 32;
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr float RESCALE_LOG2 = 8.0f;
 
 struct DecodeParams {
     float *out;
@@ -392,14 +391,7 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
                     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
                 }
-                // lazy rescale: the reference max moves only when a block's max
-                // exceeds it by more than 2^RESCALE_LOG2 (p stays <= 2^8, exact in
-                // the end since l and O share the reference); until then O and l
-                // need no rescaling
-                const float mn0 = (mx0 > m[nt][0] + RESCALE_LOG2 || m[nt][0] == -INFINITY) ? fmaxf(m[nt][0], mx0)
-                                                                                          : m[nt][0];
-                const float mn1 = (mx1 > m[nt][1] + RESCALE_LOG2 || m[nt][1] == -INFINITY) ? fmaxf(m[nt][1], mx1)
-                                                                                          : m[nt][1];
+                const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
                 // MR: a column may have seen no key yet (all masked): exponents are
                 // taken against 0 then, so p = 0 and nothing becomes NaN
                 const float r0 = (MR && mn0 == -INFINITY) ? 0.f : mn0;
@@ -411,14 +403,12 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
                 const float p2 = ex2(x[2] - r0), p3 = ex2(x[3] - r1);
                 l[nt][0] = l[nt][0] * al0 + (p0 + p2);
                 l[nt][1] = l[nt][1] * al1 + (p1 + p3);
-                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        o[nt][j][0] *= al0;
-                        o[nt][j][1] *= al1;
-                        o[nt][j][2] *= al0;
-                        o[nt][j][3] *= al1;
-                    }
+                for (int j = 0; j < 8; ++j) {
+                    o[nt][j][0] *= al0;
+                    o[nt][j][1] *= al1;
+                    o[nt][j][2] *= al0;
+                    o[nt][j][3] *= al1;
                 }
                 if constexpr (!FP8) {
                     pb[nt][0] = movmatrix_t(pack_bf16(p0, p1));
