@@ -295,6 +295,11 @@ def run_ours(args):
 
     pkv_build.build()
     wl = make_workload(args.workload)
+    if args.placement == "contiguous":
+        # the paged-vs-contiguous comparison: the pool hands out blocks in
+        # ascending order, so every sequence's blocks are consecutive in HBM
+        import numpy as np
+        wl.free_order = np.arange(wl.num_blocks, dtype=np.int32)
     dw = DeviceWorkload(wl, device=dev)
     ab = dw.algorithmic_bytes()
     stream = torch.cuda.current_stream(dev)
@@ -490,7 +495,8 @@ def run_ours(args):
                    "kv_bytes_per_step": kv_bytes, "algorithmic_bytes_per_step": step_bytes,
                    "l2": f"no flush: every step reads {kv_bytes / 1e6:.0f} MB of KV, "
                          f"{kv_bytes / L2_BYTES:.1f}x the 129 MB L2",
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "placement": args.placement},
         "roofline": roofline,
         "cache_write_avg_ms": statistics.mean(write_ms),
         "timing": ("CUDA graph replay of the captured step (cache write + attention); roofline per call "
@@ -715,6 +721,9 @@ def main():
     ap.add_argument("--ref-seqs", type=int, default=16)
     ap.add_argument("--ref-budget", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--placement", default="random", choices=["random", "contiguous"],
+                    help="physical block placement: the workload's seeded random order, or ascending "
+                         "(each sequence's blocks consecutive) for the paged-vs-contiguous comparison")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
