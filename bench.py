@@ -503,9 +503,11 @@ def run_ours(args):
                    "from a graph of the attention call alone") if graphs else
                   f"eager calls (graph capture failed: {graph_error})",
         "eager": {"ms_per_step": eager_ms, "attention_call_ms": statistics.mean(attn_ms), "steps": KE},
-        "e2e": {"value": weak_scaling_value(step_bytes, ws, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "timing": e2e_kind,
-                "eager": {"value": weak_scaling_value(step_bytes, ws, e2e_eager_ms), "ms_per_step": e2e_eager_ms}},
+        "e2e": {"value": weak_scaling_value(step_bytes, ws, e2e_eager_ms), "unit": UNIT,
+                "ms_per_step": e2e_eager_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "timing": "eager calls of the public API, copies included",
+                "graph": {"value": weak_scaling_value(step_bytes, ws, e2e_ms), "ms_per_step": e2e_ms,
+                          "timing": e2e_kind}},
         "gpu_launches": launches_per_step * K,
         "clocks": ck,
     }
