@@ -107,3 +107,31 @@ class PoolModel:
 def blocks_for(tokens: int, block_size: int = 16) -> int:
     """Number of blocks a sequence of ``tokens`` tokens occupies (ceil division)."""
     return -(-int(tokens) // block_size)
+
+
+def waste_stats(lens, reservation_tokens: int, block_size: int = 16) -> dict:
+    """Memory waste of a set of requests, contiguous against paged
+    ["Waste, and three ways to reclaim it", "PagedAttention" (the worked example:
+    four requests each reserving a whole maximum-length buffer) and "Small block
+    size" (internal waste capped at block_size - 1 tokens per sequence)].
+
+    Contiguous: every request reserves ``reservation_tokens`` slots; the slots no
+    token uses are untouched.  Paged: every request holds ceil(len / block_size)
+    blocks; the unused slots of its last block are the internal waste."""
+    lens = [int(x) for x in lens]
+    if any(L < 0 or L > reservation_tokens for L in lens) or reservation_tokens < 0:
+        raise PoolError(ERR_INVALID, "length outside the reservation")
+    used = sum(lens)
+    reserved = reservation_tokens * len(lens)
+    blocks = sum(blocks_for(L, block_size) for L in lens)
+    slots = blocks * block_size
+    return {
+        "used_tokens": used,
+        "contiguous_reserved_slots": reserved,
+        "contiguous_untouched_slots": reserved - used,
+        "contiguous_untouched_percent": 100.0 * (reserved - used) / reserved if reserved else 0.0,
+        "paged_blocks": blocks,
+        "paged_slots": slots,
+        "paged_waste_slots": slots - used,
+        "paged_waste_percent": 100.0 * (slots - used) / slots if slots else 0.0,
+    }

@@ -2,7 +2,7 @@
 import numpy as np
 import pytest
 
-from oracle.allocator import ERR_INVALID, ERR_OUT_OF_BLOCKS, PoolError, PoolModel, blocks_for
+from oracle.allocator import ERR_INVALID, ERR_OUT_OF_BLOCKS, PoolError, PoolModel, blocks_for, waste_stats
 
 
 def test_worked_allocation_example(golden):
@@ -148,3 +148,25 @@ def test_duplicate_ids_in_one_free_call():
     with pytest.raises(PoolError):
         pool.free([c, c])                                # only one reference
     assert pool.ref[c] == 1
+
+
+def test_waste_stats_on_the_worked_example(golden):
+    """The statistic on the pages' four requests: 25,468 of 32,768 reserved slots
+    untouched (77.72 %), 457 paged blocks with 12 slots of internal waste."""
+    kv, _ = golden("worked_allocation_example.txt")
+    used = [int(x) for x in kv["used_tokens"].split()]
+    w = waste_stats(used, int(kv["reservation_tokens"]), int(kv["block_size"]))
+    assert w["contiguous_reserved_slots"] == 32768 and w["contiguous_untouched_slots"] == 25468
+    assert abs(w["contiguous_untouched_percent"] - 77.72) < 0.01
+    assert (w["paged_blocks"], w["paged_waste_slots"]) == (457, 12)
+    assert abs(w["paged_waste_percent"] - 100 * 12 / 7312) < 1e-12
+
+
+def test_waste_stats_closed_forms():
+    # block-aligned lengths waste nothing when paged; one token per request wastes 15
+    w = waste_stats([16, 32, 4096], 8192)
+    assert w["paged_waste_slots"] == 0 and w["paged_blocks"] == 1 + 2 + 256
+    w = waste_stats([1] * 10, 16)
+    assert w["paged_waste_slots"] == 150 and w["contiguous_untouched_slots"] == 150
+    with pytest.raises(PoolError):
+        waste_stats([9000], 8192)
