@@ -141,6 +141,29 @@ PAGEDKV_API kv_status kv_block_refcount(const kv_pool *pool, int32_t id, int32_t
 
 PAGEDKV_API kv_status kv_pool_stats(const kv_pool *pool, kv_pool_stats_t *out);
 
+/* Memory waste of a set of requests, contiguous against paged ([P2]
+ * "PagedAttention": each request reserving a maximum-length buffer leaves most
+ * of it untouched; "Small block size": paged waste is at most 15 tokens per
+ * sequence; [P3] block management (a), (f) efficiency tracking).
+ *  lens                host int32 [n], tokens of each request, 0..reservation_tokens
+ *  reservation_tokens  slots a contiguous allocator reserves per request
+ *  Contiguous: n x reservation_tokens slots reserved, those no token uses are
+ *  untouched.  Paged: ceil(len/16) blocks per request; the unused slots of each
+ *  last block are the waste.  KV_ERR_INVALID for a length outside the range. */
+typedef struct {
+    int64_t used_tokens;
+    int64_t contiguous_reserved_slots;
+    int64_t contiguous_untouched_slots;
+    int64_t paged_blocks;
+    int64_t paged_slots;
+    int64_t paged_waste_slots;
+    double contiguous_untouched_percent;
+    double paged_waste_percent;
+} kv_waste_stats_t;
+
+PAGEDKV_API kv_status kv_waste_stats(const int32_t *lens, int32_t n, int32_t reservation_tokens,
+                                     kv_waste_stats_t *out);
+
 /* Host fault injection: the k-th kv_block_alloc call from now (k >= 1),
  * including the allocation inside kv_copy_on_write, fails with
  * KV_ERR_OUT_OF_BLOCKS exactly as if the pool were empty; k <= 0 disarms. */

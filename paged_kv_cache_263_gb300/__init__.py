@@ -18,7 +18,7 @@ __all__ = [
     "paged_attention_workspace_size", "paged_attention_decode",
     "paged_attention_chunked_prefill_workspace_size", "paged_attention_chunked_prefill",
     "kv_last_device_status", "kv_last_device_status_flags", "KV_BF16", "KV_FP8_E4M3",
-    "HEAD_DIM", "BLOCK_SIZE", "library_path", "PrefixCache", "kv_swap_out", "kv_swap_in",
+    "HEAD_DIM", "BLOCK_SIZE", "library_path", "PrefixCache", "kv_swap_out", "kv_swap_in", "kv_waste_stats",
 ]
 
 HEAD_DIM = 128
@@ -51,6 +51,13 @@ class _PrefixStats(ctypes.Structure):
                 ("evictable_blocks", ctypes.c_int32)]
 
 
+class _WasteStats(ctypes.Structure):
+    _fields_ = [("used_tokens", ctypes.c_int64), ("contiguous_reserved_slots", ctypes.c_int64),
+                ("contiguous_untouched_slots", ctypes.c_int64), ("paged_blocks", ctypes.c_int64),
+                ("paged_slots", ctypes.c_int64), ("paged_waste_slots", ctypes.c_int64),
+                ("contiguous_untouched_percent", ctypes.c_double), ("paged_waste_percent", ctypes.c_double)]
+
+
 def lib():
     """The loaded library; raises if it has not been built."""
     global _lib
@@ -71,6 +78,7 @@ def lib():
             "kv_block_refcount": (c.c_int, [P, I, c.POINTER(I)]),
             "kv_pool_stats": (c.c_int, [P, c.POINTER(_Stats)]),
             "kv_pool_fail_alloc_after": (c.c_int, [P, I]),
+            "kv_waste_stats": (c.c_int, [P, I, I, c.POINTER(_WasteStats)]),
             "kv_prefix_cache_create": (c.c_int, [P, c.POINTER(P)]),
             "kv_prefix_cache_destroy": (None, [P]),
             "kv_prefix_match": (c.c_int, [P, P, I, c.c_uint64, I, P, c.POINTER(I)]),
@@ -214,6 +222,16 @@ class KVPool:
 
     def fail_alloc_after(self, k: int):
         _check(lib().kv_pool_fail_alloc_after(self._p, int(k)), "kv_pool_fail_alloc_after")
+
+
+def kv_waste_stats(lens, reservation_tokens: int) -> dict:
+    """Contiguous-vs-paged memory waste of requests of the given lengths."""
+    import numpy as np
+    a = np.ascontiguousarray(lens, dtype=np.int32)
+    w = _WasteStats()
+    _check(lib().kv_waste_stats(a.ctypes.data_as(ctypes.c_void_p), a.size, int(reservation_tokens),
+                                ctypes.byref(w)), "kv_waste_stats")
+    return {f: getattr(w, f) for f, _ in _WasteStats._fields_}
 
 
 class PrefixCache:

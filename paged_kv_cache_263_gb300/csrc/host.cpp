@@ -210,6 +210,30 @@ kv_status kv_pool_stats(const kv_pool *pool, kv_pool_stats_t *out)
     return KV_OK;
 }
 
+kv_status kv_waste_stats(const int32_t *lens, int32_t n, int32_t reservation_tokens, kv_waste_stats_t *out)
+{
+    if (!out || n < 0 || reservation_tokens < 0 || (n > 0 && !lens)) return KV_ERR_INVALID;
+    int64_t used = 0, blocks = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        if (lens[i] < 0 || lens[i] > reservation_tokens) return KV_ERR_INVALID;
+        used += lens[i];
+        blocks += (lens[i] + 15) / 16;
+    }
+    out->used_tokens = used;
+    out->contiguous_reserved_slots = (int64_t)reservation_tokens * n;
+    out->contiguous_untouched_slots = out->contiguous_reserved_slots - used;
+    out->paged_blocks = blocks;
+    out->paged_slots = blocks * 16;
+    out->paged_waste_slots = out->paged_slots - used;
+    out->contiguous_untouched_percent =
+        out->contiguous_reserved_slots ? 100.0 * (double)out->contiguous_untouched_slots /
+                                             (double)out->contiguous_reserved_slots
+                                       : 0.0;
+    out->paged_waste_percent =
+        out->paged_slots ? 100.0 * (double)out->paged_waste_slots / (double)out->paged_slots : 0.0;
+    return KV_OK;
+}
+
 kv_status kv_pool_fail_alloc_after(kv_pool *pool, int32_t k)
 {
     if (!pool) return KV_ERR_INVALID;

@@ -140,3 +140,18 @@ def test_destroy_releases_the_cache_references():
     assert pool.stats()["free"] == 13
     cache.close()
     assert pool.stats()["free"] == 16
+
+
+def test_waste_stats_match_the_model():
+    from oracle.allocator import waste_stats
+    rng = np.random.default_rng(21)
+    for n, res in ((4, 8192), (100, 32768), (1, 16), (0, 100)):
+        lens = rng.integers(0, res + 1, size=n)
+        got = pkv.kv_waste_stats(lens, res)
+        want = waste_stats(lens, res)
+        for k, v in want.items():
+            assert got[k] == pytest.approx(v, rel=1e-12, abs=1e-12), k
+    got = pkv.kv_waste_stats([300, 2000, 600, 4400], 8192)
+    assert got["contiguous_untouched_slots"] == 25468 and got["paged_waste_slots"] == 12
+    with pytest.raises(pkv.KVError):
+        pkv.kv_waste_stats([9000], 8192)
