@@ -238,7 +238,8 @@ int oracle_paged_attention(double *out, const uint16_t *q, const void *k_cache,
     for (int s = 0; s < B; ++s) {
         int n = cu_q_lens ? cu_q_lens[s + 1] - cu_q_lens[s] : 1;
         int64_t L = context_lens[s];
-        if (n < 1 || L < n || L > (int64_t)max_blocks * block_size) return -1;
+        /* a sequence may contribute no query rows (n = 0): it has no output */
+        if (n < 0 || L < 1 || L < n || L > (int64_t)max_blocks * block_size) return -1;
         for (int64_t j = 0; j < (L + block_size - 1) / block_size; ++j) {
             int32_t b = block_tables[(int64_t)s * max_blocks + j];
             if (b < 0 || b >= num_blocks) return -2;

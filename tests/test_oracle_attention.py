@@ -294,3 +294,16 @@ def test_fp8_paged_matches_dequantised_contiguous():
     cu = wl.cu_q_lens
     for s in range(2):
         assert np.array_equal(model.expected_rows(wl, s), full[cu[s]:cu[s + 1]])
+
+
+def test_sequence_without_query_rows_has_no_output_and_changes_nothing():
+    """A sequence contributing no rows to a mixed batch (n = 0, the chunk-row
+    definition over an empty range) leaves every other row as it is without it."""
+    import numpy as np
+    from oracle import model as om
+    from synth.workloads import small_workload
+    wl = small_workload(77, lens=[100, 50, 300, 17], q_lens=[5, 0, 1, 0], hq=8, hkv=2)
+    full = om.expected_paged(wl)
+    assert full.shape[0] == 6
+    assert np.array_equal(full[0:5], om.expected_rows(wl, 0))
+    assert np.array_equal(full[5:6], om.expected_rows(wl, 2))
