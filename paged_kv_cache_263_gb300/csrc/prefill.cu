@@ -56,33 +56,46 @@ __device__ uint32_t g_status;
 using namespace pkv;
 
 constexpr int BM = 128, BN = 64;               // 128 query rows x 64 keys (4 blocks) per tile
-// warps 0-3 softmax of query tile 0, 4-7 softmax of query tile 1, 8 TMA producer,
-// 9 and 10 MMA issuers of query tile 0 and 1
-constexpr int THREADS = 352;
-constexpr int KV_STAGES = 4;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
-// shared memory: Q 2 x 32 KiB | 4 stages of (K 16 KiB, V 16 KiB) | barriers.  P lives
-// in tensor memory.
+// shared memory: Q 2 x 32 KiB | K/V operand stages of (K 16 KiB, V 16 KiB) | (fp8
+// cache: e4m3 staging stages of (K 8 KiB, V 8 KiB)) | barriers.  P lives in
+// tensor memory.
 constexpr uint32_t SQ = 0, Q_TILE = 32768;
 constexpr uint32_t SKV = 65536, KV_STAGE_BYTES = 32768, V_OFF = 16384, KV_HALF = 8192;
-constexpr uint32_t SBAR = SKV + KV_STAGES * KV_STAGE_BYTES;
-constexpr int SMEM_BYTES = SBAR + 256;
-static_assert(SKV >= 2 * 32768 && SBAR == SKV + KV_STAGES * KV_STAGE_BYTES, "shared-memory layout overlaps");
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-// barriers
+constexpr uint32_t F8_STAGE_BYTES = 16384, F8_V_OFF = 8192;
+// bf16 cache: warps 0-3 softmax of query tile 0, 4-7 softmax of query tile 1, 8 TMA
+// producer, 9 and 10 MMA issuers of query tile 0 and 1.  fp8 cache: in addition
+// warps 11-14 widen each e4m3 K/V tile to f16 operand tiles (the products then
+// run in kind::f16 with f16 operands: e4m3 -> f16 is exact, and Q is converted
+// to f16 once in shared memory).
+template <bool FP8>
+struct Lay {
+    static constexpr int THREADS = FP8 ? 480 : 352;
+    static constexpr int KV_STAGES = FP8 ? 3 : 4;
+    static constexpr int F8_STAGES = FP8 ? 3 : 0;
+    static constexpr uint32_t SF8 = SKV + KV_STAGES * KV_STAGE_BYTES;
+    static constexpr uint32_t SBAR = SF8 + F8_STAGES * F8_STAGE_BYTES;
+    static constexpr int SMEM_BYTES = SBAR + 512;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
+static_assert(SKV >= 2 * 32768, "shared-memory layout overlaps");
+// barriers (room for the larger of the two layouts)
 enum {
-    B_KVF = 0,                      // + stage: K and V of a tile landed
-    B_KVE = B_KVF + KV_STAGES,      // + stage: every MMA reading the stage is done
-    B_Q = B_KVE + KV_STAGES,        // both Q tiles landed
-    B_S = B_Q + 1,                  // + 2*group + buffer: an S tile of the group is in TMEM
+    B_KVF = 0,                      // + stage: K and V operand tiles ready
+    B_KVE = B_KVF + 4,              // + stage: every MMA reading the stage is done
+    B_Q = B_KVE + 4,                // both Q tiles landed
+    B_QC = B_Q + 1,                 // + group: fp8 cache: the group's Q tile is in f16
+    B_S = B_QC + 2,                 // + 2*group + buffer: an S tile of the group is in TMEM
     B_P = B_S + 4,                  // + group: the group's P is in TMEM (128 arrivals)
     B_PVD = B_P + 2,                // + group: the group's latest PV product finished
     B_DRAIN = B_PVD + 2,            // + group: every MMA of the group's issuer finished
-    B_TAIL = B_DRAIN + 2,           // the V rows past the context are zeroed
-    NBAR
+    B_TAIL = B_DRAIN + 2,           // bf16 cache: the V rows past the context are zeroed
+    B_F8F = B_TAIL + 1,             // + staging stage: fp8 cache: e4m3 K and V landed
+    B_F8E = B_F8F + 3,              // + staging stage: fp8 cache: the stage was widened
+    NBAR = B_F8E + 3
 };
-static_assert(NBAR * 8 + 8 <= 256, "barrier area");
+static_assert(NBAR * 8 + 8 <= 512, "barrier area");
 
 // instruction descriptors, kind::f16: fp32 accumulate, bf16 A and B, M=128
 constexpr uint32_t idesc(int n, bool b_mn_major)
@@ -92,6 +105,10 @@ constexpr uint32_t idesc(int n, bool b_mn_major)
 }
 constexpr uint32_t IDESC_S = idesc(BN, false);    // S[128 x 64] = Q K^T, K K-major
 constexpr uint32_t IDESC_PV = idesc(D, true);     // O[128 x 128] += P V, V MN-major
+// the same with f16 A and B (fp8 cache widened to f16)
+constexpr uint32_t F16_OPS = (1u << 7) | (1u << 10);
+constexpr uint32_t IDESC_S16 = IDESC_S & ~F16_OPS;
+constexpr uint32_t IDESC_PV16 = IDESC_PV & ~F16_OPS;
 
 struct PrefillParams {
     float *out;
@@ -105,6 +122,8 @@ struct PrefillParams {
     int max_blocks, num_seqs, hq, hkv, group, num_blocks, total_rows;
     int tiles_per_split, max_splits;
     float scale_log2;
+    const float *k_scale;  // fp8 cache: [Hkv] (folded into the softmax scale)
+    const float *v_scale;  // fp8 cache: [Hkv] (applied to O)
 };
 
 __device__ __forceinline__ void flag(uint32_t bits) { atomicOr(&g_status, bits); }
@@ -177,14 +196,18 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     if (threadIdx.x == 0) p.tile_off[0] = 0;
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+// (the fp8 variant declares 512 threads so that registers stay <= 128, which 15
+// warps need on an SM partition holding four of them)
+template <bool FP8>
+__global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p)
 {
+    constexpr int KV_STAGES = Lay<FP8>::KV_STAGES, F8_STAGES = Lay<FP8>::F8_STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SBAR);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay<FP8>::SBAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     auto bar = [&](int i) -> uint32_t { return smem_u32(bars + i); };
@@ -226,10 +249,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < KV_STAGES; ++i) {
-            mbar_init(bar(B_KVF + i), 1);
+            mbar_init(bar(B_KVF + i), FP8 ? 128 : 1);   // fp8: the widening warps arrive
             mbar_init(bar(B_KVE + i), has1 ? 2 : 1);   // one release per MMA issuer
         }
+        for (int i = 0; i < F8_STAGES; ++i) {
+            mbar_init(bar(B_F8F + i), 1);
+            mbar_init(bar(B_F8E + i), 128);
+        }
         mbar_init(bar(B_Q), 1);
+        for (int i = 0; i < 2; ++i) mbar_init(bar(B_QC + i), 128);
         for (int i = 0; i < 4; ++i) mbar_init(bar(B_S + i), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_P + i), 128);
@@ -267,7 +295,38 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         int issued = 0;
-        for (int jj = 0; jj < T; ++jj) {
+        if constexpr (FP8) {
+            // e4m3 K and V of each block (one 2 KiB box each) into a staging stage;
+            // the widening warps turn it into the operand tiles
+            for (int jj = 0; jj < T; ++jj) {
+                const int st = jj % F8_STAGES;
+                if (jj >= F8_STAGES && !wait_w(bar(B_F8E + st), ((jj - F8_STAGES) / F8_STAGES) & 1)) break;
+                const int j = j0 + jj;
+                const int b = j * (BN / BS) + lane;
+                int32_t id = -1;
+                if (lane < BN / BS && b < nblk) id = __ldg(bt + b);
+                const bool valid = lane < BN / BS && b < nblk && id >= 0 && id < p.num_blocks;
+                if (lane < BN / BS && b < nblk && !valid) flag(ST_BAD_BLOCK);
+                const unsigned vm = __ballot_sync(0xffffffffu, valid);
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(bar(B_F8F + st), __popc(vm) * 2 * 2048);
+                }
+                __syncwarp();
+                if (valid) {
+                    const int y = (id * p.hkv + g) * BS;
+                    const uint32_t kd = sbase + Lay<FP8>::SF8 + st * F8_STAGE_BYTES + lane * 2048;
+                    tma_load_2d(kd, &kmap, 0, y, bar(B_F8F + st));
+                    tma_load_2d(kd + F8_V_OFF, &vmap, 0, y, bar(B_F8F + st));
+                }
+                issued = jj + 1;
+            }
+            if (*abort_flag) {
+                for (int jj = max(0, issued - F8_STAGES); jj < issued; ++jj)
+                    (void)mbar_wait_bounded(bar(B_F8F + jj % F8_STAGES), (jj / F8_STAGES) & 1);
+            }
+        }
+        for (int jj = 0; jj < T && !FP8; ++jj) {
             const int st = jj % KV_STAGES;
             if (jj >= KV_STAGES && !wait_w(bar(B_KVE + st), ((jj - KV_STAGES) / KV_STAGES) & 1)) break;
             const int j = j0 + jj;
@@ -308,7 +367,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) mbar_arrive(bar(B_TAIL));
             }
         }
-        if (*abort_flag) {
+        if (!FP8 && *abort_flag) {
             // let loads already in flight land before the CTA exits
             for (int jj = max(0, issued - KV_STAGES); jj < issued; ++jj)
                 (void)mbar_wait_bounded(bar(B_KVF + jj % KV_STAGES), (jj / KV_STAGES) & 1);
@@ -333,7 +392,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)   // D = 128 in steps of 16: 4 per 64-wide half
                         umma_f16(ts, qdesc + (uint64_t)((((kk >> 2) * 16384) + (kk & 3) * 32) >> 4),
-                                 kd + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4), IDESC_S, kk > 0);
+                                 kd + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4),
+                                 FP8 ? IDESC_S16 : IDESC_S, kk > 0);
                     umma_commit(bar(B_S + 2 * gi + (jj & 1)));
                 }
                 __syncwarp();
@@ -346,7 +406,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t ts = tS(gi, jj & 1);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)   // 64 keys in steps of 16
-                        umma_f16_ts(to, ts + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), IDESC_PV,
+                        umma_f16_ts(to, ts + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), FP8 ? IDESC_PV16 : IDESC_PV,
                                     (jj > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(bar(B_PVD + gi));
                     // the stage is released once both issuers' MMAs reading it are done
@@ -355,12 +415,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
             };
             // a tile holding keys >= L is read by PV only after the producer zeroed them
+            // (fp8 cache: the widening warps write those rows as zeros)
             auto tail_ready = [&](int jj) -> bool {
-                return (j0 + jj + 1) * BN <= L || wait_w(bar(B_TAIL), 0);
+                return FP8 || (j0 + jj + 1) * BN <= L || wait_w(bar(B_TAIL), 0);
             };
             // S of the first two tiles up front; afterwards S(jj+2) follows PV(jj), so
             // each softmax finds its S computed while it worked on the tile before
-            bool ok = wait_w(bar(B_Q), 0);
+            // fp8 cache: Q is used once the softmax warps have turned it into f16
+            bool ok = FP8 ? wait_w(bar(B_QC + gi), 0) : wait_w(bar(B_Q), 0);
             for (int jj = 0; ok && jj < min(2, T); ++jj) {
                 if (!wait_w(bar(B_KVF + jj), 0)) { ok = false; break; }
                 issue_s(jj);
@@ -381,6 +443,43 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             (void)mbar_wait_bounded(bar(B_DRAIN + gi), 0);
         }
+    } else if (warp >= 11) {
+        // ======================= fp8 cache: widen each e4m3 K/V tile to f16 operand
+        // tiles (exact), in the operand stages' 128-byte-swizzled layout; keys at
+        // or past L and blocks outside the pool become zeros
+        if constexpr (FP8) {
+            const int ct = threadIdx.x - 11 * 32;      // 0..127
+            const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks;
+            for (int jj = 0; jj < T; ++jj) {
+                const int s8 = jj % F8_STAGES, st = jj % KV_STAGES;
+                if (!wait_w(bar(B_F8F + s8), (jj / F8_STAGES) & 1)) break;
+                if (jj >= KV_STAGES && !wait_w(bar(B_KVE + st), ((jj - KV_STAGES) / KV_STAGES) & 1)) break;
+                const int t0 = (j0 + jj) * BN;
+                const uint32_t src = sbase + Lay<FP8>::SF8 + s8 * F8_STAGE_BYTES;
+                const uint32_t dst = sbase + SKV + st * KV_STAGE_BYTES;
+                // tasks: (K | V) x 64 keys x 8 chunks of 16 e4m3 (d = 16c .. 16c+15)
+                for (int task = ct; task < 2 * BN * 8; task += 128) {
+                    const int which = task / (BN * 8), row = (task >> 3) % BN, c = task & 7;
+                    const int key = t0 + row;
+                    bool valid = key < L;
+                    if (valid) {
+                        const int32_t id = __ldg(bt + key / BS);
+                        valid = id >= 0 && id < p.num_blocks;
+                    }
+                    uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
+                    if (valid) lds128(src + which * F8_V_OFF + row * 128 + ((c ^ (row & 7)) << 4), w0, w1, w2, w3);
+                    const uint32_t base = dst + which * V_OFF + (c >> 2) * KV_HALF + row * 128;
+                    const int q0 = (2 * c) & 7, q1 = (2 * c + 1) & 7;
+                    st_shared_v4(base + ((q0 ^ (row & 7)) << 4), e4m3x2_to_f16x2(w0 & 0xffffu),
+                                 e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 & 0xffffu), e4m3x2_to_f16x2(w1 >> 16));
+                    st_shared_v4(base + ((q1 ^ (row & 7)) << 4), e4m3x2_to_f16x2(w2 & 0xffffu),
+                                 e4m3x2_to_f16x2(w2 >> 16), e4m3x2_to_f16x2(w3 & 0xffffu), e4m3x2_to_f16x2(w3 >> 16));
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(B_KVF + st));
+                mbar_arrive(bar(B_F8E + s8));
+            }
+        }
     } else {
         // ======================= softmax warpgroups: thread = query row = TMEM lane
         const int gi = warp >> 2;                  // which query tile of the pair
@@ -398,6 +497,27 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
             float m_ref = -INFINITY, l = 0.f;
             bool ok = true;
+            // fp8 cache: the k scale folds into the softmax scale, the v scale into O
+            const float sl = FP8 ? p.scale_log2 * __ldg(p.k_scale + g) : p.scale_log2;
+            const float vsc = FP8 ? __ldg(p.v_scale + g) : 1.f;
+            if constexpr (FP8) {
+                // the group's Q tile, bf16 -> f16 in place (exact for these values'
+                // range but the smallest subnormals), before its first product
+                ok = wait_w(bar(B_Q), 0);
+                if (ok) {
+                    const uint32_t qt = sbase + SQ + gi * Q_TILE;
+                    for (int c = r; c < Q_TILE / 16; c += 128) {
+                        uint32_t w0, w1, w2, w3;
+                        lds128(qt + c * 16, w0, w1, w2, w3);
+                        auto cv = [](uint32_t w) -> uint32_t {
+                            return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+                        };
+                        st_shared_v4(qt + c * 16, cv(w0), cv(w1), cv(w2), cv(w3));
+                    }
+                    fence_proxy_async_smem();
+                }
+                mbar_arrive(bar(B_QC + gi));
+            }
             for (int jj = 0; jj < T && ok; ++jj) {
                 const int t0 = (j0 + jj) * BN;
                 if (!wait_w(bar(B_S + 2 * gi + (jj & 1)), (jj >> 1) & 1)) { ok = false; break; }
@@ -421,7 +541,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int k = 0; k < 4; ++k) mk[k] = max3(mk[k], sv[c + k], sv[c + 4 + k]);
                 }
                 const float mraw = max3(mk[0], mk[1], fmaxf(mk[2], mk[3]));
-                const float mx = mraw * p.scale_log2;
+                const float mx = mraw * sl;
                 float alpha = 1.f;
                 if (mx > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mx != -INFINITY)) {
                     alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx);
@@ -431,7 +551,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // reference 0 keeps the exponent at -inf, i.e. p = 0.
                 const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;
                 // exponent argument and running sum on packed fp32 pairs
-                const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2), mn2 = f2_pack(mneg, mneg);
+                const uint64_t sl2 = f2_pack(sl, sl), mn2 = f2_pack(mneg, mneg);
                 uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
                 uint32_t pw[BN / 2];
 #pragma unroll
@@ -440,7 +560,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     f2_unpack(f2_fma(f2_pack(sv[2 * e], sv[2 * e + 1]), sl2, mn2), y0, y1);
                     const float p0 = ex2(y0), p1 = ex2(y1);
                     acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
-                    pw[e] = pack_bf16(p0, p1);
+                    pw[e] = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
                 }
                 const uint64_t a2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
                 float s0, s1;
@@ -474,7 +594,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const size_t rh = (size_t)(row0 + (row_valid ? i : i0)) * p.hq + head;
                 const size_t pi = rh * p.max_splits + split;
-                const float inv = (nsplit == 1 && l > 0.f) ? 1.f / l : (nsplit == 1 ? 0.f : 1.f);
+                const float inv = ((nsplit == 1 && l > 0.f) ? 1.f / l : (nsplit == 1 ? 0.f : 1.f)) * vsc;
                 float4 *dst = reinterpret_cast<float4 *>(nsplit == 1 ? p.out + rh * D : p.part_o + pi * D);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {       // 32 columns at a time (the load is warp-wide)
@@ -719,13 +839,7 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                                k_scale, v_scale, num_splits, workspace, workspace_bytes, st, false, max_q_len, true);
     }
-    if (max_q_len >= 2 && dtype == KV_FP8_E4M3) {
-        // fp8 cache with chunks: every row (chunk or decode) goes through the
-        // decode kernel as a problem of its own, over the keys it may see
-        return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
-                               total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
-                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, true, 0, true);
-    }
+    if (dtype == KV_FP8_E4M3 && (!k_scale || !v_scale)) return KV_ERR_INVALID;
     const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq,
                               num_splits);
     if (pl.total && (!workspace || workspace_bytes < pl.total || !pkv_host::aligned(workspace, 256)))
@@ -773,6 +887,8 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     p.tiles_per_split = pl.tiles_per_split;
     p.max_splits = std::max(1, pl.max_splits);
     p.scale_log2 = scale * LOG2E;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
     CUtensorMap qm, km, vm;
     const int tpt = BM / G;
     if (!pkv_host::encode_tmap_3d(&qm, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, num_q_heads, total_q_tokens,
@@ -780,19 +896,26 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
                                   CU_TENSOR_MAP_SWIZZLE_128B))
         return KV_ERR_CUDA;
     if (!pkv_decode::make_maps(k_cache, v_cache, num_blocks, num_kv_heads, dtype, &km, &vm)) return KV_ERR_CUDA;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess)
-            return KV_ERR_CUDA;
-        configured = true;
+    static bool configured[2] = {false, false};
+    const bool fp8 = dtype == KV_FP8_E4M3;
+    if (!configured[fp8]) {
+        const cudaError_t e =
+            fp8 ? cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Lay<true>::SMEM_BYTES)
+                : cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Lay<false>::SMEM_BYTES);
+        if (e != cudaSuccess) return KV_ERR_CUDA;
+        configured[fp8] = true;
     }
     tile_prefix_kernel<<<1, 1024, 0, st>>>(p);
     // grid.x bounds the number of query tiles: sum over chunks of ceil(n/tpt)
     const int64_t tiles_ub = (total_q_tokens + tpt - 1) / tpt + std::min<int64_t>(num_seqs, total_q_tokens / 2);
     if (tiles_ub > INT32_MAX || p.max_splits > 65535) return KV_ERR_UNSUPPORTED;
     dim3 grid((unsigned)tiles_ub, num_kv_heads, p.max_splits);
-    prefill_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(qm, km, vm, p);
+    if (fp8)
+        prefill_kernel<true><<<grid, Lay<true>::THREADS, Lay<true>::SMEM_BYTES, st>>>(qm, km, vm, p);
+    else
+        prefill_kernel<false><<<grid, Lay<false>::THREADS, Lay<false>::SMEM_BYTES, st>>>(qm, km, vm, p);
     if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
     if (p.max_splits > 1) {
         const int64_t warps = (int64_t)total_q_tokens * num_q_heads;
