@@ -182,3 +182,19 @@ def test_sequences_with_no_query_rows(qlens, dt):
     _, got = _run(wl)
     assert got.shape == ref.shape
     assert max_abs(got, ref) <= TOL[dt]
+
+
+def test_mixed_prefill_fp8_workload_sampled():
+    """The mixed batch over an fp8 cache: the 1,024-row chunk runs on the tensor
+    cores with e4m3 K/V widened to f16 operands."""
+    wl = make_workload("mixed_prefill_fp8")
+    dw = DeviceWorkload(wl)
+    dw.step()
+    assert pkv.kv_last_device_status() == 0
+    out = dw.out.cpu().numpy()
+    cu = wl.cu_q_lens
+    rows = [0, 1, 15, 16, 17, 511, 1000, 1023]
+    ref = omodel.expected_rows(wl, 0, rows=rows)
+    assert max_abs(out[cu[0] + np.array(rows)], ref) <= TOL["fp8"]
+    for s in (1, 100, 255):
+        assert max_abs(out[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s)) <= TOL["fp8"], s
