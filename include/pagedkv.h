@@ -333,10 +333,9 @@ PAGEDKV_API kv_status paged_attention_decode_static_scratch(
  * (num_q_heads / num_kv_heads) <= 16, e.g. a speculative draft of 4 tokens
  * under a GQA group of 4 ([P3] speculative decoding, N = 4-8) -- run instead
  * with the whole batch in the decode kernel, whose CTA then covers all rows of
- * a sequence so each K/V tile is read once.  With an fp8 cache and longer chunks,
- * every row of the batch (chunk rows included) is a decode problem of its own
- * over the keys it may see, on `stream`: total_q_tokens <= 65535 (else
- * KV_ERR_UNSUPPORTED), partitions of 16,384 keys, num_splits ignored.
+ * a sequence so each K/V tile is read once.  With an fp8 cache the chunks run
+ * on the tensor cores as well: each e4m3 K/V tile is widened exactly to f16
+ * operands, Q is rounded to f16 once, and the products accumulate in fp32.
  *
  *  out, q          device [total_q_tokens][num_q_heads][128] (fp32 / bf16)
  *  cu_q_lens       device int32 [num_seqs+1], cu_q_lens[0] = 0, non-decreasing,

@@ -56,7 +56,6 @@ struct DecodeParams {
     const int32_t *context_lens;
     const int32_t *cu_q_lens;  // mixed batches: only sequences with one query row
     int total_rows;            // rows of q/out (mixed batches)
-    int row_mode;              // every row of a mixed batch is its own problem (see row_keys)
     int col_groups;            // multi-row mode: CTAs per (split, KV head, sequence) over the columns
     const float *k_scale;
     const float *v_scale;
@@ -98,12 +97,9 @@ struct Geo {
 
 __device__ __forceinline__ void flag(uint32_t bits) { atomicOr(&g_status, bits); }
 
-// Row mode: query row r of a mixed batch as a decode problem of its own.  The
-// sequence seq owning the row is found by binary search over cu_q_lens; with n
-// rows in its chunk and context length L (chunk included), row i = r - cu[seq]
-// of the chunk sees keys 0 .. L - n + i, so the problem has L - n + i + 1 keys.
-// Returns 0 (flagged by the caller as a bad length) for a malformed batch.
-__device__ __forceinline__ int row_keys(const DecodeParams &p, int r, int &seq, int &L)
+// Multi-row mode: the context length of the sequence owning query row r of a
+// mixed batch (binary search over cu_q_lens), 0 for a malformed batch.
+__device__ __forceinline__ int row_seq_len(const DecodeParams &p, int r)
 {
     const int32_t *cu = p.cu_q_lens;
     int lo = 0, hi = p.num_seqs;                 // cu[lo] <= r < cu[hi] if well formed
@@ -112,14 +108,10 @@ __device__ __forceinline__ int row_keys(const DecodeParams &p, int r, int &seq, 
         if (__ldg(cu + mid) <= r) lo = mid;
         else hi = mid;
     }
-    seq = lo;
-    L = 0;
     const int a = __ldg(cu + lo), b = __ldg(cu + lo + 1);
     if (r < a || r >= b) return 0;
-    const int n = b - a, len = __ldg(p.context_lens + lo);
-    if (n > len || len > p.max_blocks * BS) return 0;
-    L = len;
-    return len - n + (r - a) + 1;
+    const int len = __ldg(p.context_lens + lo);
+    return (b - a > len || len > p.max_blocks * BS) ? 0 : len;
 }
 
 template <bool FP8>
@@ -187,10 +179,6 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
         }
         if (cg * CW >= nq * p.group) return;
         row = a;
-    } else if (p.row_mode) {
-        int Lseq;
-        row = wi = blockIdx.z;
-        L = row_keys(p, row, s, Lseq);
     } else {
         if (p.cu_q_lens) {
             int a = p.cu_q_lens[s], b = p.cu_q_lens[s + 1];
@@ -562,17 +550,13 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p)
     griddep_wait();   // the partials come from the decode kernel just before
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    const bool per_row = p.row_mode || p.col_groups > 0;
+    const bool per_row = p.col_groups > 0;
     if (wid >= (per_row ? p.total_rows : p.num_seqs) * p.hq) return;
     const int wi = wid / p.hq, h = wid % p.hq;   // wi: sequence, or row
     int row = wi, L;
-    if (p.row_mode) {
-        int seq, Lseq;
-        L = row_keys(p, row, seq, Lseq);
-    } else if (p.col_groups > 0) {
+    if (per_row) {
         // multi-row: the row's partitions are those of its sequence's whole context
-        int seq;
-        (void)row_keys(p, row, seq, L);
+        L = row_seq_len(p, row);
     } else {
         if (p.cu_q_lens) {
             int a = p.cu_q_lens[wi], b = p.cu_q_lens[wi + 1];
@@ -620,7 +604,7 @@ cudaError_t launch_one(const CUtensorMap &km, const CUtensorMap &vm, const Decod
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    dim3 grid(p.num_splits * (MR ? p.col_groups : 1), p.hkv, p.row_mode ? p.total_rows : p.num_seqs);
+    dim3 grid(p.num_splits * (MR ? p.col_groups : 1), p.hkv, p.num_seqs);
     return pkv_host::launch_ex(decode_kernel<FP8, NT, MR>, grid, dim3(THREADS), Geo<FP8>::SMEM, st, pdl, km, vm, p);
 }
 
@@ -665,17 +649,6 @@ void plan_splits(int32_t max_blocks, int32_t num_splits, int32_t num_seqs, int32
     *splits = (max_blocks + pb - 1) / pb;
 }
 
-// Row mode (every query row of a mixed batch a problem of its own): there are
-// as many problems as rows, so partitions need not add parallelism; they are
-// ROW_PART_BLOCKS blocks (16,384 keys) long, whatever the caller asked for.
-constexpr int32_t ROW_PART_BLOCKS = 1024;
-
-void plan_rows(int32_t max_blocks, int32_t *part_blocks, int32_t *splits)
-{
-    *part_blocks = std::min(max_blocks, ROW_PART_BLOCKS);
-    *splits = (max_blocks + *part_blocks - 1) / *part_blocks;
-}
-
 static size_t partial_bytes(int32_t problems, int32_t hq, int32_t splits)
 {
     if (splits <= 1) return 0;
@@ -690,14 +663,6 @@ size_t workspace_bytes(int32_t num_seqs, int32_t hq, int32_t max_blocks, int32_t
     int32_t pb, s;
     plan_splits(max_blocks, num_splits, num_seqs, hq, &pb, &s);
     return partial_bytes(num_seqs, hq, s);
-}
-
-size_t workspace_bytes_rows(int32_t total_rows, int32_t hq, int32_t max_blocks)
-{
-    if (total_rows < 1 || hq < 1 || max_blocks < 1) return 0;
-    int32_t pb, s;
-    plan_rows(max_blocks, &pb, &s);
-    return partial_bytes(total_rows, hq, s);
 }
 
 // Multi-row mode: the decode partitioning, partials per row.
@@ -728,8 +693,6 @@ bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int
 // Validates host-visible arguments shared by decode and the decode rows of a
 // mixed batch, then launches decode (+ reduce), with programmatic dependent
 // launch when pdl is set (see pkv_host::launch_ex).  Needing cu_q_lens:
-//  row_mode        every row of the batch, chunk rows included, is a decode
-//                  problem over the keys it may see;
 //  multi_q_len > 0 multi-row mode: every sequence's rows (at most multi_q_len)
 //                  are covered by column groups of one CTA per KV tile stream.
 kv_status run(float *out, const void *q, const void *k_cache, const void *v_cache,
@@ -737,13 +700,11 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
               const int32_t *cu_q_lens, int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t hkv,
               int32_t num_blocks, float scale, kv_dtype dt, const float *k_scale, const float *v_scale,
               int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st,
-              bool row_mode, int32_t multi_q_len, bool pdl)
+              int32_t multi_q_len, bool pdl)
 {
     const bool multi = multi_q_len > 0;
-    if ((row_mode || multi) && (!cu_q_lens || total_rows < 0)) return KV_ERR_INVALID;
-    if ((row_mode || multi) && total_rows == 0) return KV_OK;
-    if (row_mode && total_rows > 65535) return KV_ERR_UNSUPPORTED;
-    if (row_mode && multi) return KV_ERR_INVALID;
+    if (multi && (!cu_q_lens || total_rows < 0)) return KV_ERR_INVALID;
+    if (multi && total_rows == 0) return KV_OK;
     if (num_seqs == 0) return KV_OK;
     if (num_seqs < 0 || hq < 1 || hkv < 1 || num_blocks < 1 || max_blocks < 1) return KV_ERR_INVALID;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return KV_ERR_INVALID;
@@ -764,7 +725,6 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     p.context_lens = context_lens;
     p.cu_q_lens = cu_q_lens;
     p.total_rows = cu_q_lens ? total_rows : num_seqs;
-    p.row_mode = row_mode ? 1 : 0;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     p.max_blocks = max_blocks;
@@ -774,8 +734,7 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     p.group = G;
     p.num_blocks = num_blocks;
     p.scale_log2 = scale * LOG2E;
-    if (row_mode) plan_rows(max_blocks, &p.part_blocks, &p.num_splits);
-    else plan_splits(max_blocks, num_splits, num_seqs, hq, &p.part_blocks, &p.num_splits);
+    plan_splits(max_blocks, num_splits, num_seqs, hq, &p.part_blocks, &p.num_splits);
     // columns of one sequence and KV head: its rows x the group's heads
     const int64_t cols = multi ? (int64_t)multi_q_len * G : G;
     const int nt = cols > 8 ? 2 : 1;
@@ -785,10 +744,9 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
         p.col_groups = (int)groups;
     }
     if (p.num_splits > 65535) return KV_ERR_UNSUPPORTED;
-    const int32_t problems = (row_mode || multi) ? total_rows : num_seqs;
-    const size_t need = row_mode ? workspace_bytes_rows(total_rows, hq, max_blocks)
-                                 : multi ? workspace_bytes_multi(total_rows, num_seqs, hq, max_blocks, num_splits)
-                                         : workspace_bytes(num_seqs, hq, max_blocks, num_splits);
+    const int32_t problems = multi ? total_rows : num_seqs;
+    const size_t need = multi ? workspace_bytes_multi(total_rows, num_seqs, hq, max_blocks, num_splits)
+                              : workspace_bytes(num_seqs, hq, max_blocks, num_splits);
     if (need) {
         if (!workspace || workspace_bytes_given < need || !pkv_host::aligned(workspace, 256))
             return KV_ERR_INVALID;
@@ -839,7 +797,7 @@ kv_status paged_attention_decode(float *out, const void *q, const void *k_cache,
     return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            nullptr, num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                            k_scale, v_scale, num_splits, workspace, workspace_bytes,
-                           static_cast<cudaStream_t>(stream), false, 0, true);
+                           static_cast<cudaStream_t>(stream), 0, true);
 }
 
 }  // extern "C"
@@ -905,7 +863,7 @@ kv_status paged_attention_decode_static_scratch(float *out, const void *q, const
     return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            nullptr, num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                            k_scale, v_scale, num_splits, scratch, need ? STATIC_SCRATCH_BYTES : 0,
-                           static_cast<cudaStream_t>(stream), false, 0, true);
+                           static_cast<cudaStream_t>(stream), 0, true);
 }
 
 }  // extern "C"

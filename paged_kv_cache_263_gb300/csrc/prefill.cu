@@ -41,9 +41,13 @@
 //  * Decode rows (n = 1) of the batch run on a library-owned side stream in
 //    the decode kernel, concurrently with the chunk tiles.
 //
-// fp8 cache with chunks: each row of the batch becomes a decode problem of its
-// own in the decode kernel (its keys 0 .. L-n+i), which widens e4m3 exactly in
-// registers; a tcgen05 kind::f8f6f4 variant of this kernel is not built.
+// fp8 cache: the same kernel with four more warps that widen each e4m3 K/V tile
+// (landed by TMA in a staging ring) to f16 operand tiles -- exact, as every
+// e4m3 value is an f16 value -- zeroing keys past the context on the way; Q is
+// rounded to f16 once in shared memory, so both products run as kind::f16 with
+// f16 operands (one type per product); k_scale folds into the softmax scale and
+// v_scale into O.  Quantising Q to e4m3 for a kind::f8f6f4 product would cost
+// precision the bf16 queries carry.
 #include "common.cuh"
 
 #include <algorithm>
@@ -684,9 +688,8 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
               const int32_t *cu_q_lens, int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t hkv,
               int32_t num_blocks, float scale, kv_dtype dt, const float *k_scale, const float *v_scale,
               int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st,
-              bool row_mode, int32_t multi_q_len, bool pdl);
+              int32_t multi_q_len, bool pdl);
 size_t workspace_bytes(int32_t num_seqs, int32_t hq, int32_t max_blocks, int32_t num_splits);
-size_t workspace_bytes_rows(int32_t total_rows, int32_t hq, int32_t max_blocks);
 size_t workspace_bytes_multi(int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t max_blocks,
                              int32_t num_splits);
 bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int32_t hkv, kv_dtype dt,
@@ -727,14 +730,6 @@ Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq,
     if (max_q_len >= 2) off += up((size_t)(num_seqs + 1) * sizeof(int32_t));
     pl.total = off;
     return pl;
-}
-
-// Workspace of an fp8 batch with chunks: every row is a decode problem with
-// partitions as long as the chunk kernel's, so this never exceeds make_plan's
-// total for the same shape (the size query serves both dtypes).
-size_t rows_bytes(int32_t total_q, int32_t hq, int32_t max_blocks)
-{
-    return pkv_decode::workspace_bytes_rows(total_q, hq, max_blocks);
 }
 
 // Short chunks (a speculative draft being verified, a few rows per sequence)
@@ -804,7 +799,6 @@ size_t paged_attention_chunked_prefill_workspace_size(int32_t num_seqs, int32_t 
         return 0;
     size_t t = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq,
                          num_splits).total;
-    if (max_q_len >= 2) t = std::max(t, rows_bytes(total_q_tokens, num_q_heads, max_blocks_per_seq));
     if (use_multi(max_q_len, num_q_heads, num_kv_heads))
         t = std::max(t, pkv_decode::workspace_bytes_multi(total_q_tokens, num_seqs, num_q_heads, max_blocks_per_seq,
                                                           num_splits));
@@ -837,7 +831,7 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
         // short chunks: the decode kernel's multi-row mode for the whole batch
         return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
-                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, false, max_q_len, true);
+                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, max_q_len, true);
     }
     if (dtype == KV_FP8_E4M3 && (!k_scale || !v_scale)) return KV_ERR_INVALID;
     const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq,
@@ -849,7 +843,7 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
         return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                                k_scale, v_scale, num_splits, pl.decode_bytes ? ws : nullptr, pl.decode_bytes, on,
-                               false, 0, pdl);
+                               0, pdl);
     };
     if (max_q_len < 2) return decode_rows(st, true);   // decode rows only
     // decode rows (n = 1) on the side stream, forked from and joined into the

@@ -206,11 +206,10 @@ def test_host_validation_before_launch():
     assert L.paged_attention_decode(fake, fake, fake, fake, fake, 100, fake, 2, 8, 2, 400, 0.1, 0, None, None,
                                     4, fake, need - 256, None) == 1
     assert pkv.paged_attention_workspace_size(2, 8, 100, 1) == 0
-    # fp8 cache with chunks: every row is a decode problem on the z grid axis,
-    # so more than 65535 rows are refused; a short workspace is refused too
-    assert L.paged_attention_chunked_prefill(fake, fake, fake, fake, 1, 70000, 70000, fake, fake, fake, 5000, 8, 2,
-                                             6000, 0.1, 1, fake, fake, 0, fake, 1 << 30, None) == 3
+    # fp8 cache with chunks: the scales are required; a short workspace is refused
+    assert L.paged_attention_chunked_prefill(fake, fake, fake, fake, 1, 100, 100, fake, fake, fake, 2048, 8, 2,
+                                             3000, 0.1, 1, None, None, 0, fake, 1 << 30, None) == 1
     ws = pkv.paged_attention_chunked_prefill_workspace_size(1, 100, 100, 8, 2, 2048, 0)
-    assert ws >= 100 * 8 * 2 * 130 * 4          # rows x heads x two 16,384-key partitions
+    assert ws >= 100 * 8 * 2 * 130 * 4          # rows x heads x at least two KV partitions
     assert L.paged_attention_chunked_prefill(fake, fake, fake, fake, 1, 100, 100, fake, fake, fake, 2048, 8, 2,
                                              3000, 0.1, 1, fake, fake, 0, fake, 256, None) == 1
