@@ -391,6 +391,14 @@ PAGEDKV_API kv_status kv_swap_in(void *k_cache, void *v_cache, int32_t num_block
                                  kv_dtype dtype, const int32_t *block_ids, int32_t n, const void *host_k,
                                  const void *host_v, void *stream);
 
+/* Tracing aid.  While enabled, each paged_attention_chunked_prefill call records
+ * CUDA events around its tensor-core chunk kernel on `stream` (only outside
+ * stream capture); kv_trace_prefill_kernel_ms waits for the last such kernel of
+ * the current device and returns its duration in ms, or a negative value if no
+ * kernel was recorded since the previous query. */
+PAGEDKV_API kv_status kv_trace_prefill(int32_t enable);
+PAGEDKV_API double kv_trace_prefill_kernel_ms(void);
+
 /* Waits for `stream`, then returns and clears the sticky device status word
  * set by earlier calls (KV_OK or KV_ERR_DEVICE_BOUNDS); KV_ERR_CUDA if the
  * stream itself reports an error. */

@@ -19,6 +19,7 @@ __all__ = [
     "paged_attention_chunked_prefill_workspace_size", "paged_attention_chunked_prefill",
     "kv_last_device_status", "kv_last_device_status_flags", "KV_BF16", "KV_FP8_E4M3",
     "HEAD_DIM", "BLOCK_SIZE", "library_path", "PrefixCache", "kv_swap_out", "kv_swap_in", "kv_waste_stats",
+    "kv_trace_prefill", "kv_trace_prefill_kernel_ms",
 ]
 
 HEAD_DIM = 128
@@ -98,6 +99,8 @@ def lib():
                                                                 P, I, P]),
             "kv_swap_out": (c.c_int, [P, P, I, I, c.c_int, P, I, P, P, P]),
             "kv_swap_in": (c.c_int, [P, P, I, I, c.c_int, P, I, P, P, P]),
+            "kv_trace_prefill": (c.c_int, [I]),
+            "kv_trace_prefill_kernel_ms": (c.c_double, []),
             "kv_last_device_status": (c.c_int, [P]),
             "kv_last_device_status_flags": (c.c_uint32, []),
         }
@@ -439,6 +442,16 @@ def kv_swap_in(k_cache, v_cache, block_ids, host_k, host_v, stream=None):
     _check(lib().kv_swap_in(_ptr(k_cache), _ptr(v_cache), k_cache.shape[0], k_cache.shape[1],
                             _cache_dtype(k_cache), _ptr(block_ids), n, _ptr(host_k), _ptr(host_v),
                             _stream(stream)), "kv_swap_in")
+
+
+def kv_trace_prefill(enable: bool):
+    """Record CUDA events around the chunk kernel of each mixed call (tracing aid)."""
+    _check(lib().kv_trace_prefill(1 if enable else 0), "kv_trace_prefill")
+
+
+def kv_trace_prefill_kernel_ms() -> float:
+    """Duration of the last traced chunk kernel in ms (waits for it); < 0 if none."""
+    return float(lib().kv_trace_prefill_kernel_ms())
 
 
 def kv_last_device_status(stream=None) -> int:

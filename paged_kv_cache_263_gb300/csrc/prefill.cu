@@ -776,6 +776,30 @@ SideStream *side_stream()
 }
 }  // namespace
 
+namespace {
+// Tracing aid: CUDA events around the tensor-core chunk kernel of each call,
+// per device, recorded only while enabled (not during stream capture).
+struct Trace {
+    cudaEvent_t start = nullptr, stop = nullptr;
+    bool recorded = false;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+Trace g_trace[MAX_DEVICES];
+
+Trace *trace_for_call()
+{
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    if (!g_trace_on) return nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+    Trace &t = g_trace[dev];
+    if (!t.start && (cudaEventCreate(&t.start) != cudaSuccess || cudaEventCreate(&t.stop) != cudaSuccess))
+        return nullptr;
+    return &t;
+}
+}  // namespace
+
 namespace pkv_prefill {
 uint32_t take_status()
 {
@@ -906,10 +930,16 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     const int64_t tiles_ub = (total_q_tokens + tpt - 1) / tpt + std::min<int64_t>(num_seqs, total_q_tokens / 2);
     if (tiles_ub > INT32_MAX || p.max_splits > 65535) return KV_ERR_UNSUPPORTED;
     dim3 grid((unsigned)tiles_ub, num_kv_heads, p.max_splits);
+    Trace *tr = trace_for_call();
+    if (tr) cudaEventRecord(tr->start, st);
     if (fp8)
         prefill_kernel<true><<<grid, Lay<true>::THREADS, Lay<true>::SMEM_BYTES, st>>>(qm, km, vm, p);
     else
         prefill_kernel<false><<<grid, Lay<false>::THREADS, Lay<false>::SMEM_BYTES, st>>>(qm, km, vm, p);
+    if (tr) {
+        cudaEventRecord(tr->stop, st);
+        tr->recorded = true;
+    }
     if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
     if (p.max_splits > 1) {
         const int64_t warps = (int64_t)total_q_tokens * num_q_heads;
@@ -917,6 +947,26 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
         if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
     }
     return KV_OK;
+}
+
+kv_status kv_trace_prefill(int32_t enable)
+{
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    g_trace_on = enable != 0;
+    return KV_OK;
+}
+
+double kv_trace_prefill_kernel_ms(void)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return -1.0;
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    Trace &t = g_trace[dev];
+    if (!t.recorded || cudaEventSynchronize(t.stop) != cudaSuccess) return -1.0;
+    float ms = -1.f;
+    if (cudaEventElapsedTime(&ms, t.start, t.stop) != cudaSuccess) return -1.0;
+    t.recorded = false;
+    return ms;
 }
 
 }  // extern "C"
