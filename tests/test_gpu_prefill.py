@@ -198,3 +198,18 @@ def test_mixed_prefill_fp8_workload_sampled():
     assert max_abs(out[cu[0] + np.array(rows)], ref) <= TOL["fp8"]
     for s in (1, 100, 255):
         assert max_abs(out[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s)) <= TOL["fp8"], s
+
+
+def test_chunk_kernel_trace_events():
+    wl = small_workload(1500, lens=[3000, 40], q_lens=[256, 1], hq=16, hkv=2)
+    dw = DeviceWorkload(wl)
+    dw.step()
+    pkv.kv_trace_prefill(True)
+    dw.attention()
+    ms = pkv.kv_trace_prefill_kernel_ms()
+    assert 0 < ms < 1000
+    assert pkv.kv_trace_prefill_kernel_ms() < 0          # consumed
+    pkv.kv_trace_prefill(False)
+    dw.attention()
+    assert pkv.kv_trace_prefill_kernel_ms() < 0          # not recorded while disabled
+    assert pkv.kv_last_device_status() == 0
