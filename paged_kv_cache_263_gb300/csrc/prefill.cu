@@ -76,20 +76,19 @@ constexpr uint32_t F8_STAGE_BYTES = 16384, F8_V_OFF = 8192;
 template <bool FP8>
 struct Lay {
     static constexpr int THREADS = FP8 ? 480 : 352;
-    static constexpr int KV_STAGES = FP8 ? 3 : 5;
+    static constexpr int KV_STAGES = FP8 ? 3 : 4;
     static constexpr int F8_STAGES = FP8 ? 3 : 0;
     static constexpr uint32_t SF8 = SKV + KV_STAGES * KV_STAGE_BYTES;
     static constexpr uint32_t SBAR = SF8 + F8_STAGES * F8_STAGE_BYTES;
     static constexpr int SMEM_BYTES = SBAR + 512;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-    static_assert(KV_STAGES <= 5 && F8_STAGES <= 3, "barrier slots");
 };
 static_assert(SKV >= 2 * 32768, "shared-memory layout overlaps");
 // barriers (room for the larger of the two layouts)
 enum {
     B_KVF = 0,                      // + stage: K and V operand tiles ready
-    B_KVE = B_KVF + 5,              // + stage: every MMA reading the stage is done
-    B_Q = B_KVE + 5,                // both Q tiles landed
+    B_KVE = B_KVF + 4,              // + stage: every MMA reading the stage is done
+    B_Q = B_KVE + 4,                // both Q tiles landed
     B_QC = B_Q + 1,                 // + group: fp8 cache: the group's Q tile is in f16
     B_S = B_QC + 2,                 // + 2*group + buffer: an S tile of the group is in TMEM
     B_P = B_S + 4,                  // + group: the group's P is in TMEM (128 arrivals)
