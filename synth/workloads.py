@@ -242,6 +242,11 @@ def make_workload(name: str) -> Workload:
         return Workload("split_fp8", seed, 64, 8, pool, "fp8", lens, np.ones(8, np.int32),
                         rng.permutation(pool), num_splits=16,
                         description="long-context split-KV decode, fp8-e4m3 cache, 16 partitions")
+    if name == "mixed_prefill_small_fp8":
+        wl = make_workload("mixed_prefill_small")
+        wl.name, wl.kv_dtype, wl.seed = "mixed_prefill_small_fp8", "fp8", 2645
+        wl.description = "the profiling mix over an fp8-e4m3 cache"
+        return wl
     if name == "mixed_prefill_fp8":
         # the chunked-prefill mix with an fp8-e4m3 cache
         wl = make_workload("mixed_prefill")
@@ -271,7 +276,7 @@ def make_workload(name: str) -> Workload:
 
 
 WORKLOADS = ("tiny", "llama8b", "llama70b_prefix", "mixed_prefill", "split_fp8")
-EXTRA_WORKLOADS = ("mixed_prefill_small", "mixed_prefill_fp8", "spec_verify", "spec_verify8")
+EXTRA_WORKLOADS = ("mixed_prefill_small", "mixed_prefill_small_fp8", "mixed_prefill_fp8", "spec_verify", "spec_verify8")
 
 
 def small_workload(seed: int, lens, q_lens=None, hq=8, hkv=2, kv_dtype="bf16", num_blocks=None,
