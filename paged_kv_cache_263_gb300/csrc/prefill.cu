@@ -461,9 +461,12 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                 const int t0 = (j0 + jj) * BN;
                 const uint32_t src = sbase + Lay<FP8>::SF8 + s8 * F8_STAGE_BYTES;
                 const uint32_t dst = sbase + SKV + st * KV_STAGE_BYTES;
-                // tasks: (K | V) x 64 keys x 8 chunks of 16 e4m3 (d = 16c .. 16c+15)
+                // tasks: (K | V) x 8 chunks of 16 e4m3 (d = 16c .. 16c+15) x 64 keys; the
+                // lanes of a warp take consecutive keys, so the 8 lanes of each
+                // quarter-warp access 8 distinct 16-byte bank groups (the 128-byte
+                // swizzle XORs the chunk with the key's low 3 bits)
                 for (int task = ct; task < 2 * BN * 8; task += 128) {
-                    const int which = task / (BN * 8), row = (task >> 3) % BN, c = task & 7;
+                    const int which = task / (BN * 8), row = task % BN, c = (task / BN) & 7;
                     const int key = t0 + row;
                     bool valid = key < L;
                     if (valid) {
@@ -473,17 +476,11 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                     uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
                     if (valid) lds128(src + which * F8_V_OFF + row * 128 + ((c ^ (row & 7)) << 4), w0, w1, w2, w3);
                     const uint32_t base = dst + which * V_OFF + (c >> 2) * KV_HALF + row * 128;
-                    const uint32_t a0 = base + ((((2 * c) & 7) ^ (row & 7)) << 4);       // d 16c .. 16c+7
-                    const uint32_t a1 = base + ((((2 * c + 1) & 7) ^ (row & 7)) << 4);   // d 16c+8 .. 16c+15
-                    const uint32_t l0 = e4m3x2_to_f16x2(w0 & 0xffffu), l1 = e4m3x2_to_f16x2(w0 >> 16);
-                    const uint32_t l2 = e4m3x2_to_f16x2(w1 & 0xffffu), l3 = e4m3x2_to_f16x2(w1 >> 16);
-                    const uint32_t h0 = e4m3x2_to_f16x2(w2 & 0xffffu), h1 = e4m3x2_to_f16x2(w2 >> 16);
-                    const uint32_t h2 = e4m3x2_to_f16x2(w3 & 0xffffu), h3 = e4m3x2_to_f16x2(w3 >> 16);
-                    // lanes with c >= 4 write their two chunks in the other order, so
-                    // each store of a quarter-warp covers all eight 16-byte bank groups
-                    const bool sw = (c & 4) != 0;
-                    st_shared_v4(sw ? a1 : a0, sw ? h0 : l0, sw ? h1 : l1, sw ? h2 : l2, sw ? h3 : l3);
-                    st_shared_v4(sw ? a0 : a1, sw ? l0 : h0, sw ? l1 : h1, sw ? l2 : h2, sw ? l3 : h3);
+                    const int q0 = (2 * c) & 7, q1 = (2 * c + 1) & 7;   // d 16c .. +7 and 16c+8 .. +15
+                    st_shared_v4(base + ((q0 ^ (row & 7)) << 4), e4m3x2_to_f16x2(w0 & 0xffffu),
+                                 e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 & 0xffffu), e4m3x2_to_f16x2(w1 >> 16));
+                    st_shared_v4(base + ((q1 ^ (row & 7)) << 4), e4m3x2_to_f16x2(w2 & 0xffffu),
+                                 e4m3x2_to_f16x2(w2 >> 16), e4m3x2_to_f16x2(w3 & 0xffffu), e4m3x2_to_f16x2(w3 >> 16));
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(bar(B_KVF + st));
