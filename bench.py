@@ -262,19 +262,11 @@ def run_reference(args):
 
 def _launches_per_step(pkv, wl):
     """Kernels one step launches: the cache write, then the attention call's
-    kernels (decode + optional LSE merge; for a batch with chunks also the
-    tile-count prefix, the chunk kernel and its optional merge; the decode
-    kernel of the batch's one-row sequences always launches)."""
-    mb = wl.max_blocks_per_seq
-    dec_split = pkv.paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, mb, wl.num_splits) > 0
-    n = 1 + 1 + (1 if dec_split else 0)
-    if not wl.is_decode:
-        if int(wl.q_lens.max()) * wl.group <= 64:     # short chunks: multi-row decode mode only
-            return n
-        if wl.kv_dtype == "fp8":           # every row in the decode kernel, 16,384-key partitions
-            return 1 + 1 + (1 if mb > 1024 else 0)
-        n += 2 + (1 if mb * 16 > 16384 else 0)
-    return n
+    kernels as the library itself plans them for these sizes (decode + its
+    optional LSE merge; for a batch with chunks also the tile-count prefix,
+    the chunk kernel and its optional merge)."""
+    return 1 + pkv.paged_attention_launch_count(wl.num_seqs, int(wl.q_lens.sum()), int(wl.q_lens.max()), wl.num_q_heads, wl.num_kv_heads,
+                                                wl.max_blocks_per_seq, wl.num_splits)
 
 
 # ------------------------------------------------------------------ ours

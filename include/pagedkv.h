@@ -352,6 +352,17 @@ PAGEDKV_API size_t paged_attention_chunked_prefill_workspace_size(int32_t num_se
                                                       int32_t max_blocks_per_seq,
                                                       int32_t num_splits);
 
+/* Number of kernels one successful paged_attention_chunked_prefill call with
+ * these sizes enqueues, on the caller's stream and the library's side stream
+ * together (host-only; reads no device memory).  With max_q_len = 1 it is also
+ * the count of a paged_attention_decode call with the same num_seqs,
+ * num_q_heads, max_blocks_per_seq and num_splits.  Returns 0 for sizes a call
+ * would accept without launching anything (no sequences or no query rows) and
+ * for sizes it would reject. */
+PAGEDKV_API int32_t paged_attention_launch_count(int32_t num_seqs, int32_t total_q_tokens, int32_t max_q_len,
+                                                 int32_t num_q_heads, int32_t num_kv_heads,
+                                                 int32_t max_blocks_per_seq, int32_t num_splits);
+
 PAGEDKV_API kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32_t *cu_q_lens,
                                           const int32_t *context_lens, int32_t num_seqs,
                                           int32_t total_q_tokens, int32_t max_q_len,

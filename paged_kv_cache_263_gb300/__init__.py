@@ -17,6 +17,7 @@ __all__ = [
     "KVError", "lib", "KVPool", "kv_status_string", "reshape_and_cache",
     "paged_attention_workspace_size", "paged_attention_decode",
     "paged_attention_chunked_prefill_workspace_size", "paged_attention_chunked_prefill",
+    "paged_attention_launch_count",
     "kv_last_device_status", "kv_last_device_status_flags", "KV_BF16", "KV_FP8_E4M3",
     "HEAD_DIM", "BLOCK_SIZE", "library_path", "PrefixCache", "kv_swap_out", "kv_swap_in", "kv_waste_stats",
     "kv_trace_prefill", "kv_trace_prefill_kernel_ms",
@@ -92,6 +93,7 @@ def lib():
             "paged_attention_decode": (c.c_int, [P, P, P, P, P, I, P, I, I, I, I, F, c.c_int, P, P,
                                                  I, P, SZ, P]),
             "paged_attention_chunked_prefill_workspace_size": (SZ, [I, I, I, I, I, I, I]),
+            "paged_attention_launch_count": (I, [I, I, I, I, I, I, I]),
             "paged_attention_chunked_prefill": (c.c_int, [P, P, P, P, I, I, I, P, P, P, I, I, I, I,
                                                           F, c.c_int, P, P, I, P, SZ, P]),
             "paged_attention_decode_static_scratch_bytes": (SZ, []),
@@ -328,6 +330,12 @@ def paged_attention_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq, nu
 def paged_attention_chunked_prefill_workspace_size(num_seqs, total_q_tokens, max_q_len, num_q_heads,
                                                    num_kv_heads, max_blocks_per_seq, num_splits=0) -> int:
     return int(lib().paged_attention_chunked_prefill_workspace_size(
+        num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq, num_splits))
+
+
+def paged_attention_launch_count(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads,
+                                 max_blocks_per_seq, num_splits=0) -> int:
+    return int(lib().paged_attention_launch_count(
         num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq, num_splits))
 
 

@@ -697,6 +697,8 @@ size_t workspace_bytes_multi(int32_t total_rows, int32_t num_seqs, int32_t hq, i
                              int32_t num_splits);
 bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int32_t hkv, kv_dtype dt,
                CUtensorMap *km, CUtensorMap *vm);
+void plan_splits(int32_t max_blocks, int32_t num_splits, int32_t num_seqs, int32_t hq, int32_t *part_blocks,
+                 int32_t *splits);
 }  // namespace pkv_decode
 
 namespace {
@@ -830,6 +832,24 @@ size_t paged_attention_chunked_prefill_workspace_size(int32_t num_seqs, int32_t 
         t = std::max(t, pkv_decode::workspace_bytes_multi(total_q_tokens, num_seqs, num_q_heads, max_blocks_per_seq,
                                                           num_splits));
     return t;
+}
+
+int32_t paged_attention_launch_count(int32_t num_seqs, int32_t total_q_tokens, int32_t max_q_len,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t max_blocks_per_seq,
+                                     int32_t num_splits)
+{
+    if (num_seqs < 1 || total_q_tokens < 1 || max_q_len < 1 || num_q_heads < 1 || num_kv_heads < 1 ||
+        max_blocks_per_seq < 1)
+        return 0;
+    // the decode kernel, plus its LSE merge when the context is partitioned
+    int32_t pb = 0, s = 0;
+    pkv_decode::plan_splits(max_blocks_per_seq, num_splits, num_seqs, num_q_heads, &pb, &s);
+    const int32_t decode = 1 + (s > 1 ? 1 : 0);
+    if (max_q_len < 2 || use_multi(max_q_len, num_q_heads, num_kv_heads)) return decode;
+    // the decode rows, the tile-count prefix, the chunk tiles and their merge
+    const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq,
+                              num_splits);
+    return decode + 2 + (pl.max_splits > 1 ? 1 : 0);
 }
 
 kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32_t *cu_q_lens,

@@ -213,3 +213,23 @@ def test_host_validation_before_launch():
     assert ws >= 100 * 8 * 2 * 130 * 4          # rows x heads x at least two KV partitions
     assert L.paged_attention_chunked_prefill(fake, fake, fake, fake, 1, 100, 100, fake, fake, fake, 2048, 8, 2,
                                              3000, 0.1, 1, fake, fake, 0, fake, 256, None) == 1
+
+
+def test_launch_count_follows_the_plan():
+    """The kernels a call enqueues, from the host plan alone: decode (+ merge
+    when the context is partitioned), short chunks in the multi-row decode
+    mode, longer chunks adding the tile prefix, the chunk kernel and its merge."""
+    n = pkv.paged_attention_launch_count
+    assert n(0, 0, 1, 8, 2, 100, 0) == 0                  # nothing to do
+    assert n(4, 4, 1, 8, 2, 1, 0) == 1                    # one block: one partition, no merge
+    assert n(4, 4, 1, 8, 2, 100, 1) == 1                  # one forced partition
+    assert n(4, 4, 1, 8, 2, 100, 4) == 2                  # four partitions: merge
+    assert n(4, 16, 4, 16, 4, 100, 1) == 1                # 4 rows x G 4 = 16 columns: multi-row mode
+    assert n(4, 16, 4, 16, 4, 100, 4) == 2
+    assert n(4, 20, 5, 16, 4, 60, 1) == 1 + 2             # 5 x 4 columns: chunk tiles; 960 keys, one partition
+    # a small batch shortens the chunk partitions to 1,024 keys: 1,600 keys take two
+    assert n(4, 20, 5, 16, 4, 100, 1) == 1 + 3
+    assert n(1, 100, 100, 8, 2, 1, 1) == 1 + 2            # 16 keys: one partition of the chunk's keys
+    # 32,768 keys exceed the longest chunk partition (16,384): the chunk merge runs
+    assert n(1, 100, 100, 8, 2, 2048, 1) == 1 + 3
+    assert n(1, 100, 100, 8, 2, 2048, 4) == 2 + 3

@@ -175,8 +175,8 @@ def test_calls_from_several_streams_and_a_captured_graph():
                                       ([40, 0, 1, 0], "fp8")])
 def test_sequences_with_no_query_rows(qlens, dt):
     """A sequence may contribute no rows to a mixed batch (cu_q_lens repeats a
-    value): the tensor-core path (5 rows x G 4), the multi-row mode (4 x 4) and
-    the fp8 per-row mode all skip it and get every other row right."""
+    value): the tensor-core path (5 rows x G 4, and 40 rows over an fp8 cache)
+    and the multi-row mode (4 x 4) all skip it and get every other row right."""
     wl = small_workload(1200 + sum(qlens), lens=[100, 50, 300, 17], q_lens=qlens, hq=16, hkv=4, kv_dtype=dt)
     _, _, ref = expected_full(wl)
     _, got = _run(wl)
