@@ -20,7 +20,8 @@
 //  * S[128x64] = Q K^T and O[128x128] += P V run as tcgen05.mma (K=16 steps),
 //    one issuing warp per query tile (warps 9 and 10).  S is double-buffered
 //    per tile in tensor memory, so QK^T of tile j+2 runs while the softmax
-//    works on tile j.  P (bf16) is written over its S buffer and read by the
+//    works on tile j; the softmax waits for the previous PV product only when
+//    it must rescale O.  P (bf16) is written over its S buffer and read by the
 //    second product as the A operand straight from tensor memory; K is the
 //    K-major B operand of the first product, V the MN-major B operand of the
 //    second, both from the same shared-memory stage.  Tensor memory: S 2 x 64
@@ -35,9 +36,9 @@
 //  * Keys at or past the context end inside the last tile are masked in S; the
 //    producer zeroes their V rows after the load lands (0 x garbage could be
 //    NaN), signalled on its own barrier.
-//  * Long contexts are cut into partitions of whole tiles (16,384 keys, less
-//    when the grid would be too small to fill the GPU), merged by a
-//    fixed-order log-sum-exp kernel (no atomics).
+//  * Long contexts are cut into equal partitions of whole tiles (at most
+//    16,384 keys, less when the grid would be too small to fill the GPU),
+//    merged by a fixed-order log-sum-exp kernel (no atomics).
 //  * Decode rows (n = 1) of the batch run on a library-owned side stream in
 //    the decode kernel, concurrently with the chunk tiles.
 //
@@ -91,8 +92,8 @@ enum {
     B_Q = B_KVE + 4,                // both Q tiles landed
     B_QC = B_Q + 1,                 // + group: fp8 cache: the group's Q tile is in f16
     B_S = B_QC + 2,                 // + 2*group + buffer: an S tile of the group is in TMEM
-    B_P = B_S + 4,                  // + group: the group's P is in TMEM (128 arrivals)
-    B_PVD = B_P + 2,                // + group: the group's latest PV product finished
+    B_P = B_S + 4,                  // + 2*group + buffer: the group's P is in TMEM (128 arrivals)
+    B_PVD = B_P + 4,                // + group: the group's latest PV product finished
     B_DRAIN = B_PVD + 2,            // + group: every MMA of the group's issuer finished
     B_TAIL = B_DRAIN + 2,           // bf16 cache: the V rows past the context are zeroed
     B_F8F = B_TAIL + 1,             // + staging stage: fp8 cache: e4m3 K and V landed
@@ -238,11 +239,14 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
     const int last = has1 ? 2 * pair + 1 : 2 * pair;
     const int kmax = L - n + min(n, (last + 1) * tpt);   // keys visible to the pair's last row
     const int KT = (kmax + BN - 1) / BN;
-    const int j0 = split * p.tiles_per_split;
-    if (j0 >= KT) return;
-    const int j1 = min(KT, j0 + p.tiles_per_split);
-    const int T = j1 - j0;
+    // the pair's keys in nsplit partitions of (nearly) equal length, at most
+    // tiles_per_split tiles each, so that no short partition trails the grid
     const int nsplit = (KT + p.tiles_per_split - 1) / p.tiles_per_split;
+    const int tps = (KT + nsplit - 1) / nsplit;   // ceil(KT / tps) == nsplit
+    const int j0 = split * tps;
+    if (j0 >= KT) return;
+    const int j1 = min(KT, j0 + tps);
+    const int T = j1 - j0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (sbase & 1023u) {
         // the 128-byte swizzle needs 1024-byte aligned tiles; never observed, but
@@ -262,9 +266,11 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
         }
         mbar_init(bar(B_Q), 1);
         for (int i = 0; i < 2; ++i) mbar_init(bar(B_QC + i), 128);
-        for (int i = 0; i < 4; ++i) mbar_init(bar(B_S + i), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(bar(B_S + i), 1);
             mbar_init(bar(B_P + i), 128);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_PVD + i), 1);
             mbar_init(bar(B_DRAIN + i), 1);
         }
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                 issue_s(jj);
             }
             for (int jj = 0; jj < T && ok; ++jj) {
-                if (!wait_w(bar(B_P + gi), jj & 1) || !tail_ready(jj)) { ok = false; break; }
+                if (!wait_w(bar(B_P + 2 * gi + (jj & 1)), (jj >> 1) & 1) || !tail_ready(jj)) { ok = false; break; }
                 // in issue order: PV(jj) reads P from S buffer jj % 2 before S(jj+2)
                 // overwrites it
                 issue_pv(jj);
@@ -574,13 +580,13 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                 f2_unpack(a2, s0, s1);
                 const float sum = s0 + s1;
                 l = l * alpha + sum;
-                if (jj > 0) {
-                    // PV(jj-1) finished: O holds every earlier tile, and PV(jj-2), which
-                    // read the P columns about to be overwritten, finished before it
+                // PV(jj-2), which read the P columns about to be overwritten, finished
+                // before S(jj) (issued after it by the same thread) completed.  O is
+                // rescaled only once PV(jj-1) has accumulated into it; PV(jj) waits
+                // for this warp's P, so it cannot start before the rescale is done.
+                if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                     if (!wait_w(bar(B_PVD + gi), (jj - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
-                }
-                if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float o[32];
@@ -595,9 +601,14 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                 tmem_st32u(tS(gi, jj & 1) + lane_base, pw);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(B_P + gi));
+                // one P barrier per S buffer: a warp reaches buffer b's next phase only
+                // after S(jj+2) completed, which the issuer started only once all 128
+                // rows had arrived for this phase -- arrivals never mix two tiles
+                mbar_arrive(bar(B_P + 2 * gi + (jj & 1)));
             }
-            if (ok && wait_w(bar(B_PVD + gi), (T - 1) & 1)) {
+            // every MMA of the group has finished (a one-phase barrier: PV(T-2) may
+            // still run here, so a parity wait on the per-tile barrier could alias)
+            if (ok && wait_w(bar(B_DRAIN + gi), 0)) {
                 tc_fence_after();
                 const size_t rh = (size_t)(row0 + (row_valid ? i : i0)) * p.hq + head;
                 const size_t pi = rh * p.max_splits + split;
