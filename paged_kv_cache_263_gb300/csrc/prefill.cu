@@ -308,26 +308,33 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
         if constexpr (FP8) {
             // e4m3 K and V of each block (one 2 KiB box each) into a staging stage;
             // the widening warps turn it into the operand tiles
+            // lanes 0-7 each load one box per tile: lane = 2 x block + (K | V); the
+            // block ids of the next tile are read during the wait for a free stage
+            const int blk8 = (lane >> 1) & 3, kv = lane & 1;
+            auto block_id8 = [&](int jj) -> int32_t {
+                const int b = (j0 + jj) * (BN / BS) + blk8;
+                return (lane < 8 && jj < T && b < nblk) ? __ldg(bt + b) : -1;
+            };
+            int32_t next_id = block_id8(0);
             for (int jj = 0; jj < T; ++jj) {
                 const int st = jj % F8_STAGES;
+                const int32_t id = next_id;
+                next_id = block_id8(jj + 1);
                 if (jj >= F8_STAGES && !wait_w(bar(B_F8E + st), ((jj - F8_STAGES) / F8_STAGES) & 1)) break;
                 const int j = j0 + jj;
-                const int b = j * (BN / BS) + lane;
-                int32_t id = -1;
-                if (lane < BN / BS && b < nblk) id = __ldg(bt + b);
-                const bool valid = lane < BN / BS && b < nblk && id >= 0 && id < p.num_blocks;
-                if (lane < BN / BS && b < nblk && !valid) flag(ST_BAD_BLOCK);
+                const bool in = lane < 8 && j * (BN / BS) + blk8 < nblk;
+                const bool valid = in && id >= 0 && id < p.num_blocks;
+                if (in && !valid && kv == 0) flag(ST_BAD_BLOCK);
                 const unsigned vm = __ballot_sync(0xffffffffu, valid);
                 if (lane == 0) {
                     fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(bar(B_F8F + st), __popc(vm) * 2 * 2048);
+                    mbar_arrive_expect_tx(bar(B_F8F + st), __popc(vm) * 2048);
                 }
                 __syncwarp();
                 if (valid) {
                     const int y = (id * p.hkv + g) * BS;
-                    const uint32_t kd = sbase + Lay<FP8>::SF8 + st * F8_STAGE_BYTES + lane * 2048;
-                    tma_load_2d(kd, &kmap, 0, y, bar(B_F8F + st));
-                    tma_load_2d(kd + F8_V_OFF, &vmap, 0, y, bar(B_F8F + st));
+                    const uint32_t dst = sbase + Lay<FP8>::SF8 + st * F8_STAGE_BYTES + kv * F8_V_OFF + blk8 * 2048;
+                    tma_load_2d(dst, kv ? &vmap : &kmap, 0, y, bar(B_F8F + st));
                 }
                 issued = jj + 1;
             }
@@ -336,29 +343,36 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                     (void)mbar_wait_bounded(bar(B_F8F + jj % F8_STAGES), (jj / F8_STAGES) & 1);
             }
         }
+        // bf16 cache: lanes 0-15 each load one 2 KiB box per tile, lane = 4 x block
+        // of the tile + operand (K dims 0-63, K 64-127, V 0-63, V 64-127), so the
+        // tile's 16 loads leave in one instruction; each lane's block id for the
+        // next tile is read while the producer waits for the stage to free up
+        const int blk = (lane >> 2) & 3, opnd = lane & 3;
+        auto block_id = [&](int jj) -> int32_t {
+            const int b = (j0 + jj) * (BN / BS) + blk;
+            return (!FP8 && lane < 16 && jj < T && b < nblk) ? __ldg(bt + b) : -1;
+        };
+        int32_t next_id = block_id(0);
         for (int jj = 0; jj < T && !FP8; ++jj) {
             const int st = jj % KV_STAGES;
+            const int32_t id = next_id;
+            next_id = block_id(jj + 1);
             if (jj >= KV_STAGES && !wait_w(bar(B_KVE + st), ((jj - KV_STAGES) / KV_STAGES) & 1)) break;
             const int j = j0 + jj;
-            const int b = j * (BN / BS) + (lane & 3);
-            int32_t id = -1;
-            if (lane < BN / BS && b < nblk) id = __ldg(bt + b);
-            const bool valid = lane < BN / BS && b < nblk && id >= 0 && id < p.num_blocks;
-            if (lane < BN / BS && b < nblk && !valid) flag(ST_BAD_BLOCK);
+            const bool in = lane < 16 && j * (BN / BS) + blk < nblk;
+            const bool valid = in && id >= 0 && id < p.num_blocks;
+            if (in && !valid && opnd == 0) flag(ST_BAD_BLOCK);
             const unsigned vm = __ballot_sync(0xffffffffu, valid);
             if (lane == 0) {
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar(B_KVF + st), __popc(vm) * 4 * 2048);
+                mbar_arrive_expect_tx(bar(B_KVF + st), __popc(vm) * 2048);
             }
             __syncwarp();
             if (valid) {
                 const int y = (id * p.hkv + g) * BS;
-                const uint32_t kd = sbase + SKV + st * KV_STAGE_BYTES + lane * 2048;
-                const uint32_t vd = kd + V_OFF;
-                tma_load_2d(kd, &kmap, 0, y, bar(B_KVF + st));
-                tma_load_2d(kd + KV_HALF, &kmap, 64, y, bar(B_KVF + st));
-                tma_load_2d(vd, &vmap, 0, y, bar(B_KVF + st));
-                tma_load_2d(vd + KV_HALF, &vmap, 64, y, bar(B_KVF + st));
+                const uint32_t dst = sbase + SKV + st * KV_STAGE_BYTES + (opnd >> 1) * V_OFF + (opnd & 1) * KV_HALF +
+                                     blk * 2048;
+                tma_load_2d(dst, (opnd >> 1) ? &vmap : &kmap, (opnd & 1) * 64, y, bar(B_KVF + st));
             }
             issued = jj + 1;
             const int first = L - j * BN;            // first row of the tile at or past L
