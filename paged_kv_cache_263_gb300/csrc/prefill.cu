@@ -472,36 +472,59 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
         // tiles (exact), in the operand stages' 128-byte-swizzled layout; keys at
         // or past L and blocks outside the pool become zeros
         if constexpr (FP8) {
+            // thread ct owns key row ct % 64 of every tile and the chunks of 16 e4m3
+            // (d = 16c .. 16c+15) with c = ct / 64 + 2k, k = 0..3, of both K and V; the
+            // lanes of a warp take consecutive keys, so the 8 lanes of each
+            // quarter-warp access 8 distinct 16-byte bank groups (the 128-byte
+            // swizzle XORs the chunk with the key's low 3 bits)
             const int ct = threadIdx.x - 11 * 32;      // 0..127
+            const int row = ct & (BN - 1), c0 = ct >> 6;
             const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks;
+            // the row's key of tile jj lies inside the context and its block in the
+            // pool (read one tile ahead, during the waits)
+            auto row_ok = [&](int jj) -> bool {
+                const int key = (j0 + jj) * BN + row;
+                if (jj >= T || key >= L) return false;
+                const int32_t id = __ldg(bt + key / BS);
+                return id >= 0 && id < p.num_blocks;
+            };
+            bool next_ok = row_ok(0);
             for (int jj = 0; jj < T; ++jj) {
                 const int s8 = jj % F8_STAGES, st = jj % KV_STAGES;
+                const bool valid = next_ok;
+                next_ok = row_ok(jj + 1);
                 if (!wait_w(bar(B_F8F + s8), (jj / F8_STAGES) & 1)) break;
                 if (jj >= KV_STAGES && !wait_w(bar(B_KVE + st), ((jj - KV_STAGES) / KV_STAGES) & 1)) break;
-                const int t0 = (j0 + jj) * BN;
-                const uint32_t src = sbase + Lay<FP8>::SF8 + s8 * F8_STAGE_BYTES;
-                const uint32_t dst = sbase + SKV + st * KV_STAGE_BYTES;
-                // tasks: (K | V) x 8 chunks of 16 e4m3 (d = 16c .. 16c+15) x 64 keys; the
-                // lanes of a warp take consecutive keys, so the 8 lanes of each
-                // quarter-warp access 8 distinct 16-byte bank groups (the 128-byte
-                // swizzle XORs the chunk with the key's low 3 bits)
-                for (int task = ct; task < 2 * BN * 8; task += 128) {
-                    const int which = task / (BN * 8), row = task % BN, c = (task / BN) & 7;
-                    const int key = t0 + row;
-                    bool valid = key < L;
-                    if (valid) {
-                        const int32_t id = __ldg(bt + key / BS);
-                        valid = id >= 0 && id < p.num_blocks;
+                const uint32_t src = sbase + Lay<FP8>::SF8 + s8 * F8_STAGE_BYTES + row * 128;
+                const uint32_t dst = sbase + SKV + st * KV_STAGE_BYTES + row * 128;
+                // all eight 16-byte loads first, then the conversions and stores
+                uint32_t w[2][4][4];
+#pragma unroll
+                for (int which = 0; which < 2; ++which)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = c0 + 2 * k;
+                        if (valid)
+                            lds128(src + which * F8_V_OFF + ((c ^ (row & 7)) << 4), w[which][k][0], w[which][k][1],
+                                   w[which][k][2], w[which][k][3]);
+                        else
+                            w[which][k][0] = w[which][k][1] = w[which][k][2] = w[which][k][3] = 0u;
                     }
-                    uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
-                    if (valid) lds128(src + which * F8_V_OFF + row * 128 + ((c ^ (row & 7)) << 4), w0, w1, w2, w3);
-                    const uint32_t base = dst + which * V_OFF + (c >> 2) * KV_HALF + row * 128;
-                    const int q0 = (2 * c) & 7, q1 = (2 * c + 1) & 7;   // d 16c .. +7 and 16c+8 .. +15
-                    st_shared_v4(base + ((q0 ^ (row & 7)) << 4), e4m3x2_to_f16x2(w0 & 0xffffu),
-                                 e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 & 0xffffu), e4m3x2_to_f16x2(w1 >> 16));
-                    st_shared_v4(base + ((q1 ^ (row & 7)) << 4), e4m3x2_to_f16x2(w2 & 0xffffu),
-                                 e4m3x2_to_f16x2(w2 >> 16), e4m3x2_to_f16x2(w3 & 0xffffu), e4m3x2_to_f16x2(w3 >> 16));
-                }
+#pragma unroll
+                for (int which = 0; which < 2; ++which)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = c0 + 2 * k;
+                        const uint32_t base = dst + which * V_OFF + (c >> 2) * KV_HALF;
+                        const int q0 = (2 * c) & 7, q1 = (2 * c + 1) & 7;   // d 16c .. +7 and 16c+8 .. +15
+                        const uint32_t *x = w[which][k];
+                        st_shared_v4(base + ((q0 ^ (row & 7)) << 4), e4m3x2_to_f16x2(x[0] & 0xffffu),
+                                     e4m3x2_to_f16x2(x[0] >> 16), e4m3x2_to_f16x2(x[1] & 0xffffu),
+                                     e4m3x2_to_f16x2(x[1] >> 16));
+                        st_shared_v4(base + ((q1 ^ (row & 7)) << 4), e4m3x2_to_f16x2(x[2] & 0xffffu),
+                                     e4m3x2_to_f16x2(x[2] >> 16), e4m3x2_to_f16x2(x[3] & 0xffffu),
+                                     e4m3x2_to_f16x2(x[3] >> 16));
+                    }
                 fence_proxy_async_smem();
                 mbar_arrive(bar(B_KVF + st));
                 mbar_arrive(bar(B_F8E + s8));
