@@ -724,7 +724,10 @@ __global__ void __launch_bounds__(128) prefill_reduce_kernel(const PrefillParams
 
 constexpr int TILES_PER_SPLIT = 16384 / BN;   // 16,384 keys per partition at most
 constexpr int MIN_TILES_PER_SPLIT = 1024 / BN; // 1,024 keys at least
-constexpr int64_t TARGET_CTAS = 4 * 152;       // four CTAs per SM of the grid, at least
+constexpr int64_t NUM_SMS = 152;               // a chunk CTA holds a whole SM: waves of 152
+constexpr double CTA_FIXED_TILES = 4.0;        // a CTA's Q load, set-up and epilogue, in tile-times
+// HBM bytes moved while a CTA works through one 64-key tile (~0.86 us at ~6.5 TB/s)
+constexpr double BYTES_PER_TILE_TIME = 5.6e6;
 
 struct Plan {
     size_t decode_bytes, part_o_off, part_ml_off, tile_off_off, total;
@@ -750,19 +753,43 @@ void plan_splits(int32_t max_blocks, int32_t num_splits, int32_t num_seqs, int32
 }  // namespace pkv_decode
 
 namespace {
-// KV partition length: 16,384 keys, halved (down to 1,024) while the grid
-// would hold fewer than TARGET_CTAS CTAs -- short chunks over a few thousand
-// keys otherwise leave most SMs idle (one CTA per SM fits).  The CTA count is
-// estimated from the host-visible sizes only: chunk sequences ~ total_q /
-// max_q_len, each with ceil(ceil(max_q_len / tpt) / 2) pairs of query tiles.
+// KV partitions of a chunk's keys.  Every CTA (one per pair of query tiles, KV
+// head and partition) holds a whole SM, so the grid runs in waves of NUM_SMS
+// CTAs, and the partitions of a key range are of equal length.  Their count s
+// minimises a makespan model: waves(s) x (W / s + CTA_FIXED_TILES) tile-times,
+// plus -- when s > 1 -- each partition's partial results written and merged
+// (rows x heads x 130 floats, twice), converted to tile-times.  W is the longest
+// key range in tiles, and the number of (pair, KV head) problems is estimated
+// from host-visible sizes only: chunk sequences ~ total_q / max_q_len, each with
+// ceil(ceil(max_q_len / tpt) / 2) pairs of query tiles.  Equal partitions alone
+// can leave a last wave almost empty (768 CTAs = 5.05 waves), which the model
+// avoids by taking one more partition.  Returns the partition length in tiles.
 int plan_tiles_per_split(int32_t total_q, int32_t max_q_len, int32_t hq, int32_t hkv, int max_kv_tiles)
 {
     const int G = std::max(1, hq / std::max(1, hkv)), tpt = std::max(1, BM / G);
     const int64_t chunks = std::max<int64_t>(1, (int64_t)total_q / std::max(1, max_q_len));
     const int64_t pairs = chunks * (((int64_t)max_q_len + tpt - 1) / tpt + 1) / 2;
-    int tps = TILES_PER_SPLIT;
-    while (tps > MIN_TILES_PER_SPLIT && pairs * hkv * ((max_kv_tiles + tps - 1) / tps) < TARGET_CTAS) tps /= 2;
-    return tps;
+    const int64_t problems = std::max<int64_t>(1, pairs * std::max(1, hkv));
+    const int W = std::max(1, max_kv_tiles);
+    const double merge_per_split = (double)total_q * hq * (D + 2) * 4.0 * 2.0 / BYTES_PER_TILE_TIME;
+    const int s_lo = (W + TILES_PER_SPLIT - 1) / TILES_PER_SPLIT;
+    const int s_hi = std::max(s_lo, (W + MIN_TILES_PER_SPLIT - 1) / MIN_TILES_PER_SPLIT);
+    auto cost = [&](int s) {
+        const int len = (W + s - 1) / s;
+        const int splits = (W + len - 1) / len;        // what the kernel makes of len
+        const int64_t waves = (problems * splits + NUM_SMS - 1) / NUM_SMS;
+        return (double)waves * (len + CTA_FIXED_TILES) + (splits > 1 ? splits * merge_per_split : 0.0);
+    };
+    double best = cost(s_lo);
+    for (int s = s_lo + 1; s <= s_hi; ++s) best = std::min(best, cost(s));
+    // the model takes every key range as long as the longest; with several chunk
+    // sequences the real ranges are ragged, which favours finer partitions: then
+    // the most partitions within 2% of the best modelled cost
+    const double slack = chunks > 1 ? 1.02 : 1.0;
+    int pick = s_lo;
+    for (int s = s_lo; s <= s_hi; ++s)
+        if (cost(s) <= best * slack) pick = s;
+    return (W + pick - 1) / pick;
 }
 
 Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq, int32_t hkv, int32_t max_blocks,
