@@ -1,7 +1,7 @@
 """Prefix reuse end to end on the GPU: requests that share a system prompt take
 its blocks from the prefix cache, write K/V and run attention only for their
 uncached remainder, and get the same rows as the fp64 oracle over their whole
-context -- and bitwise the same rows as a run without the cache."""
+context -- and, within rounding, the same rows as a run without the cache."""
 import numpy as np
 import pytest
 import torch
@@ -113,16 +113,14 @@ def test_shared_system_prompt_is_prefilled_once():
     for (rid, toks), (s, rows) in zip(reqs, first + batch):
         err = max_abs(rows, _expected(rid, toks, s))
         assert err <= TOL["bf16"], (rid, err)
-    # without the cache every request prefills its whole prompt; the rows the
-    # cached run computed in the chunk kernel are bitwise the same (a remainder
-    # of one row is a decode row, another kernel: within tolerance)
+    # without the cache every request prefills its whole prompt; the rows agree
+    # with the cached run's within rounding.  They are not bitwise equal: the
+    # chunk kernel's KV partitions follow the batch shape (its wave model), so
+    # a 300-row chunk and a 2,300-row prompt cut the same keys differently.
     plain = _Server(1200, False, 2)
     for (rid, toks), (s, rows) in zip(reqs[1:], batch):
         (_, full), = plain.run([(rid, toks)])
-        if len(rows) >= 2:
-            assert np.array_equal(full[s:], rows), rid
-        else:
-            assert max_abs(full[s:], rows) <= TOL["bf16"], rid
+        assert max_abs(full[s:], rows) <= TOL["bf16"], rid
 
 
 def test_tenant_keys_keep_prefixes_apart_on_the_gpu():
