@@ -451,6 +451,57 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
+// Log-sum-exp merge of ns partial results by one warp: ml = ns (max, sum)
+// pairs, o = ns rows of 128 floats; returns this lane's 4 output floats (dims
+// 4 lane .. 4 lane + 3), normalised, or zeros when every partition is empty.
+// Lane i reads the (max, sum) of partitions i, i + 32, ... together, so the
+// whole merge costs a few memory round trips instead of a chain per
+// partition; the order of every sum is fixed, so the result is deterministic.
+__device__ __forceinline__ float4 lse_merge_warp(const float *__restrict__ ml, const float *__restrict__ o, int ns,
+                                                 int lane)
+{
+    float M = -INFINITY;
+    for (int i = lane; i < ns; i += 32) M = fmaxf(M, ml[2 * i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lsum = 0.f;
+    if (M != -INFINITY) {
+        for (int i0 = 0; i0 < ns; i0 += 32) {
+            // weights of partitions i0 .. i0 + 31, one per lane
+            float f = 0.f;
+            if (i0 + lane < ns) {
+                const float2 e = *reinterpret_cast<const float2 *>(ml + 2 * (i0 + lane));
+                f = ex2(e.x - M);
+                lsum += f * e.y;
+            }
+            const int n = min(32, ns - i0);
+            // four partitions' rows in flight at a time
+            for (int k0 = 0; k0 < n; k0 += 4) {
+                float4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    v[u] = k0 + u < n ? reinterpret_cast<const float4 *>(o + (size_t)(i0 + k0 + u) * D)[lane]
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float fk = __shfl_sync(0xffffffffu, f, (k0 + u) & 31);
+                    if (k0 + u < n) {
+                        acc.x += fk * v[u].x;
+                        acc.y += fk * v[u].y;
+                        acc.z += fk * v[u].z;
+                        acc.w += fk * v[u].w;
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    return make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
 // max of three fp32 values
 __device__ __forceinline__ float max3(float a, float b, float c)
 {

@@ -570,24 +570,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p)
     const int ns = (nblk + p.part_blocks - 1) / p.part_blocks;
     if (ns <= 1) return;
     const size_t base = ((size_t)wi * p.hq + h) * p.num_splits;
-    float M = -INFINITY;
-    for (int i = 0; i < ns; ++i) M = fmaxf(M, p.part_ml[(base + i) * 2]);
-    float Ls = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-        for (int i = 0; i < ns; ++i) {
-            const float mi = p.part_ml[(base + i) * 2];
-            const float f = ex2(mi - M);
-            Ls += f * p.part_ml[(base + i) * 2 + 1];
-            const float4 v = reinterpret_cast<const float4 *>(p.part_o + (base + i) * D)[lane];
-            acc.x += f * v.x;
-            acc.y += f * v.y;
-            acc.z += f * v.z;
-            acc.w += f * v.w;
-        }
-    }
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    const float4 r = lse_merge_warp(p.part_ml + base * 2, p.part_o + base * D, ns, lane);
     reinterpret_cast<float4 *>(p.out + ((size_t)row * p.hq + h) * D)[lane] = r;
 }
 

@@ -702,24 +702,8 @@ __global__ void __launch_bounds__(128) prefill_reduce_kernel(const PrefillParams
     const int ns = (KT + p.tiles_per_split - 1) / p.tiles_per_split;
     if (ns <= 1) return;
     const size_t base = ((size_t)row * p.hq + h) * p.max_splits;
-    float M = -INFINITY;
-    for (int k = 0; k < ns; ++k) M = fmaxf(M, p.part_ml[(base + k) * 2]);
-    float Ls = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-        for (int k = 0; k < ns; ++k) {
-            const float f = ex2(p.part_ml[(base + k) * 2] - M);
-            Ls += f * p.part_ml[(base + k) * 2 + 1];
-            const float4 v = reinterpret_cast<const float4 *>(p.part_o + (base + k) * D)[lane];
-            acc.x += f * v.x;
-            acc.y += f * v.y;
-            acc.z += f * v.z;
-            acc.w += f * v.w;
-        }
-    }
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
     reinterpret_cast<float4 *>(p.out + ((size_t)row * p.hq + h) * D)[lane] =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        lse_merge_warp(p.part_ml + base * 2, p.part_o + base * D, ns, lane);
 }
 
 constexpr int TILES_PER_SPLIT = 16384 / BN;   // 16,384 keys per partition at most
