@@ -59,7 +59,7 @@ struct DecodeParams {
     int col_groups;            // multi-row mode: CTAs per (split, KV head, sequence) over the columns
     const float *k_scale;
     const float *v_scale;
-    float *part_o;             // [B][Hq][S][128]   (B = rows in row mode)
+    float *part_o;             // [B][Hq][S][128]   (B = rows in the multi-row mode)
     float *part_ml;            // [B][Hq][S][2]
     int max_blocks;
     int num_seqs;
@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
 }
 
 // Log-sum-exp merge of the split partitions: one warp per (sequence, q head),
-// or per (row, q head) in the row and multi-row modes.
+// or per (row, q head) in the multi-row mode.
 __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p)
 {
     griddep_wait();   // the partials come from the decode kernel just before
