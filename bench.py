@@ -174,9 +174,15 @@ class OracleSample:
     """The fp64 oracle (as it stands) on the first ``m`` sequences of the
     workload: block tables from the oracle's allocator model, a compact pool
     holding only those sequences' blocks, the oracle's own scatter; ``run()``
-    is one call of the paged oracle on that sample."""
+    is one call of the paged oracle on that sample.
 
-    def __init__(self, wl, m):
+    A chunk longer than ``row_cap`` rows is run on its last ``row_cap`` rows
+    only.  Its other rows would cost the same per (row, visible key) pair, so
+    ``scale`` = (row, key) pairs of the full sample / pairs run, and a call's
+    time x ``scale`` estimates the full sample's; ``algo_bytes`` counts the full
+    sample."""
+
+    def __init__(self, wl, m, row_cap=16):
         import numpy as np
         import torch
 
@@ -186,8 +192,13 @@ class OracleSample:
 
         self.oracle = oracle
         m = max(1, min(int(m), wl.num_seqs))
+        full_q = np.asarray(wl.q_lens[:m], np.int64)
+        run_q = np.minimum(full_q, row_cap) if row_cap else full_q
+        lens = np.asarray(wl.context_lens[:m], np.int64)
+        self.scale = float((full_q * lens).sum()) / max(1.0, float((run_q * lens).sum()))
+        self.capped = bool((run_q < full_q).any())
         sub = Workload(wl.name + "_sample", wl.seed, wl.num_q_heads, wl.num_kv_heads, 0, wl.kv_dtype,
-                       wl.context_lens[:m], wl.q_lens[:m], np.zeros(0, np.int32), wl.prefix_tokens,
+                       wl.context_lens[:m], run_q.astype(np.int32), np.zeros(0, np.int32), wl.prefix_tokens,
                        wl.cow_block, wl.num_splits)
         nblk = int(sum(-(-int(L) // 16) for L in sub.context_lens))
         sub.num_blocks = nblk + (m if sub.cow_block >= 0 else 0)
@@ -201,15 +212,19 @@ class OracleSample:
         self.sub, self.m, self.wl = sub, m, wl
         eb = sub.kv_elem_bytes
         kv_bytes = 2 * nblk * sub.num_kv_heads * 16 * 128 * eb
-        self.algo_bytes = kv_bytes + sub.total_q * sub.num_q_heads * 128 * (2 + 4)
+        self.algo_bytes = kv_bytes + int(full_q.sum()) * sub.num_q_heads * 128 * (2 + 4)
 
     def run(self):
         self.oracle.paged_attention(self.q, self.kc, self.vc, self.tb.tables, self.sub.context_lens, self.cu,
                                     dtype=self.code, k_scale=self.ks, v_scale=self.vs, scale=self.sub.scale)
 
     def describe(self):
-        return (f"first {self.m} of {self.wl.num_seqs} sequences ({int(self.sub.context_lens.sum())} "
-                f"context tokens) of the same workload, fp64 paged oracle")
+        d = (f"first {self.m} of {self.wl.num_seqs} sequences ({int(self.sub.context_lens.sum())} "
+             f"context tokens) of the same workload, fp64 paged oracle")
+        if self.capped:
+            d += (f"; chunks run on their last {int(self.sub.q_lens.max())} rows, time scaled by "
+                  f"{self.scale:.1f} (row, key) pairs of the full sample per pair run")
+        return d
 
 
 def cpu_oracle_baseline(wl, budget_s=10.0, max_seqs=16):
@@ -221,7 +236,7 @@ def cpu_oracle_baseline(wl, budget_s=10.0, max_seqs=16):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    per = el / reps
+    per = el / reps * smp.scale
     return {"value": smp.algo_bytes / per / 1e9, "unit": UNIT, "cores": smp.oracle.max_threads(),
             "kind": "oracle", "sample": f"{smp.describe()}, {reps} calls in {el:.1f} s"}
 
@@ -237,7 +252,7 @@ def run_reference(args):
     probe = OracleSample(wl, 1)
     t0 = time.perf_counter()
     probe.run()
-    per_seq = max(time.perf_counter() - t0, 1e-6)
+    per_seq = max(time.perf_counter() - t0, 1e-6)      # one sequence, chunk rows capped
     budget = args.ref_budget / max(1, args.steps + args.warmup)
     smp = OracleSample(wl, min(args.ref_seqs, max(1, int(budget / per_seq))))
     for _ in range(args.warmup):
@@ -247,12 +262,13 @@ def run_reference(args):
         t0 = time.perf_counter()
         smp.run()
         times.append(time.perf_counter() - t0)
-    total = sum(times)
+    total = sum(times) * smp.scale            # the full sample's time (chunk rows capped: scaled)
     v = smp.algo_bytes * len(times) / total / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "sample": smp.describe(), "device": "host cores"},
+            "data": "synthetic", "config": {"workload": wl.name, "sample": smp.describe(), "device": "host cores",
+                                            "time_scale": smp.scale},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": smp.oracle.max_threads(), "kind": "oracle",
                              "sample": smp.describe()},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
