@@ -391,12 +391,16 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
                 const float p2 = ex2(x[2] - r0), p3 = ex2(x[3] - r1);
                 l[nt][0] = l[nt][0] * al0 + (p0 + p2);
                 l[nt][1] = l[nt][1] * al1 + (p1 + p3);
+                // alpha is exactly 1 once a column's max stops growing: skipping the
+                // multiplications then changes no bit
+                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    o[nt][j][0] *= al0;
-                    o[nt][j][1] *= al1;
-                    o[nt][j][2] *= al0;
-                    o[nt][j][3] *= al1;
+                    for (int j = 0; j < 8; ++j) {
+                        o[nt][j][0] *= al0;
+                        o[nt][j][1] *= al1;
+                        o[nt][j][2] *= al0;
+                        o[nt][j][3] *= al1;
+                    }
                 }
                 if constexpr (!FP8) {
                     pb[nt][0] = movmatrix_t(pack_bf16(p0, p1));
