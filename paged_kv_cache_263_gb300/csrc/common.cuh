@@ -5,6 +5,8 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stdint.h>
 
 #include <utility>
@@ -358,6 +360,22 @@ __device__ __forceinline__ void griddep_launch_dependents()
 
 #if defined(__CUDACC__)
 namespace pkv_host {
+// Raises Kernel's dynamic shared-memory limit to `bytes` once per device; safe
+// to call from several host threads (the attribute belongs to the device's
+// context, so every device a process uses gets its own call).
+template <auto Kernel>
+cudaError_t ensure_dynamic_smem(int bytes)
+{
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
 // Launch, with programmatic stream serialisation when pdl is set (the kernel
 // calls pkv::griddep_wait() before it reads what earlier kernels produced).
 // Used where the kernel's predecessor on the stream is a kernel (typically the

@@ -583,14 +583,8 @@ template <bool FP8, int NT, bool MR>
 cudaError_t launch_one(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &p,
                        cudaStream_t st, bool pdl)
 {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP8, NT, MR>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Geo<FP8>::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    const cudaError_t e = pkv_host::ensure_dynamic_smem<decode_kernel<FP8, NT, MR>>(Geo<FP8>::SMEM);
+    if (e != cudaSuccess) return e;
     dim3 grid(p.num_splits * (MR ? p.col_groups : 1), p.hkv, p.num_seqs);
     return pkv_host::launch_ex(decode_kernel<FP8, NT, MR>, grid, dim3(THREADS), Geo<FP8>::SMEM, st, pdl, km, vm, p);
 }

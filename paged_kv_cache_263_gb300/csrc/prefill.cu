@@ -996,17 +996,10 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
                                   CU_TENSOR_MAP_SWIZZLE_128B))
         return KV_ERR_CUDA;
     if (!pkv_decode::make_maps(k_cache, v_cache, num_blocks, num_kv_heads, dtype, &km, &vm)) return KV_ERR_CUDA;
-    static bool configured[2] = {false, false};
     const bool fp8 = dtype == KV_FP8_E4M3;
-    if (!configured[fp8]) {
-        const cudaError_t e =
-            fp8 ? cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Lay<true>::SMEM_BYTES)
-                : cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Lay<false>::SMEM_BYTES);
-        if (e != cudaSuccess) return KV_ERR_CUDA;
-        configured[fp8] = true;
-    }
+    if ((fp8 ? pkv_host::ensure_dynamic_smem<prefill_kernel<true>>(Lay<true>::SMEM_BYTES)
+             : pkv_host::ensure_dynamic_smem<prefill_kernel<false>>(Lay<false>::SMEM_BYTES)) != cudaSuccess)
+        return KV_ERR_CUDA;
     tile_prefix_kernel<<<1, 1024, 0, st>>>(p);
     // grid.x bounds the number of query tiles: sum over chunks of ceil(n/tpt)
     const int64_t tiles_ub = (total_q_tokens + tpt - 1) / tpt + std::min<int64_t>(num_seqs, total_q_tokens / 2);
