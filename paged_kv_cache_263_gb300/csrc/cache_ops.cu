@@ -102,7 +102,7 @@ static uint32_t take_status_cache()
     return v;
 }
 
-static uint32_t g_last_flags = 0;
+static std::atomic<uint32_t> g_last_flags{0};   // read from any host thread
 
 kv_status pkv_launch_block_copy(void *k_cache, void *v_cache, int32_t src, int32_t dst,
                                 int32_t num_kv_heads, kv_dtype dtype, cudaStream_t stream)
@@ -157,10 +157,10 @@ kv_status kv_last_device_status(void *stream)
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KV_ERR_CUDA;
     uint32_t f = take_status_cache() | pkv_decode::take_status() | pkv_prefill::take_status() |
                  pkv_swap::take_status();
-    g_last_flags = f;
+    g_last_flags.store(f, std::memory_order_relaxed);
     return f ? KV_ERR_DEVICE_BOUNDS : KV_OK;
 }
 
-uint32_t kv_last_device_status_flags(void) { return g_last_flags; }
+uint32_t kv_last_device_status_flags(void) { return g_last_flags.load(std::memory_order_relaxed); }
 
 }  // extern "C"
