@@ -757,7 +757,8 @@ int plan_tiles_per_split(int32_t total_q, int32_t max_q_len, int32_t hq, int32_t
     const int W = std::max(1, max_kv_tiles);
     const double merge_per_split = (double)total_q * hq * (D + 2) * 4.0 * 2.0 / BYTES_PER_TILE_TIME;
     const int s_lo = (W + TILES_PER_SPLIT - 1) / TILES_PER_SPLIT;
-    const int s_hi = std::max(s_lo, (W + MIN_TILES_PER_SPLIT - 1) / MIN_TILES_PER_SPLIT);
+    // (the partition count is the grid's z extent: at most 65,535)
+    const int s_hi = std::max(s_lo, std::min(65535, (W + MIN_TILES_PER_SPLIT - 1) / MIN_TILES_PER_SPLIT));
     auto cost = [&](int s) {
         const int len = (W + s - 1) / s;
         const int splits = (W + len - 1) / len;        // what the kernel makes of len
