@@ -336,6 +336,11 @@ PAGEDKV_API kv_status paged_attention_decode_static_scratch(
  * a sequence so each K/V tile is read once.  With an fp8 cache the chunks run
  * on the tensor cores as well: each e4m3 K/V tile is widened exactly to f16
  * operands, Q is rounded to f16 once, and the products accumulate in fp32.
+ * A chunk's keys are cut into equal partitions of at most 16,384 keys, merged
+ * with the same log-sum-exp reduction; the library picks their number from the
+ * batch shape (num_splits applies to the decode rows), so a row's last bits
+ * may differ between batches of different shapes, never with the physical
+ * placement of the blocks.
  *
  *  out, q          device [total_q_tokens][num_q_heads][128] (fp32 / bf16)
  *  cu_q_lens       device int32 [num_seqs+1], cu_q_lens[0] = 0, non-decreasing,
