@@ -192,6 +192,9 @@ class OracleSample:
         from synth.workloads import Workload
 
         self.oracle = oracle
+        # every core this process may run on (a launcher's OMP_NUM_THREADS=1 is for
+        # its GPU ranks; only one rank runs the oracle)
+        self.threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
         m = max(1, min(int(m), wl.num_seqs))
         full_q = np.asarray(wl.q_lens[:m], np.int64)
         run_q = np.minimum(full_q, row_cap) if row_cap else full_q
@@ -215,10 +218,10 @@ class OracleSample:
         kv_bytes = 2 * nblk * sub.num_kv_heads * 16 * 128 * eb
         self.algo_bytes = kv_bytes + int(full_q.sum()) * sub.num_q_heads * 128 * (2 + 4)
 
-    def run(self, nthreads=0):
+    def run(self, nthreads=None):
         self.oracle.paged_attention(self.q, self.kc, self.vc, self.tb.tables, self.sub.context_lens, self.cu,
                                     dtype=self.code, k_scale=self.ks, v_scale=self.vs, scale=self.sub.scale,
-                                    nthreads=nthreads)
+                                    nthreads=self.threads if nthreads is None else nthreads)
 
     def describe(self):
         d = (f"first {self.m} of {self.wl.num_seqs} sequences ({int(self.sub.context_lens.sum())} "
@@ -231,7 +234,7 @@ class OracleSample:
 
 def cpu_oracle_baseline(wl, budget_s=10.0, max_seqs=16, single_core=False):
     smp = OracleSample(wl, max_seqs)
-    cores = smp.oracle.max_threads()
+    cores = smp.threads
 
     def timed(nthreads, budget):
         reps, t0 = 0, time.perf_counter()
@@ -283,7 +286,7 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": wl.name, "sample": smp.describe(), "device": "host cores",
                                             "time_scale": smp.scale},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": smp.oracle.max_threads(), "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": smp.threads, "kind": "oracle",
                              "sample": smp.describe()},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
