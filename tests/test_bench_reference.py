@@ -41,3 +41,25 @@ def test_reference_arm_line(workload):
 def test_reference_arm_enforces_three_warmup_steps():
     d = _line("--workload", "tiny", "--steps", "1", "--warmup", "0", "--ref-seqs", "1", "--ref-budget", "1")
     assert d["warmup"] == 3
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    """Launched as the driver launches N > 1: rank 0 alone runs the oracle and
+    prints one line (on every core of its affinity set); the other rank exits 0
+    without work."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port),
+                        os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--workload", "tiny",
+                        "--steps", "1", "--warmup", "3", "--ref-seqs", "1", "--ref-budget", "1"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    affinity = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    assert d["cpu_baseline"]["cores"] == affinity
