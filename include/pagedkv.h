@@ -426,6 +426,17 @@ PAGEDKV_API kv_status kv_last_device_status(void *stream);
  * kv_last_device_status (which clears them). */
 PAGEDKV_API uint32_t kv_last_device_status_flags(void);
 
+/* Self-test of the failure path ([P3] failure handling is the serving
+ * system's; here: every device-side wait is bounded).  Launches one CTA on
+ * `stream` whose thread waits, at most limit_us microseconds (1 .. 2,000,000),
+ * on an mbarrier phase that nothing completes -- the same kind of bounded wait
+ * the attention pipelines use -- then gives up and sets the timeout flag (8) in
+ * the device status word.  Nothing faults, traps or hangs; the next
+ * kv_last_device_status(stream) returns KV_ERR_DEVICE_BOUNDS with flag 8, and
+ * the context stays usable.  KV_ERR_INVALID for a limit outside the range
+ * (nothing launched). */
+PAGEDKV_API kv_status kv_selftest_bounded_wait(uint32_t limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

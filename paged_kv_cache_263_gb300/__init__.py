@@ -20,7 +20,7 @@ __all__ = [
     "paged_attention_launch_count",
     "kv_last_device_status", "kv_last_device_status_flags", "KV_BF16", "KV_FP8_E4M3",
     "HEAD_DIM", "BLOCK_SIZE", "library_path", "PrefixCache", "kv_swap_out", "kv_swap_in", "kv_waste_stats",
-    "kv_trace_prefill", "kv_trace_prefill_kernel_ms",
+    "kv_trace_prefill", "kv_trace_prefill_kernel_ms", "kv_selftest_bounded_wait",
 ]
 
 HEAD_DIM = 128
@@ -105,6 +105,7 @@ def lib():
             "kv_trace_prefill_kernel_ms": (c.c_double, []),
             "kv_last_device_status": (c.c_int, [P]),
             "kv_last_device_status_flags": (c.c_uint32, []),
+            "kv_selftest_bounded_wait": (c.c_int, [c.c_uint32, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -472,3 +473,9 @@ def kv_last_device_status(stream=None) -> int:
 
 def kv_last_device_status_flags() -> int:
     return int(lib().kv_last_device_status_flags())
+
+
+def kv_selftest_bounded_wait(limit_us: int = 10000, stream=None) -> None:
+    """Launches the failure-path self-test: a device wait that nothing ends gives
+    up after limit_us and sets the timeout flag (8) in the status word."""
+    _check(lib().kv_selftest_bounded_wait(int(limit_us), _stream(stream)), "kv_selftest_bounded_wait")

@@ -88,6 +88,26 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Failure-path self-test: one thread waits, with the given limit, on an
+// mbarrier phase that nothing completes -- the bounded wait every pipeline wait
+// uses -- gives up, and records ST_TIMEOUT in the status word.  Nothing faults
+// or traps, and the context stays usable.  The loop ends on the clock or, as a
+// second bound, after 2^20 tries.
+__global__ void __launch_bounds__(32) bounded_wait_selftest_kernel(unsigned long long limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 0; it < (1u << 20); ++it) {
+        if (mbar_try_wait(b, 0)) return;           // nothing ever arrives on this barrier
+        if (globaltimer() - t0 > limit_ns) break;
+    }
+    atomicOr(&g_status, ST_TIMEOUT);
+}
+
 }  // namespace
 
 namespace pkv_decode { uint32_t take_status(); }
@@ -162,5 +182,13 @@ kv_status kv_last_device_status(void *stream)
 }
 
 uint32_t kv_last_device_status_flags(void) { return g_last_flags.load(std::memory_order_relaxed); }
+
+kv_status kv_selftest_bounded_wait(uint32_t limit_us, void *stream)
+{
+    if (limit_us == 0 || limit_us > 2000000u) return KV_ERR_INVALID;
+    bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        (unsigned long long)limit_us * 1000ull);
+    return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
 
 }  // extern "C"

@@ -233,3 +233,10 @@ def test_launch_count_follows_the_plan():
     # 32,768 keys exceed the longest chunk partition (16,384): the chunk merge runs
     assert n(1, 100, 100, 8, 2, 2048, 1) == 1 + 3
     assert n(1, 100, 100, 8, 2, 2048, 4) == 2 + 3
+
+
+def test_bounded_wait_selftest_refuses_bad_limits():
+    """The failure-path self-test checks its limit on the host: nothing launches."""
+    L = pkv.lib()
+    assert L.kv_selftest_bounded_wait(0, None) == 1
+    assert L.kv_selftest_bounded_wait(2_000_001, None) == 1
