@@ -74,7 +74,7 @@ typedef enum {
     KV_OK = 0,
     KV_ERR_INVALID = 1,        /* bad argument, double free, sharing a free block */
     KV_ERR_OUT_OF_BLOCKS = 2,  /* pool exhausted; the pool is left unchanged */
-    KV_ERR_UNSUPPORTED = 3,    /* shape or dtype this build does not handle */
+    KV_ERR_UNSUPPORTED = 3,    /* shape or dtype this library does not handle */
     KV_ERR_CUDA = 4,           /* a CUDA runtime/driver call or launch failed */
     KV_ERR_DEVICE_BOUNDS = 5   /* device data was out of range (see above) */
 } kv_status;
