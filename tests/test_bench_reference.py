@@ -63,3 +63,31 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     affinity = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     assert d["cpu_baseline"]["cores"] == affinity
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_for_tests", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    return b
+
+
+def test_roofline_traffic_only_while_the_profiled_kernel_is_unchanged(tmp_path):
+    """roofline.traffic comes from the committed ncu summary only while the hash
+    of decode.cu's device-code region matches the one recorded with the counters;
+    an edited kernel reports null."""
+    b = _bench_module()
+    src = os.path.join(ROOT, "paged_kv_cache_263_gb300", "csrc", "decode.cu")
+    with open(os.path.join(ROOT, "profiles", "decode_llama8b_traffic.txt")) as f:
+        recorded = dict(l.split(":", 1) for l in f if ":" in l and not l.startswith("#"))
+    assert b.kernel_source_hash(src) == recorded["kernel_source_sha256"].strip()
+    assert b._traffic(src) == int(recorded["traffic_bytes_per_launch"])
+    # the same file with one device-code line changed
+    text = open(src).read()
+    a = text.index("// ---- device code begin")
+    edited = text[:a] + text[a:].replace("griddep_wait();", "griddep_wait(); ", 1)
+    p = tmp_path / "decode.cu"
+    p.write_text(edited)
+    assert b.kernel_source_hash(str(p)) != b.kernel_source_hash(src)
+    assert b._traffic(str(p)) is None
