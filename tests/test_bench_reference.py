@@ -91,3 +91,18 @@ def test_roofline_traffic_only_while_the_profiled_kernel_is_unchanged(tmp_path):
     p.write_text(edited)
     assert b.kernel_source_hash(str(p)) != b.kernel_source_hash(src)
     assert b._traffic(str(p)) is None
+
+
+def test_launches_per_step_from_the_library_plan():
+    """gpu_launches = steps x (cache write + the kernels the library plans for the
+    attention call), counted without a GPU."""
+    b = _bench_module()
+    import paged_kv_cache_263_gb300 as pkv
+    from synth.workloads import make_workload
+    expect = {"llama8b": 3,          # write, decode, LSE merge
+              "tiny": 3,
+              "spec_verify": 3,      # write, multi-row decode, merge
+              "mixed_prefill": 6,    # write, decode rows + merge, tile prefix, chunk kernel, chunk merge
+              "spec_verify8": 6}
+    for name, n in expect.items():
+        assert b._launches_per_step(pkv, make_workload(name)) == n, name
