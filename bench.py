@@ -1,16 +1,18 @@
 """Benchmark of one paged-attention layer step on GB300.
 
-Default workload: Llama-3-8B layer-shape decode (64 sequences, 32 query / 8 KV
-heads, head_dim 128, contexts uniform in [512, 4096], bf16 cache in a
-65,536-block pool, one new token per sequence appended with reshape_and_cache
-through a slot mapping).  A step is the whole hot path for that batch: the
-cache write of the new tokens, then paged decode attention (split-KV
-partitions merged by the log-sum-exp kernel).
+Default workload: Llama-3-70B layer-shape decode with a shared prefix (128
+sequences, 64 query / 8 KV heads, head_dim 128; every sequence starts with
+the same 2,000-token prefix held once in 125 ref-counted blocks, then a
+private tail of floor(exp(U[ln 1K, ln 32K])) tokens; block 124 forked by
+copy-on-write; bf16 cache; one new token per sequence appended with
+reshape_and_cache through a slot mapping).  A step is the whole hot path for
+that batch: the cache write of the new tokens, then paged decode attention
+(split-KV partitions merged by the log-sum-exp kernel).
 
 Reported metric: achieved HBM GB/s of the step -- algorithmic bytes (every
-K/V element of every sequence read once, Q read, O written, block-table rows
-and lengths read, new K/V written) divided by the measured step time -- and
-microseconds per layer step.
+K/V element of every sequence read once per token, shared prefix blocks
+once, Q read, O written, block-table rows and lengths read, new K/V written)
+divided by the measured step time -- and microseconds per layer step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -68,6 +70,61 @@ def prefill_flops(wl):
     return 4 * wl.num_q_heads * wl.head_dim * total
 
 
+def _blocks(n, bs=16):
+    return -(-int(n) // bs)
+
+
+def algorithmic_bytes(wl) -> dict:
+    """HBM bytes one step must move at least.
+
+    * ``kv_unique``: every cached K/V element read once per (sequence, KV head),
+      counted per token (L tokens x Hkv x D x element bytes, K and V), with the
+      tokens of shared prefix blocks counted once.  This is the method's own
+      byte count.
+    * ``kv_tiles``: the same in whole 16-token (block, head) tiles, which is
+      what a block-granular kernel reads: a sequence's last block is fetched
+      whole although only L mod 16 of its rows are used.
+    * Q read, O written, block-table rows and lengths read, new K/V written."""
+    eb = wl.kv_elem_bytes
+    tok = 2 * wl.num_kv_heads * wl.head_dim * eb                  # K + V bytes of one token
+    tile = wl.block_size * wl.head_dim * eb                       # one (block, head) tile
+    nblk = [_blocks(int(L)) for L in wl.context_lens]
+    pb = _blocks(wl.prefix_tokens) if wl.prefix_tokens else 0
+    # tokens of the prefix blocks every sequence still shares (the copy-on-write
+    # block has one private copy per sequence)
+    shared_tok = sum(min(16, wl.prefix_tokens - 16 * b) for b in range(pb) if b != wl.cow_block)
+    shared_blk = pb - (1 if 0 <= wl.cow_block < pb else 0)
+    dupes = max(wl.num_seqs - 1, 0)
+    kv_unique = tok * (int(wl.context_lens.sum()) - dupes * shared_tok)
+    kv_tiles = 2 * tile * wl.num_kv_heads * (sum(nblk) - dupes * shared_blk)
+    kv_logical = tok * int(wl.context_lens.sum())
+    q = wl.total_q * wl.num_q_heads * wl.head_dim * 2
+    o = wl.total_q * wl.num_q_heads * wl.head_dim * 4
+    meta = 4 * sum(nblk) + 4 * wl.num_seqs
+    new_kv = 2 * wl.total_q * wl.num_kv_heads * wl.head_dim * (2 + eb) + 8 * wl.total_q
+    return {"kv_unique": kv_unique, "kv_tiles": kv_tiles, "kv_logical": kv_logical, "q": q, "o": o,
+            "meta": meta, "new_kv": new_kv, "total": kv_unique + q + o + meta + new_kv}
+
+
+def bench_config(wl, ws, placement) -> dict:
+    """The ``config`` object of the JSON line; both arms print the same one."""
+    ab = algorithmic_bytes(wl)
+    kv_bytes = ab["kv_unique"]
+    flush = kv_bytes < 2 * L2_BYTES
+    return {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
+            "kv_dtype": wl.kv_dtype, "num_blocks": wl.num_blocks,
+            "context_tokens": int(wl.context_lens.sum()), "new_tokens_per_step": wl.total_q,
+            "prefix_tokens": wl.prefix_tokens,
+            "kv_bytes_per_step": kv_bytes, "algorithmic_bytes_per_step": ab["total"],
+            "l2": (f"flushed before every timed step ({2 * L2_BYTES / 1e6:.0f} MB written): the "
+                   f"{kv_bytes / 1e6:.1f} MB of KV fit in the 129 MB L2") if flush else
+                  (f"no flush: every step reads {kv_bytes / 1e6:.0f} MB of KV, "
+                   f"{kv_bytes / L2_BYTES:.1f}x the 129 MB L2"),
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+            "placement": placement}
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -102,9 +159,12 @@ class Clocks:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.skip = 0
         self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
 
-    def start(self):
+    def start(self, wait_s=5.0):
+        """Start sampling every 100 ms; return once the first sample is written
+        (taken before the load starts, so it is left out of the summary)."""
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
@@ -112,6 +172,15 @@ class Clocks:
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t0 = time.monotonic()
+        while time.monotonic() - t0 < wait_s and self.proc.poll() is None:
+            with open(self.path) as f:
+                n = sum(1 for _ in f)
+            if n:
+                self.skip = n
+                return
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -125,7 +194,8 @@ class Clocks:
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for ln in f:
+            lines = f.readlines()[self.skip:]
+            for ln in lines:
                 p = [x.strip() for x in ln.split(",")]
                 if len(p) < 9:
                     continue
@@ -153,12 +223,13 @@ def kernel_source_hash(path):
     return hashlib.sha256(text[a:b].encode()).hexdigest()
 
 
-def _traffic(kernel_src):
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
-    if that summary was taken on the current device code; else None."""
+def _traffic(kernel_src, workload):
+    """Per-launch DRAM bytes of the decode kernel on this workload from the
+    committed ncu summary ``profiles/decode_<workload>_traffic.txt``, if that
+    summary was taken on the current device code; else None."""
     try:
         kv = {}
-        with open(os.path.join(ROOT, "profiles", "decode_llama8b_traffic.txt")) as f:
+        with open(os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.txt")) as f:
             for ln in f:
                 if ":" in ln and not ln.startswith("#"):
                     k, v = ln.split(":", 1)
@@ -214,9 +285,9 @@ class OracleSample:
         self.ks, self.vs = sub.fp8_scales() if self.code == oracle.FP8 else (None, None)
         self.cu = None if sub.is_decode else sub.cu_q_lens
         self.sub, self.m, self.wl = sub, m, wl
-        eb = sub.kv_elem_bytes
-        kv_bytes = 2 * nblk * sub.num_kv_heads * 16 * 128 * eb
-        self.algo_bytes = kv_bytes + int(full_q.sum()) * sub.num_q_heads * 128 * (2 + 4)
+        # the bench's own byte count (per token, shared prefix blocks once) for
+        # the sample, with Q and O of every row of the full sample
+        self.algo_bytes = algorithmic_bytes(sub)["kv_unique"] + int(full_q.sum()) * sub.num_q_heads * 128 * (2 + 4)
 
     def run(self, nthreads=None):
         self.oracle.paged_attention(self.q, self.kc, self.vc, self.tb.tables, self.sub.context_lens, self.cu,
@@ -284,10 +355,9 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "sample": smp.describe(), "device": "host cores",
-                                            "time_scale": smp.scale},
+            "data": "synthetic", "config": bench_config(wl, ws, args.placement),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": smp.threads, "kind": "oracle",
-                             "sample": smp.describe()},
+                             "sample": smp.describe(), "device": "host cores", "time_scale": smp.scale},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -389,7 +459,7 @@ def run_ours(args):
         import numpy as np
         wl.free_order = np.arange(wl.num_blocks, dtype=np.int32)
     dw = DeviceWorkload(wl, device=dev)
-    ab = dw.algorithmic_bytes()
+    ab = algorithmic_bytes(wl)
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -430,19 +500,47 @@ def run_ours(args):
         graph_error = f"{type(e).__name__}: {e}"[:200]
         torch.cuda.synchronize(dev)
     clocks = Clocks(local)
-    clocks.start()                      # sampling covers the warm-up and the timed steps
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     # a workload whose K/V fits in L2 is timed step by step with L2 flushed
     # (a 2x-L2 buffer overwritten, outside the timed events) before each step
     flush = ab["kv_unique"] < 2 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+
+    def clock_window(one_step):
+        """Sample the clocks under load: nvidia-smi starts, then the step runs
+        back to back for at least --clock-window seconds right before the timed
+        region (untimed), and the sampler keeps running through the timed
+        steps.  A timed region of a few ms alone would see no sample."""
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            one_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        est_ms = max(a.elapsed_time(b) / 3, 1e-3)
+        n = max(1, int(args.clock_window * 1e3 / est_ms) + 1)
+        clocks.start()
+        for i in range(n):
+            one_step()
+            if i % 256 == 255:
+                torch.cuda.synchronize(dev)    # keep the host from running far ahead
+        barrier()
+        return n
+
     if graphs:
         g_step, g_attn = graphs
         for _ in range(args.warmup):
+            if flush:
+                flush_buf.zero_()
             g_step.replay()
         barrier()
         if flush:
+            def one():
+                flush_buf.zero_()
+                g_step.replay()
+            window_steps = clock_window(one)
             fe = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
             t_start.record(stream)
             for i in range(K):
@@ -463,6 +561,7 @@ def run_ours(args):
             torch.cuda.synchronize(dev)
             attn_avg_graph = sum(a.elapsed_time(b) for a, b in fa) / K
         else:
+            window_steps = clock_window(g_step.replay)
             t_start.record(stream)
             for i in range(K):
                 g_step.replay()
@@ -493,6 +592,8 @@ def run_ours(args):
     for _ in range(args.warmup):
         dw.step()
     barrier()
+    if not graphs:
+        window_steps = clock_window(dw.step)
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
@@ -590,8 +691,11 @@ def run_ours(args):
                     "kernel": "paged_attention_decode (decode kernel + LSE reduce)" if wl.is_decode else
                               "paged_attention_chunked_prefill (whole call)",
                     "bytes_per_launch": attn_bytes, "avg_launch_ms": attn_avg,
-                    "traffic": _traffic(os.path.join(ROOT, "paged_kv_cache_263_gb300", "csrc", "decode.cu"))
-                    if wl.name == "llama8b" else None}
+                    "bytes": "K/V per token (L x Hkv x 128 x 2 tensors x element bytes, shared prefix "
+                             "blocks once) + Q + O + block-table rows and lengths",
+                    "kv_tile_bytes_per_launch": ab["kv_tiles"],
+                    "traffic": _traffic(os.path.join(ROOT, "paged_kv_cache_263_gb300", "csrc", "decode.cu"),
+                                        wl.name) if wl.is_decode else None}
     else:
         flops = prefill_flops(wl)
         # the chunk kernel's own launches, timed with the library's trace events
@@ -625,17 +729,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if wl.kv_dtype == "bf16" else "fp8-e4m3 cache, f16 math",
         "data": "synthetic",
-        "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
-                   "num_kv_heads": wl.num_kv_heads, "head_dim": 128, "block_size": 16,
-                   "kv_dtype": wl.kv_dtype, "num_blocks": wl.num_blocks,
-                   "context_tokens": int(wl.context_lens.sum()), "new_tokens_per_step": wl.total_q,
-                   "kv_bytes_per_step": kv_bytes, "algorithmic_bytes_per_step": step_bytes,
-                   "l2": (f"flushed before every timed step ({2 * L2_BYTES / 1e6:.0f} MB written): the "
-                          f"{kv_bytes / 1e6:.1f} MB of KV fit in the 129 MB L2") if flush else
-                         (f"no flush: every step reads {kv_bytes / 1e6:.0f} MB of KV, "
-                          f"{kv_bytes / L2_BYTES:.1f}x the 129 MB L2"),
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "placement": args.placement},
+        "config": bench_config(wl, ws, args.placement),
         "roofline": roofline,
         "cache_write_avg_ms": statistics.mean(write_ms),
         "timing": ("CUDA graph replay of the captured step (cache write + attention); roofline per call "
@@ -653,6 +747,9 @@ def run_ours(args):
                                         "copy streams while step i computes; every step moves its own bytes"}},
         "gpu_launches": launches_per_step * K,
         "clocks": ck,
+        "clock_window": {"steps": window_steps, "seconds_min": args.clock_window,
+                         "timing": "untimed back-to-back steps right before the timed region, sampled "
+                                   "with nvidia-smi every 100 ms together with the timed steps"},
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_baseline(wl, budget_s=args.cpu_budget, single_core=wl.name == "tiny")
@@ -860,7 +957,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=500)
-    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--workload", default="llama70b_prefix")
+    ap.add_argument("--clock-window", type=float, default=1.0,
+                    help="seconds of untimed steps, sampled for clocks, right before the timed region")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-seqs", type=int, default=16)

@@ -310,7 +310,10 @@ PAGEDKV_API kv_status paged_attention_decode(float *out, const void *q, const vo
  *    other host threads on the same device) race on it and must be serialised.
  *    It keeps the last call's contents; nothing in it has to start at zero.
  *  - The first call on a device looks up the array's device address with that
- *    device current; make that first call before any stream capture. */
+ *    device current; make that first call before any stream capture.  The
+ *    address is kept with the context that was current; after a device reset
+ *    (a new context) the next call looks it up again, so that call also
+ *    belongs outside any capture. */
 PAGEDKV_API size_t paged_attention_decode_static_scratch_bytes(void);
 PAGEDKV_API kv_status paged_attention_decode_static_scratch(
     float *out, const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,

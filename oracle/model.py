@@ -117,22 +117,27 @@ def expected_paged(wl, tb=None, caches=None, nthreads=0) -> np.ndarray:
                            v_scale=vs, scale=wl.scale, nthreads=nthreads)
 
 
-def _kv_f64(wl, which, s, t1):
-    """Logical K or V of sequence s, tokens 0..t1-1, as the cache holds them (fp64)."""
+def _kv_f64(wl, which, s, t1, dequant=None):
+    """Logical K or V of sequence s, tokens 0..t1-1, as the cache holds them (fp64).
+    For fp8 the bytes are encoded with the workload's scales and decoded with
+    ``dequant`` = (k_scales, v_scales) when given (default: the same scales)."""
     x = wl.seq_kv(which, s, 0, t1)
     if wl.kv_dtype != "fp8":
         return x.to(torch.float64).numpy()
     ks, vs = wl.fp8_scales()
     sc = ks if which == "k" else vs
+    dec = sc if dequant is None else np.asarray(dequant[0 if which == "k" else 1], np.float32)
     f = x.to(torch.float32).numpy()
     codes = e4m3_encode(f / sc[None, :, None].astype(np.float32))
-    return e4m3_decode(codes) * sc[None, :, None].astype(np.float64)
+    return e4m3_decode(codes) * dec[None, :, None].astype(np.float64)
 
 
-def expected_rows(wl, s: int, rows=None, nthreads=0) -> np.ndarray:
+def expected_rows(wl, s: int, rows=None, nthreads=0, dequant=None) -> np.ndarray:
     """fp64 outputs [len(rows)][Hq][D] of query rows ``rows`` (indices within the
     sequence's chunk, default all) of sequence s, from the generator's
-    contiguous values -- usable at any workload size."""
+    contiguous values -- usable at any workload size.  ``dequant`` replaces the
+    scales the fp8 bytes are decoded with (tests use it to model a kernel that
+    applies the wrong scales to the right bytes)."""
     n = int(wl.q_lens[s])
     L = int(wl.context_lens[s])
     if rows is None:
@@ -148,8 +153,8 @@ def expected_rows(wl, s: int, rows=None, nthreads=0) -> np.ndarray:
             j += 1
         r0, r1 = int(rows[i]), int(rows[j]) + 1
         Lsub = L - n + r1                       # keys visible to the last row of the run
-        k = _kv_f64(wl, "k", s, Lsub)
-        v = _kv_f64(wl, "v", s, Lsub)
+        k = _kv_f64(wl, "k", s, Lsub, dequant)
+        v = _kv_f64(wl, "v", s, Lsub, dequant)
         q = wl.q_values(np.arange(cu[s] + r0, cu[s] + r1)).to(torch.float64).numpy()
         out[i:j + 1] = contiguous_attention(q, k, v, scale=wl.scale, nthreads=nthreads)
         i = j + 1

@@ -379,6 +379,8 @@ def paged_attention_decode_static_scratch(out, q, k_cache, v_cache, block_tables
     Calls that overlap on the GPU share that array and must be serialised."""
     _need(out, "out", torch.float32)
     _need(q, "q", torch.bfloat16)
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache")
     _need(block_tables, "block_tables", torch.int32)
     _need(context_lens, "context_lens", torch.int32)
     B, hq, d = q.shape

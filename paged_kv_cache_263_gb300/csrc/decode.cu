@@ -798,24 +798,53 @@ kv_status paged_attention_decode(float *out, const void *q, const void *k_cache,
 // serialise them.  Nothing in it needs to start at zero: every partial that is
 // read was written earlier in the same call.  The first call on a device looks
 // up the array's device address (cudaGetSymbolAddress, with that device
-// current); make that first call before any stream capture.
+// current); make that first call before any stream capture.  The address is
+// remembered together with the device's current context, so a call after a
+// device reset (a new primary context, a new copy of the array) looks it up
+// again instead of using the old one; such a call again belongs outside any
+// capture.
 namespace {
 constexpr size_t STATIC_SCRATCH_BYTES = size_t(32) << 20;
 static __device__ __align__(256) uint8_t g_static_scratch[STATIC_SCRATCH_BYTES];
 constexpr int MAX_DEVICES = 64;
 std::mutex g_scratch_mu;
 void *g_scratch_addr[MAX_DEVICES] = {};
+void *g_scratch_ctx[MAX_DEVICES] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+CtxGetCurrentFn get_ctx_current()
+{
+    static CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(p);
+    }();
+    return fn;
+}
 
 kv_status static_scratch_address(void **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
     if (dev < 0 || dev >= MAX_DEVICES) return KV_ERR_UNSUPPORTED;
+    CtxGetCurrentFn ctx_fn = get_ctx_current();
+    if (!ctx_fn) return KV_ERR_CUDA;
+    // null until the runtime has set up this device's primary context
+    CUcontext ctx = nullptr;
+    if (ctx_fn(&ctx) != CUDA_SUCCESS) return KV_ERR_CUDA;
     std::lock_guard<std::mutex> g(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || !ctx || g_scratch_ctx[dev] != static_cast<void *>(ctx)) {
         void *p = nullptr;
+        // the lookup sets up the primary context when it is not yet current
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return KV_ERR_CUDA;
+        if (ctx_fn(&ctx) != CUDA_SUCCESS) return KV_ERR_CUDA;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_addr[dev];
     return KV_OK;

@@ -45,7 +45,7 @@ class DeviceWorkload:
             self.k_cache = torch.zeros(shape, dtype=cache_dtype, device=self.device)
             self.v_cache = torch.zeros(shape, dtype=cache_dtype, device=self.device)
         if wl.kv_dtype == "fp8":
-            ks, vs = wl.fp8_scales()
+            ks, vs = wl.fp8_scales(device=self.device)
             self.k_scale = torch.from_numpy(ks).to(self.device)
             self.v_scale = torch.from_numpy(vs).to(self.device)
         else:
@@ -149,24 +149,3 @@ class DeviceWorkload:
     def step(self, stream=None):
         self.write_new_tokens(stream)
         return self.attention(stream)
-
-    # ------------------------------------------------------------- bytes
-    def algorithmic_bytes(self) -> dict:
-        """HBM bytes one step must move at least: every cached K/V element read
-        once per (sequence, KV head) -- shared prefix blocks counted once --,
-        Q read, O written, block-table rows and lengths read, new K/V written."""
-        wl = self.wl
-        eb = wl.kv_elem_bytes
-        tile = wl.block_size * wl.head_dim * eb                     # one (block, head) tile
-        nblk = [_blocks(int(L)) for L in wl.context_lens]
-        logical_tiles = sum(nblk) * wl.num_kv_heads
-        pb = _blocks(wl.prefix_tokens) if wl.prefix_tokens else 0
-        shared_dupes = (wl.num_seqs - 1) * max(pb - (1 if wl.cow_block >= 0 else 0), 0) * wl.num_kv_heads
-        kv_unique = 2 * tile * (logical_tiles - shared_dupes)
-        kv_logical = 2 * tile * logical_tiles
-        q = wl.total_q * wl.num_q_heads * wl.head_dim * 2
-        o = wl.total_q * wl.num_q_heads * wl.head_dim * 4
-        meta = 4 * sum(nblk) + 4 * wl.num_seqs
-        new_kv = 2 * wl.total_q * wl.num_kv_heads * wl.head_dim * (2 + eb) + 8 * wl.total_q
-        return {"kv_unique": kv_unique, "kv_logical": kv_logical, "q": q, "o": o, "meta": meta,
-                "new_kv": new_kv, "total": kv_unique + q + o + meta + new_kv}

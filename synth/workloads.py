@@ -43,11 +43,24 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-from . import IH4_MAX_ABS, normal_bf16, stream_key
+from . import normal_bf16, stream_key
 
-__all__ = ["Workload", "make_workload", "WORKLOADS", "EXTRA_WORKLOADS", "small_workload"]
+__all__ = ["Workload", "make_workload", "WORKLOADS", "EXTRA_WORKLOADS", "small_workload",
+           "DISTINCT_FP8_FACTORS", "E4M3_MAX"]
 
 Q_STREAM, K_STREAM, V_STREAM = 0, 1, 2
+
+E4M3_MAX = np.float32(448.0)          # largest finite e4m3 magnitude
+
+# Per-(tensor, KV head) multipliers of the fp8 scales for parity tests of the
+# scale path: K and V scales then differ from each other and from head to head
+# by up to 8x, so a kernel that swapped them, or read one head's scale for
+# another, would be far outside the tolerance.  Factors below 1 make the
+# largest values saturate at 448, which is part of what the tests exercise.
+DISTINCT_FP8_FACTORS = (
+    np.array([1.0, 2.5, 0.5, 4.0, 0.75, 3.0, 1.5, 0.625], dtype=np.float32),   # K, head 0..7
+    np.array([3.0, 0.5, 2.0, 0.625, 4.0, 1.0, 0.75, 2.5], dtype=np.float32),   # V, head 0..7
+)
 
 
 @dataclass
@@ -67,7 +80,9 @@ class Workload:
     head_dim: int = 128
     block_size: int = 16
     description: str = ""
+    fp8_scale_factors: tuple = None  # (K [Hkv], V [Hkv]) fp32 multipliers of the amax scales
     _tail_base: np.ndarray = field(default=None, repr=False)
+    _fp8_scales: tuple = field(default=None, repr=False)
 
     def __post_init__(self):
         self.context_lens = np.asarray(self.context_lens, dtype=np.int32)
@@ -148,13 +163,50 @@ class Workload:
         out = normal_bf16(stream_key(self.seed, Q_STREAM), ctr)
         return out.view(len(rows), self.num_q_heads, self.head_dim)
 
-    def fp8_scales(self):
-        """Per-KV-head fp32 scales for K and V.  The generator's values are bounded
-        by IH4_MAX_ABS, so amax/448 with that bound maps every value into the
-        finite e4m3 range without saturation."""
-        s = np.float32(np.float32(IH4_MAX_ABS) / np.float32(448.0))
-        ks = np.full(self.num_kv_heads, s, dtype=np.float32)
-        return ks, ks.copy()
+    @property
+    def unique_tokens(self) -> int:
+        """Distinct logical tokens of the workload: the shared prefix once plus
+        every sequence's own tokens.  Their value-stream keys are exactly
+        0 .. unique_tokens - 1 (see token_keys)."""
+        return int(self.prefix_tokens + (self.context_lens.astype(np.int64) - self.prefix_tokens).sum())
+
+    def kv_amax(self, device="cpu", chunk_tokens=1 << 15):
+        """Per-KV-head max |x| of the K and of the V values of every token of the
+        workload (bf16 values, so exact in fp32): two fp32 arrays [Hkv].  A max
+        is exact, so the result does not depend on the device that scans."""
+        ka = torch.zeros(self.num_kv_heads, dtype=torch.float32, device=device)
+        va = torch.zeros_like(ka)
+        n = self.unique_tokens
+        for a in range(0, n, chunk_tokens):
+            keys = np.arange(a, min(n, a + chunk_tokens), dtype=np.int64)
+            for which, acc in (("k", ka), ("v", va)):
+                x = self.kv_values(which, keys, device).float().abs()
+                torch.maximum(acc, x.amax(dim=(0, 2)), out=acc)
+        return ka.cpu().numpy(), va.cpu().numpy()
+
+    def fp8_scales(self, device=None):
+        """Per-KV-head fp32 scales of K and of V for the fp8-e4m3 cache.
+
+        The reading taken for the scale (the pages leave it open): one scale per
+        KV head and per tensor, s = amax / 448 over all of that head's values
+        in the workload (IEEE fp32 division), so the largest value maps to the
+        largest finite e4m3 magnitude.  With ``fp8_scale_factors`` set, each
+        scale is then multiplied (fp32) by its factor.  Computed once and kept;
+        the scan runs on ``device`` (default: the GPU if torch has one, else
+        the CPU -- the max is exact, so both give the same bits)."""
+        if self._fp8_scales is None:
+            if device is None:
+                device = "cuda" if torch.cuda.is_available() else "cpu"
+            ka, va = self.kv_amax(device)
+            ks = (ka.astype(np.float32) / E4M3_MAX).astype(np.float32)
+            vs = (va.astype(np.float32) / E4M3_MAX).astype(np.float32)
+            if self.fp8_scale_factors is not None:
+                kf, vf = self.fp8_scale_factors
+                ks = (ks * np.resize(np.asarray(kf, np.float32), self.num_kv_heads)).astype(np.float32)
+                vs = (vs * np.resize(np.asarray(vf, np.float32), self.num_kv_heads)).astype(np.float32)
+            self._fp8_scales = (ks, vs)
+        ks, vs = self._fp8_scales
+        return ks.copy(), vs.copy()
 
     # ------------------------------------------------------------ bytes
     def kv_bytes_per_token(self) -> int:
@@ -186,7 +238,15 @@ def _pool_to_fit(lens, prefix, cow, bs=16, slack=1.02):
     return int(math.ceil(need * slack / 1024.0) * 1024)
 
 
-def make_workload(name: str) -> Workload:
+def make_workload(name: str, fp8_scale_factors=None) -> Workload:
+    """The named workload; ``fp8_scale_factors`` (K, V multipliers per KV head)
+    changes the fp8 scales of an fp8 workload (see Workload.fp8_scales)."""
+    wl = _make(name)
+    wl.fp8_scale_factors = fp8_scale_factors
+    return wl
+
+
+def _make(name: str) -> Workload:
     if name in ("tiny", "cfg1", "1"):
         seed = 2631
         rng = np.random.Generator(np.random.PCG64(seed))
@@ -243,13 +303,13 @@ def make_workload(name: str) -> Workload:
                         rng.permutation(pool), num_splits=16,
                         description="long-context split-KV decode, fp8-e4m3 cache, 16 partitions")
     if name == "mixed_prefill_small_fp8":
-        wl = make_workload("mixed_prefill_small")
+        wl = _make("mixed_prefill_small")
         wl.name, wl.kv_dtype, wl.seed = "mixed_prefill_small_fp8", "fp8", 2645
         wl.description = "the profiling mix over an fp8-e4m3 cache"
         return wl
     if name == "mixed_prefill_fp8":
         # the chunked-prefill mix with an fp8-e4m3 cache
-        wl = make_workload("mixed_prefill")
+        wl = _make("mixed_prefill")
         wl.name, wl.kv_dtype, wl.seed = "mixed_prefill_fp8", "fp8", 2639
         wl.description = "chunked-prefill mix over an fp8-e4m3 cache"
         return wl
@@ -281,7 +341,7 @@ EXTRA_WORKLOADS = ("mixed_prefill_small", "mixed_prefill_small_fp8", "mixed_pref
 
 def small_workload(seed: int, lens, q_lens=None, hq=8, hkv=2, kv_dtype="bf16", num_blocks=None,
                    prefix_tokens=0, cow_block=-1, num_splits=0, head_dim=128, block_size=16,
-                   name="small") -> Workload:
+                   name="small", fp8_scale_factors=None) -> Workload:
     """A small workload for parity tests: same recipe, caller-chosen sizes."""
     rng = np.random.Generator(np.random.PCG64(seed))
     lens = np.asarray(lens, dtype=np.int32)
@@ -292,4 +352,4 @@ def small_workload(seed: int, lens, q_lens=None, hq=8, hkv=2, kv_dtype="bf16", n
     return Workload(name, seed, hq, hkv, num_blocks, kv_dtype, lens, q_lens,
                     rng.permutation(num_blocks), prefix_tokens=prefix_tokens,
                     cow_block=cow_block, num_splits=num_splits, head_dim=head_dim,
-                    block_size=block_size)
+                    block_size=block_size, fp8_scale_factors=fp8_scale_factors)

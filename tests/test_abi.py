@@ -240,3 +240,40 @@ def test_bounded_wait_selftest_refuses_bad_limits():
     L = pkv.lib()
     assert L.kv_selftest_bounded_wait(0, None) == 1
     assert L.kv_selftest_bounded_wait(2_000_001, None) == 1
+
+
+class _FakeDeviceTensor:
+    """Stands in for a contiguous CUDA tensor where only the binding's argument
+    checks look at it (no GPU here; nothing is launched)."""
+
+    def __init__(self, dtype, shape):
+        self.dtype, self.shape, self.is_cuda = dtype, shape, True
+
+    def is_contiguous(self):
+        return True
+
+
+@pytest.mark.parametrize("bad", ["k_cpu", "v_cpu", "k_strided"])
+def test_static_scratch_decode_checks_the_caches_before_any_launch(bad, monkeypatch):
+    """A CPU or non-contiguous cache is refused by the binding with ValueError
+    before the library is called, as paged_attention_decode does."""
+    import torch
+    called = []
+    monkeypatch.setattr(pkv, "lib", lambda: called.append(1))
+    out = _FakeDeviceTensor(torch.float32, (2, 8, 128))
+    q = _FakeDeviceTensor(torch.bfloat16, (2, 8, 128))
+    bt = _FakeDeviceTensor(torch.int32, (2, 4))
+    cl = _FakeDeviceTensor(torch.int32, (2,))
+    good = _FakeDeviceTensor(torch.bfloat16, (16, 2, 16, 128))
+    cpu = torch.zeros(16, 2, 16, 128, dtype=torch.bfloat16)
+    k, v = good, good
+    if bad == "k_cpu":
+        k = cpu
+    elif bad == "v_cpu":
+        v = cpu
+    else:
+        k = _FakeDeviceTensor(torch.bfloat16, (16, 2, 16, 128))
+        k.is_contiguous = lambda: False
+    with pytest.raises(ValueError, match="k_cache|v_cache"):
+        pkv.paged_attention_decode_static_scratch(out, q, k, v, bt, cl)
+    assert not called

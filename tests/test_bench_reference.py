@@ -29,11 +29,15 @@ def test_reference_arm_line(workload):
     assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["config"]["workload"] == workload and d["dtype"] == "f64" and d["data"] == "synthetic"
+    # both arms print the same config object
+    b = _bench_module()
+    from synth.workloads import make_workload
+    assert d["config"] == b.bench_config(make_workload(workload), 1, "random")
     # a long chunk is sampled on a few rows, its time scaled by (row, key) pairs
-    assert d["config"]["time_scale"] >= 1.0
-    if workload == "mixed_prefill_small":
-        assert d["config"]["time_scale"] > 10 and "scaled" in d["config"]["sample"]
     cb = d["cpu_baseline"]
+    assert cb["time_scale"] >= 1.0
+    if workload == "mixed_prefill_small":
+        assert cb["time_scale"] > 10 and "scaled" in cb["sample"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
 
@@ -82,7 +86,7 @@ def test_roofline_traffic_only_while_the_profiled_kernel_is_unchanged(tmp_path):
     with open(os.path.join(ROOT, "profiles", "decode_llama8b_traffic.txt")) as f:
         recorded = dict(l.split(":", 1) for l in f if ":" in l and not l.startswith("#"))
     assert b.kernel_source_hash(src) == recorded["kernel_source_sha256"].strip()
-    assert b._traffic(src) == int(recorded["traffic_bytes_per_launch"])
+    assert b._traffic(src, "llama8b") == int(recorded["traffic_bytes_per_launch"])
     # the same file with one device-code line changed
     text = open(src).read()
     a = text.index("// ---- device code begin")
@@ -90,7 +94,8 @@ def test_roofline_traffic_only_while_the_profiled_kernel_is_unchanged(tmp_path):
     p = tmp_path / "decode.cu"
     p.write_text(edited)
     assert b.kernel_source_hash(str(p)) != b.kernel_source_hash(src)
-    assert b._traffic(str(p)) is None
+    assert b._traffic(str(p), "llama8b") is None
+    assert b._traffic(src, "no_such_workload") is None
 
 
 def test_launches_per_step_from_the_library_plan():
@@ -106,3 +111,28 @@ def test_launches_per_step_from_the_library_plan():
               "spec_verify8": 6}
     for name, n in expect.items():
         assert b._launches_per_step(pkv, make_workload(name)) == n, name
+
+
+def test_algorithmic_bytes_count_tokens_and_the_shared_prefix_once():
+    """K/V bytes are per token (L x Hkv x 128 x 2 x element bytes), the shared
+    prefix blocks once; whole 16-token tiles are reported beside them."""
+    b = _bench_module()
+    from synth.workloads import make_workload, small_workload
+    wl = make_workload("llama8b")
+    ab = b.algorithmic_bytes(wl)
+    assert ab["kv_unique"] == int(wl.context_lens.sum()) * 8 * 128 * 2 * 2
+    assert ab["kv_tiles"] == sum(-(-int(L) // 16) for L in wl.context_lens) * 8 * 16 * 128 * 2 * 2
+    assert ab["kv_tiles"] - ab["kv_unique"] < 64 * 16 * 8 * 128 * 4
+    # 70B shape: 124 prefix blocks shared by all 128 sequences, block 124 forked per sequence
+    wl = make_workload("llama70b_prefix")
+    ab = b.algorithmic_bytes(wl)
+    tok = 8 * 128 * 2 * 2
+    assert ab["kv_unique"] == tok * (int(wl.context_lens.sum()) - 127 * 1984)
+    assert ab["kv_logical"] - ab["kv_unique"] == tok * 127 * 1984
+    # a 40-token prefix: blocks 0 and 1 shared (32 tokens), block 2 (8 tokens) forked
+    wl = small_workload(5, lens=[50, 60, 70], prefix_tokens=40, cow_block=2, hkv=2)
+    ab = b.algorithmic_bytes(wl)
+    assert ab["kv_unique"] == 2 * 128 * 2 * 2 * (180 - 2 * 32)
+    # fp8: one byte per element
+    wl = make_workload("split_fp8")
+    assert b.algorithmic_bytes(wl)["kv_unique"] == 8 * 131072 * 8 * 128 * 2

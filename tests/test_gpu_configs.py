@@ -9,7 +9,7 @@ import oracle
 from oracle import model as omodel
 from paged_kv_cache_263_gb300.workload import DeviceWorkload
 import paged_kv_cache_263_gb300 as pkv
-from synth.workloads import make_workload
+from synth.workloads import DISTINCT_FP8_FACTORS, make_workload
 from tests.gpu_util import TOL, cache_bytes, max_abs, require_gpu
 
 pytestmark = pytest.mark.gpu
@@ -47,8 +47,8 @@ def _check_cache_samples(wl, dw, tb, n=2000, seed=0):
     assert np.array_equal(got_v, ref_v)
 
 
-def _check(name, sample_seqs, nthreads=0):
-    wl = make_workload(name)
+def _check(name, sample_seqs, nthreads=0, fp8_scale_factors=None):
+    wl = make_workload(name, fp8_scale_factors=fp8_scale_factors)
     tb = omodel.build_tables(wl)
     dw = DeviceWorkload(wl)
     assert np.array_equal(dw.tables_host, tb.tables)
@@ -85,4 +85,16 @@ def test_llama70b_shared_prefix_decode():
 
 
 def test_split_kv_fp8_long_context():
-    _check("split_fp8", [0, 5])
+    _, _ = _check("split_fp8", [0, 5])
+
+
+def test_split_kv_fp8_long_context_distinct_per_head_scales():
+    """The full-size split-KV fp8 batch with K and V scales that differ by head
+    and by tensor (up to 8x): sampled sequences against the oracle, and the
+    oracle with the K and V scales swapped is far from the GPU output."""
+    dw, _ = _check("split_fp8", [2, 7], fp8_scale_factors=DISTINCT_FP8_FACTORS)
+    wl = dw.wl
+    ks, vs = wl.fp8_scales()
+    assert len(set(ks.tolist()) | set(vs.tolist())) == 16
+    got = dw.out.cpu().numpy()
+    assert max_abs(got[2:3], omodel.expected_rows(wl, 2, dequant=(vs, ks))) > 4 * TOL["fp8"]

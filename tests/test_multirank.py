@@ -27,7 +27,7 @@ def _worker(rank, world, port, out):
 def test_slowest_rank_time_and_weak_scaling():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()       # no fork of a multi-threaded process
     out = mgr.dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     assert out[0] == out[1] == 15.0

@@ -307,3 +307,23 @@ def test_sequence_without_query_rows_has_no_output_and_changes_nothing():
     assert full.shape[0] == 6
     assert np.array_equal(full[0:5], om.expected_rows(wl, 0))
     assert np.array_equal(full[5:6], om.expected_rows(wl, 2))
+
+
+def test_expected_rows_dequant_override_models_wrong_scales_on_the_right_bytes():
+    """expected_rows(dequant=...) decodes the same fp8 bytes with other scales:
+    with the workload's own scales it is the paged oracle bit for bit, and with
+    K and V scales swapped it equals the paged oracle called with swapped
+    scales over the same cache."""
+    from synth.workloads import DISTINCT_FP8_FACTORS
+    wl = small_workload(72, lens=[60, 33], q_lens=[1, 4], hq=8, hkv=2, kv_dtype="fp8",
+                        fp8_scale_factors=DISTINCT_FP8_FACTORS)
+    tb = model.build_tables(wl)
+    kc, vc = model.build_cache(wl, tb)
+    ks, vs = wl.fp8_scales()
+    q = wl.q_values().contiguous().view(torch.int16).numpy().view(np.uint16)
+    cu = wl.cu_q_lens
+    for dq in ((ks, vs), (vs, ks)):
+        full = oracle.paged_attention(q, kc, vc, tb.tables, wl.context_lens, cu, dtype=oracle.FP8,
+                                      k_scale=dq[0], v_scale=dq[1], scale=wl.scale)
+        for s in range(2):
+            assert np.array_equal(model.expected_rows(wl, s, dequant=dq), full[cu[s]:cu[s + 1]])

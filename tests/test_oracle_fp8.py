@@ -100,3 +100,47 @@ def test_cache_write_quantises_with_fp32_division():
             assert np.array_equal(vc[b, h, o], oracle.e4m3_encode(xf[t, h] / vs[h]))
     # the skipped token wrote nothing
     assert kc[0, :, 2].sum() == 0 and (kc[1, :, 0:1].sum() == 0)
+
+
+def test_paged_attention_dequantises_with_each_heads_own_k_and_v_scale():
+    """Closed form for the fp8 cache with per-KV-head scales that differ between
+    K and V and across heads ("Quantising the cache": the stored byte times its
+    scale is the value).  Sequence 0 has one key: every query head h of KV head
+    g = h // G returns e4m3(v) * v_scale[g].  Sequence 1 has two keys: the
+    weights are the two-way softmax of scale * q . (e4m3(k_t) * k_scale[g]),
+    written out by hand here.  The decode of the bytes is torch's.  A swapped
+    pair of scales, or head 0's scale used for every head, fails the check."""
+    Hq, Hkv, D, G = 6, 3, 128, 2
+    rng = np.random.default_rng(11)
+    codes = rng.integers(0, 256, size=(4, Hkv, 16, D), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x30                      # no NaN codes
+    kc, vc = codes[:2].copy(), codes[2:].copy()              # 2 blocks each
+    ks = np.array([0.37, 2.9, 0.011], np.float32)
+    vs = np.array([5.0, 0.11, 0.8], np.float32)
+    tables = np.array([[1], [0]], np.int32)
+    lens = np.array([1, 2], np.int32)
+    q = torch.randn(2, Hq, D, dtype=torch.float64).to(torch.bfloat16)
+    q_bits = q.view(torch.int16).numpy().view(np.uint16)
+    scale = 1.0 / np.sqrt(D)
+
+    def dec(c):
+        return torch.from_numpy(np.ascontiguousarray(c)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+    def run(k_scale, v_scale):
+        return oracle.paged_attention(q_bits, kc, vc, tables, lens, dtype=oracle.FP8, k_scale=k_scale,
+                                      v_scale=v_scale, scale=scale)
+
+    out = run(ks, vs)
+    qd = q.to(torch.float64).numpy()
+    exp = np.zeros_like(out)
+    for h in range(Hq):
+        g = h // G
+        exp[0, h] = dec(vc[1, g, 0]) * float(vs[g])                       # one key: its value
+        k0, k1 = dec(kc[0, g, 0]) * float(ks[g]), dec(kc[0, g, 1]) * float(ks[g])
+        z0, z1 = scale * qd[1, h] @ k0, scale * qd[1, h] @ k1
+        w1 = 1.0 / (1.0 + np.exp(z0 - z1))
+        exp[1, h] = (1.0 - w1) * dec(vc[0, g, 0]) * float(vs[g]) + w1 * dec(vc[0, g, 1]) * float(vs[g])
+    assert np.abs(out - exp).max() <= 1e-12 * max(1.0, np.abs(exp).max())
+    # the check has teeth: plausible scale mistakes move the result far away
+    for wk, wv in ((vs, ks), (np.full(3, ks[0], np.float32), np.full(3, vs[0], np.float32))):
+        assert np.abs(run(wk, wv) - exp).max() > 0.1

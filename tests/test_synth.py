@@ -69,3 +69,30 @@ def test_prefix_tokens_share_keys():
     a = wl.token_keys(0, 0, 2010)
     b = wl.token_keys(5, 0, 2010)
     assert np.array_equal(a[:2000], b[:2000]) and not np.array_equal(a[2000:], b[2000:])
+
+
+def test_fp8_scales_are_per_head_amax_over_every_token():
+    """The fp8 scales of a workload: per KV head, separately for K and V, the
+    largest |value| over every token of every sequence (the shared prefix once)
+    divided by 448 in fp32.  Checked by brute force: each sequence's K/V
+    gathered token by token through its own keys, then an elementwise max."""
+    import numpy as np
+    from synth.workloads import DISTINCT_FP8_FACTORS, small_workload
+    wl = small_workload(21, lens=[40, 77, 300], hq=8, hkv=4, kv_dtype="fp8", prefix_tokens=40, cow_block=2)
+    ka = np.zeros(4, np.float32)
+    va = np.zeros(4, np.float32)
+    for s in range(wl.num_seqs):
+        k = wl.seq_kv("k", s).float().abs().numpy()
+        v = wl.seq_kv("v", s).float().abs().numpy()
+        ka = np.maximum(ka, k.max(axis=(0, 2)))
+        va = np.maximum(va, v.max(axis=(0, 2)))
+    ks, vs = wl.fp8_scales(device="cpu")
+    assert np.array_equal(ks, (ka / np.float32(448)).astype(np.float32))
+    assert np.array_equal(vs, (va / np.float32(448)).astype(np.float32))
+    assert ks.dtype == np.float32 and len(set(ks.tolist())) > 1 and not np.array_equal(ks, vs)
+    # with the test factors each scale is multiplied by its own factor
+    wl2 = small_workload(21, lens=[40, 77, 300], hq=8, hkv=4, kv_dtype="fp8", prefix_tokens=40, cow_block=2,
+                         fp8_scale_factors=DISTINCT_FP8_FACTORS)
+    ks2, vs2 = wl2.fp8_scales(device="cpu")
+    assert np.array_equal(ks2, (ks * DISTINCT_FP8_FACTORS[0][:4]).astype(np.float32))
+    assert np.array_equal(vs2, (vs * DISTINCT_FP8_FACTORS[1][:4]).astype(np.float32))

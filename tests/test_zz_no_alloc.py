@@ -6,8 +6,10 @@ it is up, a host without any allocator), so they cannot hand the library the
 workspace its split-KV partials need.  paged_attention_decode_static_scratch
 keeps those partials in a fixed-size device array inside the library instead.
 Here it is called through the C ABI twice in a row, on two different batches
-that both need split partials, and each output is compared with the output of
-the ordinary paged_attention_decode (caller workspace) on the same inputs.
+that both need split partials.  Each output must equal, bit for bit, the output
+of the ordinary paged_attention_decode (caller workspace) on the same inputs --
+the two run the same kernels with the same partitions, only the partials live
+elsewhere -- and must match the fp64 oracle within the parity tolerance.
 The file name sorts last so a stop-at-first-failure run has already run every
 other test when it gets here."""
 import numpy as np
@@ -16,8 +18,9 @@ import torch
 
 import paged_kv_cache_263_gb300 as pkv
 from paged_kv_cache_263_gb300.workload import DeviceWorkload
+from oracle import model as omodel
 from synth.workloads import make_workload, small_workload
-from tests.gpu_util import TOL, max_abs, require_gpu
+from tests.gpu_util import TOL, expected_full, max_abs, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -51,7 +54,16 @@ def test_static_scratch_decode_matches_workspace_decode_twice():
         assert 0 < need <= cap                 # both calls really use the scratch
         ref, got = _both(dw)
         assert np.isfinite(got).all()
-        assert max_abs(got, ref) <= TOL[wl.kv_dtype]
+        assert np.array_equal(got, ref)
+        if wl.num_seqs > 8:
+            # the large batch: the oracle's rows of the shortest, longest and two more sequences
+            order = np.argsort(wl.context_lens)
+            seqs = [int(order[0]), int(order[-1]), 7, 40]
+            for s in seqs:
+                assert max_abs(got[s:s + 1], omodel.expected_rows(wl, s)) <= TOL[wl.kv_dtype]
+        else:
+            _, _, exp = expected_full(wl)
+            assert max_abs(got, exp) <= TOL[wl.kv_dtype]
 
 
 def test_static_scratch_refuses_batches_that_do_not_fit():
