@@ -30,7 +30,7 @@ def _stale() -> bool:
     if not os.path.exists(OUT):
         return True
     t = os.path.getmtime(OUT)
-    deps = _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [
+    deps = _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + [
         os.path.join(os.path.dirname(HERE), "include", "pagedkv.h"), __file__]
     return any(os.path.getmtime(f) > t for f in deps)
 

@@ -15,6 +15,7 @@
 // "Sharing, and what makes a prefix reusable" (a writer into a shared block
 // first gets its own copy); "M.65 Inference serving", block management (g).
 #include "common.cuh"
+#include "trace.h"
 
 #include <algorithm>
 
@@ -145,6 +146,7 @@ kv_status reshape_and_cache(const void *k, const void *v, void *k_cache, void *v
                             int32_t num_blocks, kv_dtype dtype, const float *k_scale,
                             const float *v_scale, void *stream)
 {
+    PKV_NVTX_RANGE("reshape_and_cache");
     if (num_tokens == 0) return KV_OK;
     if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 1) return KV_ERR_INVALID;
     if (!k || !v || !k_cache || !v_cache || !slot_mapping) return KV_ERR_INVALID;

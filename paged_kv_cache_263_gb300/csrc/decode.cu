@@ -34,6 +34,7 @@
 //    partitions with the log-sum-exp rule in fixed order -- no atomics, so the
 //    result is bitwise independent of physical placement.
 #include "common.cuh"
+#include "trace.h"
 
 #include <algorithm>
 #include <mutex>
@@ -775,6 +776,7 @@ kv_status paged_attention_decode(float *out, const void *q, const void *k_cache,
                                  const float *k_scale, const float *v_scale, int32_t num_splits,
                                  void *workspace, size_t workspace_bytes, void *stream)
 {
+    PKV_NVTX_RANGE("paged_attention_decode");
     return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            nullptr, num_seqs, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                            k_scale, v_scale, num_splits, workspace, workspace_bytes,
@@ -863,6 +865,7 @@ kv_status paged_attention_decode_static_scratch(float *out, const void *q, const
                                                 kv_dtype dtype, const float *k_scale,
                                                 const float *v_scale, int32_t num_splits, void *stream)
 {
+    PKV_NVTX_RANGE("paged_attention_decode_static_scratch");
     const size_t need = pkv_decode::workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, num_splits);
     if (need > STATIC_SCRATCH_BYTES) return KV_ERR_UNSUPPORTED;
     void *scratch = nullptr;

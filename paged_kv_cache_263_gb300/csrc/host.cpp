@@ -10,6 +10,7 @@
 // to reclaim it", section "Sharing, and what makes a prefix reusable" (one
 // physical copy, many block tables; a writer first gets its own copy).
 #include <cuda.h>
+#include "trace.h"
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -155,6 +156,7 @@ kv_status kv_block_share(kv_pool *pool, const int32_t *ids, int32_t n)
 kv_status kv_copy_on_write(kv_pool *pool, int32_t id, int32_t *out_id, void *k_cache,
                            void *v_cache, int32_t num_kv_heads, kv_dtype dtype, void *stream)
 {
+    PKV_NVTX_RANGE("kv_copy_on_write");
     if (!pool || !out_id) return KV_ERR_INVALID;
     if ((k_cache == nullptr) != (v_cache == nullptr)) return KV_ERR_INVALID;
     if (k_cache && (num_kv_heads < 1 || (dtype != KV_BF16 && dtype != KV_FP8_E4M3)))

@@ -50,6 +50,7 @@
 // v_scale into O.  Quantising Q to e4m3 for a kind::f8f6f4 product would cost
 // precision the bf16 queries carry.
 #include "common.cuh"
+#include "trace.h"
 
 #include <algorithm>
 #include <mutex>
@@ -923,6 +924,7 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
                                           int32_t num_splits, void *workspace,
                                           size_t workspace_bytes, void *stream)
 {
+    PKV_NVTX_RANGE("paged_attention_chunked_prefill");
     if (num_seqs == 0 || total_q_tokens == 0) return KV_OK;
     if (num_seqs < 0 || total_q_tokens < 0 || max_q_len < 1 || !cu_q_lens || !context_lens || !out || !q ||
         !k_cache || !v_cache || !block_tables || num_q_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 ||

@@ -16,6 +16,7 @@
 // and each thread keeps UNROLL units in flight to cover the link's latency.
 // The grid is a whole number of waves over the 152 SMs.
 #include "common.cuh"
+#include "trace.h"
 
 #include <algorithm>
 
@@ -140,6 +141,7 @@ kv_status kv_swap_out(const void *k_cache, const void *v_cache, int32_t num_bloc
                       kv_dtype dtype, const int32_t *block_ids, int32_t n, void *host_k, void *host_v,
                       void *stream)
 {
+    PKV_NVTX_RANGE("kv_swap_out");
     return launch(true, const_cast<void *>(k_cache), const_cast<void *>(v_cache), num_blocks, num_kv_heads, dtype,
                   block_ids, n, host_k, host_v, static_cast<cudaStream_t>(stream));
 }
@@ -147,6 +149,7 @@ kv_status kv_swap_out(const void *k_cache, const void *v_cache, int32_t num_bloc
 kv_status kv_swap_in(void *k_cache, void *v_cache, int32_t num_blocks, int32_t num_kv_heads, kv_dtype dtype,
                      const int32_t *block_ids, int32_t n, const void *host_k, const void *host_v, void *stream)
 {
+    PKV_NVTX_RANGE("kv_swap_in");
     return launch(false, k_cache, v_cache, num_blocks, num_kv_heads, dtype, block_ids, n, host_k, host_v,
                   static_cast<cudaStream_t>(stream));
 }

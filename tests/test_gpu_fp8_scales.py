@@ -47,19 +47,20 @@ def _check(wl, q_scale=None, plant=True):
     dw = DeviceWorkload(wl)
     caches = omodel.build_cache(wl, tb)
     assert np.array_equal(dw.tables_host, tb.tables)
-    # the cache the kernels read holds the oracle's bytes (per-head scales at the write)
-    assert np.array_equal(cache_bytes(dw.k_cache), caches[0])
-    assert np.array_equal(cache_bytes(dw.v_cache), caches[1])
     q_bits = None
     if q_scale is not None:
         q = (wl.q_values().float() * q_scale).to(torch.bfloat16)
         dw.q.copy_(q.to(dw.q.device))
         q_bits = bits(q)
-    dw.step()
+    dw.step()                                   # writes the step's new tokens, then attends
     assert pkv.kv_last_device_status() == 0
+    # the cache the kernels read holds the oracle's bytes (per-head scales at the write)
+    assert np.array_equal(cache_bytes(dw.k_cache), caches[0])
+    assert np.array_equal(cache_bytes(dw.v_cache), caches[1])
     got = dw.out.cpu().numpy().astype(np.float64)
     ks, vs = wl.fp8_scales()
-    assert len(set(ks.tolist()) | set(vs.tolist())) == 2 * wl.num_kv_heads      # all distinct
+    # K and V scales differ head by head, and the heads' scales differ from each other
+    assert (ks != vs).all() and len(set(ks.tolist())) == len(set(vs.tolist())) == wl.num_kv_heads
     err = max_abs(got, _oracle(wl, tb, caches, ks, vs, q_bits))
     assert err <= TOL["fp8"], err
     if not plant:
