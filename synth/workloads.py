@@ -332,11 +332,22 @@ def _make(name: str) -> Workload:
         return Workload("spec_verify8", seed, 64, 8, pool, "bf16", lens, np.full(32, 8, np.int32),
                         rng.permutation(pool),
                         description="speculative verify: 32 sequences x 8 draft tokens, Llama-3-70B layer shape")
+    if name == "prefill_chunk":
+        # the chunk of the mixed batch alone (no decode rows): the tensor-core
+        # kernel's own roofline without the decode rows sharing the SMs
+        seed = 2646
+        rng = np.random.Generator(np.random.PCG64(seed))
+        lens = np.array([101024], dtype=np.int32)
+        pool = _pool_to_fit(lens, 0, -1)
+        return Workload("prefill_chunk", seed, 64, 8, pool, "bf16", lens, np.array([1024], np.int32),
+                        rng.permutation(pool),
+                        description="one 1,024-token chunk over 100,000 cached tokens, alone")
     raise KeyError(name)
 
 
 WORKLOADS = ("tiny", "llama8b", "llama70b_prefix", "mixed_prefill", "split_fp8")
-EXTRA_WORKLOADS = ("mixed_prefill_small", "mixed_prefill_small_fp8", "mixed_prefill_fp8", "spec_verify", "spec_verify8")
+EXTRA_WORKLOADS = ("mixed_prefill_small", "mixed_prefill_small_fp8", "mixed_prefill_fp8", "spec_verify", "spec_verify8",
+                   "prefill_chunk")
 
 
 def small_workload(seed: int, lens, q_lens=None, hq=8, hkv=2, kv_dtype="bf16", num_blocks=None,
