@@ -213,3 +213,25 @@ def test_chunk_kernel_trace_events():
     dw.attention()
     assert pkv.kv_trace_prefill_kernel_ms() < 0          # not recorded while disabled
     assert pkv.kv_last_device_status() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,qlens", [(32, 4, [8, 9, 16]), (16, 8, [64, 3, 1]), (8, 2, [32, 32, 1])])
+def test_one_tile_chunks_never_leak_and_match(hq, hkv, qlens):
+    """Chunks whose rows x heads fit one 128-row tile (the second tile of the
+    CTA absent): parity with the oracle, and a NaN-poisoned cache gives the
+    same bits."""
+    lens = [80, 200, 3001]
+    wl = small_workload(1600 + hq, lens=lens, q_lens=qlens, hq=hq, hkv=hkv)
+    _, _, ref = expected_full(wl)
+    _, clean = _run(wl)
+    assert max_abs(clean, ref) <= TOL["bf16"]
+    _, dirty = _run(small_workload(1600 + hq, lens=lens, q_lens=qlens, hq=hq, hkv=hkv), poison=True)
+    assert np.isfinite(dirty).all() and np.array_equal(clean, dirty)
+
+
+def test_one_tile_chunk_over_many_partitions():
+    wl = small_workload(1610, lens=[40000, 7000, 33], q_lens=[16, 10, 1], hq=64, hkv=8)
+    _, got = _run(wl)
+    cu = wl.cu_q_lens
+    for s in range(3):
+        assert max_abs(got[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s)) <= TOL["bf16"], s
