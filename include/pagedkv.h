@@ -277,7 +277,16 @@ PAGEDKV_API kv_status reshape_and_cache(const void *k, const void *v, void *k_ca
  *  context_lens   device int32 [num_seqs], 1 <= len <= max_blocks_per_seq*16
  *  scale          softmax scale (1/sqrt(128) for the standard head)
  *  dtype          cache element type; for KV_FP8_E4M3 k_scale/v_scale are the
- *                 device fp32 [num_kv_heads] dequantisation scales
+ *                 device fp32 [num_kv_heads] dequantisation scales, one per KV
+ *                 head and separate for K and V: query head h reads KV head
+ *                 g = h / (num_q_heads / num_kv_heads), its keys are e4m3 x
+ *                 k_scale[g] and its values e4m3 x v_scale[g].
+ *                 Query range with KV_FP8_E4M3: the kernels multiply in f16, so
+ *                 each bf16 query component is rounded to f16 once -- exact for
+ *                 2^-14 <= |q| < 65,520; smaller magnitudes keep fewer bits
+ *                 (f16 subnormals; zero at or below 2^-25), and |q| >= 65,520 becomes
+ *                 infinite (the output is then NaN).  The bf16 cache has no such
+ *                 limit: Q stays bf16.
  *  num_splits     maximum partitions per sequence; partition length is
  *                 ceil(max_blocks_per_seq / num_splits) blocks.  0 = choose.
  *  workspace      device scratch of at least paged_attention_workspace_size()
@@ -338,7 +347,8 @@ PAGEDKV_API kv_status paged_attention_decode_static_scratch(
  * with the whole batch in the decode kernel, whose CTA then covers all rows of
  * a sequence so each K/V tile is read once.  With an fp8 cache the chunks run
  * on the tensor cores as well: each e4m3 K/V tile is widened exactly to f16
- * operands, Q is rounded to f16 once, and the products accumulate in fp32.
+ * operands, Q is rounded to f16 once (the query range of the decode call above
+ * applies), and the products accumulate in fp32.
  * A chunk's keys are cut into equal partitions of at most 16,384 keys, merged
  * with the same log-sum-exp reduction; the library picks their number from the
  * batch shape (num_splits applies to the decode rows), so a row's last bits
