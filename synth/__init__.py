@@ -13,14 +13,17 @@ numbers.  Two kinds of randomness are used.
   "Mix13" 64-bit finaliser.  Element ``n`` of stream ``key`` is
   ``mix13(key + n * GAMMA)``.
 
-The 64-bit word is turned into an approximately standard-normal value with an
-exact Irwin-Hall(4) construction: the four 16-bit lanes are summed (an exact
-integer), centred, converted to fp32 (exact, |x| < 2^18) and multiplied once by
-the fp32 constant sqrt(3)/65536 (one IEEE multiply: identical on every IEEE
-machine), then rounded to bf16 with round-to-nearest-even.  The result has
-mean 0, variance 1 and support [-3.4641, 3.4641].  All of this is integer
-arithmetic in torch int64 tensors (two's-complement wrap-around) plus one fp32
-multiply, so CPU and GPU produce bit-identical tensors.
+Element ``n`` of a tensor's stream takes the three words of counters 3n, 3n+1
+and 3n+2 and is the classic sum-of-twelve-uniforms approximation of a standard
+normal value: the twelve 16-bit lanes of the three words are summed (an exact
+integer in [0, 12 x 65535]), centred at 6 x 65535 and scaled by 2^-16 -- the
+variance of twelve uniform 16-bit lanes is (65536^2 - 1) / 65536^2 x 65536^2,
+so the result has mean 0 and variance 1 to within 2^-32 -- then rounded to
+bf16 with round-to-nearest-even.  The centred sum is below 2^19 in magnitude,
+so its conversion to fp32 and the power-of-two scaling are exact: only the
+final bf16 rounding rounds.  The support is [-5.99991, 5.99991].  All of this
+is integer arithmetic in torch int64 tensors (two's-complement wrap-around)
+plus exact fp32 steps, so CPU and GPU produce bit-identical tensors.
 """
 from __future__ import annotations
 
@@ -31,7 +34,7 @@ import torch
 
 __all__ = [
     "MASK64", "GAMMA", "splitmix64_py", "stream_key", "mix13_t", "normal_bf16",
-    "IH4_SCALE_F32", "IH4_MAX_ABS",
+    "NORMAL_LANES", "NORMAL_CENTRE", "NORMAL_MAX_ABS",
 ]
 
 MASK64 = (1 << 64) - 1
@@ -39,10 +42,11 @@ GAMMA = 0x9E3779B97F4A7C15
 _M1 = 0xBF58476D1CE4E5B9
 _M2 = 0x94D049BB133111EB
 
-# fp32(sqrt(3) / 65536): one Irwin-Hall(4) unit of 16-bit lanes -> unit variance
-IH4_SCALE_F32 = np.float32(math.sqrt(3.0) / 65536.0)
+# twelve 16-bit lanes (three 64-bit words) per value
+NORMAL_LANES = 12
+NORMAL_CENTRE = NORMAL_LANES * 65535 // 2          # 393,210: the lanes' mean sum
 # largest magnitude the generator can produce (before bf16 rounding)
-IH4_MAX_ABS = float(np.float32(np.float32(131070.0) * IH4_SCALE_F32))
+NORMAL_MAX_ABS = NORMAL_CENTRE / 65536.0
 
 
 def _s64(u: int) -> int:
@@ -77,14 +81,15 @@ def mix13_t(x: torch.Tensor) -> torch.Tensor:
 
 
 def normal_bf16(key: int, counters: torch.Tensor) -> torch.Tensor:
-    """bf16 N(0,1)-like values for the given int64 counters of stream ``key``.
+    """bf16 values with mean 0 and variance 1 (sum of twelve uniform 16-bit lanes)
+    for the given int64 counters of stream ``key``.
 
     Works on any device; the output has the shape and device of ``counters``.
     """
-    dev = counters.device
-    x = counters.to(torch.int64) * _s64(GAMMA) + _s64(key)
-    h = mix13_t(x)
-    s = (h & 0xFFFF) + (_lsr(h, 16) & 0xFFFF) + (_lsr(h, 32) & 0xFFFF) + _lsr(h, 48)
-    c = torch.tensor(float(IH4_SCALE_F32), dtype=torch.float32, device=dev)
-    f = (s - 131070).to(torch.float32) * c
-    return f.to(torch.bfloat16)
+    c3 = counters.to(torch.int64) * 3
+    s = None
+    for j in range(NORMAL_LANES // 4):
+        h = mix13_t((c3 + j) * _s64(GAMMA) + _s64(key))
+        part = (h & 0xFFFF) + (_lsr(h, 16) & 0xFFFF) + (_lsr(h, 32) & 0xFFFF) + _lsr(h, 48)
+        s = part if s is None else s + part
+    return ((s - NORMAL_CENTRE).to(torch.float32) * (2.0 ** -16)).to(torch.bfloat16)

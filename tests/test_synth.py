@@ -5,7 +5,7 @@ import math
 import numpy as np
 import torch
 
-from synth import GAMMA, IH4_MAX_ABS, MASK64, mix13_t, normal_bf16, splitmix64_py, stream_key
+from synth import GAMMA, MASK64, NORMAL_MAX_ABS, mix13_t, normal_bf16, splitmix64_py, stream_key
 from synth.workloads import WORKLOADS, make_workload
 
 
@@ -28,11 +28,34 @@ def test_torch_mix_matches_python_bigints():
 
 def test_normal_moments_and_bound():
     key = stream_key(2630, 1)
-    x = normal_bf16(key, torch.arange(1 << 20)).float()
-    assert abs(x.mean().item()) < 0.01
-    assert abs(x.var().item() - 1.0) < 0.01
-    assert x.abs().max().item() <= IH4_MAX_ABS * (1 + 2 ** -8)
-    assert abs(IH4_MAX_ABS - 131070 * math.sqrt(3) / 65536) < 1e-6
+    x = normal_bf16(key, torch.arange(1 << 21)).float()
+    assert abs(x.mean().item()) < 0.005
+    assert abs(x.var().item() - 1.0) < 0.005
+    assert x.abs().max().item() <= NORMAL_MAX_ABS * (1 + 2 ** -8)
+    assert abs(NORMAL_MAX_ABS - 6 * 65535 / 65536) < 1e-12
+    # tails past 3.5 sigma exist (a standard normal puts 4.7e-4 there; the
+    # twelve-lane sum slightly less): about 800 of 2M
+    tail = (x.abs() > 3.5).float().mean().item()
+    assert 2e-4 < tail < 6e-4
+
+
+def test_normal_values_follow_their_definition():
+    """A few values recomputed from the definition with Python integers: three
+    SplitMix64 words, the sum of their twelve 16-bit lanes, centred, times 2^-16,
+    rounded to bf16 (round to nearest even)."""
+    import struct
+    key = stream_key(77, 3)
+    ctr = [0, 1, 2, 12345, (1 << 40) + 17]
+    got = normal_bf16(key, torch.tensor(ctr)).view(torch.int16).numpy().astype(np.uint16)
+    for c, g in zip(ctr, got):
+        s = 0
+        for j in range(3):
+            w = splitmix64_py((key + (3 * c + j) * GAMMA) & MASK64)
+            s += sum((w >> (16 * i)) & 0xFFFF for i in range(4))
+        f = (s - 6 * 65535) / 65536.0                      # exact in fp64 and in fp32
+        u = struct.unpack("<I", struct.pack("<f", f))[0]
+        rne = (u + 0x7FFF + ((u >> 16) & 1)) >> 16         # bf16, round to nearest even
+        assert int(g) == rne, (c, hex(int(g)), hex(rne))
 
 
 def test_counter_based_values_are_position_independent():
