@@ -278,6 +278,13 @@ class OracleSample:
         nblk = int(sum(-(-int(L) // 16) for L in sub.context_lens))
         sub.num_blocks = nblk + (m if sub.cow_block >= 0 else 0)
         sub.free_order = np.arange(sub.num_blocks, dtype=np.int32)
+        if sub.kv_dtype == "fp8":
+            # the workload's own scales when the GPU arm already scanned them; the
+            # reference arm scans the sample's values on the host cores
+            if wl._fp8_scales is not None:
+                sub._fp8_scales = wl._fp8_scales
+            else:
+                sub.fp8_scales(device="cpu")
         self.tb = omodel.build_tables(sub)
         self.kc, self.vc = omodel.build_cache(sub, self.tb)
         self.q = sub.q_values().contiguous().view(torch.int16).numpy().view(np.uint16)
