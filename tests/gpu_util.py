@@ -3,7 +3,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 from oracle import model as omodel
 
 

@@ -9,7 +9,6 @@ import torch
 
 import oracle
 import paged_kv_cache_263_gb300 as pkv
-from oracle import model as omodel
 from paged_kv_cache_263_gb300.workload import DeviceWorkload
 from synth.workloads import make_workload, small_workload
 from tests.gpu_util import TOL, bits, cache_bytes, expected_full, max_abs, require_gpu

@@ -4,7 +4,6 @@ of each sample into a shared block gives it its own copy ("M.65 Inference
 serving", block management (g): initially share the prefix blocks, copy the
 affected block when generations diverge; "Waste, and three ways to reclaim it",
 "Copy on write")."""
-import numpy as np
 import pytest
 
 from oracle import model as omodel

@@ -1,6 +1,5 @@
 """The seeded input generator: bit-exact to its published definition, and the
 workload recipes have the stated shapes."""
-import math
 
 import numpy as np
 import torch
