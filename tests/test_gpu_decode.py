@@ -9,9 +9,10 @@ import torch
 
 import oracle
 import paged_kv_cache_263_gb300 as pkv
+from oracle import model as omodel
 from paged_kv_cache_263_gb300.workload import DeviceWorkload
 from synth.workloads import make_workload, small_workload
-from tests.gpu_util import TOL, bits, cache_bytes, expected_full, max_abs, require_gpu
+from tests.gpu_util import TOL, bits, cache_bytes, check_close, expected_full, max_abs, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -145,3 +146,38 @@ def test_copy_on_write_device_copy():
     assert np.array_equal(cache_bytes(dw.k_cache), caches[0])
     assert np.array_equal(cache_bytes(dw.v_cache), caches[1])
     assert max_abs(dw.out.cpu().numpy(), ref) <= TOL["bf16"]
+
+
+def test_empty_batches_launch_nothing_and_succeed():
+    """Zero tokens to write, zero sequences to decode, a mixed batch with no query
+    rows and one whose sequences contribute none: each call returns success, the
+    cache is untouched and no device flag is raised."""
+    dev = "cuda"
+    kc = torch.full((4, 2, 16, 128), 0.5, dtype=torch.bfloat16, device=dev)
+    vc = kc.clone()
+    before = kc.clone()
+    e = torch.empty(0, 2, 128, dtype=torch.bfloat16, device=dev)
+    pkv.reshape_and_cache(e, e, kc, vc, torch.empty(0, dtype=torch.int64, device=dev))
+    out = torch.empty(0, 8, 128, dtype=torch.float32, device=dev)
+    q = torch.empty(0, 8, 128, dtype=torch.bfloat16, device=dev)
+    bt = torch.zeros(0, 4, dtype=torch.int32, device=dev)
+    cl = torch.zeros(0, dtype=torch.int32, device=dev)
+    pkv.paged_attention_decode(out, q, kc, vc, bt, cl)
+    pkv.paged_attention_chunked_prefill(out, q, torch.zeros(1, dtype=torch.int32, device=dev), cl, 1, kc, vc, bt)
+    # two sequences with context but no query rows this step
+    bt2 = torch.tensor([[0, 1, -1, -1], [2, -1, -1, -1]], dtype=torch.int32, device=dev)
+    cl2 = torch.tensor([20, 9], dtype=torch.int32, device=dev)
+    cu2 = torch.zeros(3, dtype=torch.int32, device=dev)
+    pkv.paged_attention_chunked_prefill(out, q, cu2, cl2, 1, kc, vc, bt2)
+    torch.cuda.synchronize()
+    assert pkv.kv_last_device_status() == 0
+    assert torch.equal(kc, before) and torch.equal(vc, before)
+
+
+def test_million_token_context_over_many_partitions():
+    """A 2^20-token context (65,536 blocks): 256 split-KV partitions merged in one
+    log-sum-exp pass, next to a short sequence; both against the oracle."""
+    wl = small_workload(1700, lens=[1 << 20, 777], hq=8, hkv=2)
+    dw, got = _run(wl)
+    for s in range(2):
+        check_close(got[s:s + 1], omodel.expected_rows(wl, s), "bf16", s)

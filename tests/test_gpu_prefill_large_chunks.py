@@ -11,7 +11,7 @@ import paged_kv_cache_263_gb300 as pkv
 from oracle import model as omodel
 from paged_kv_cache_263_gb300.workload import DeviceWorkload
 from synth.workloads import small_workload
-from tests.gpu_util import TOL, expected_full, max_abs, require_gpu
+from tests.gpu_util import TOL, check_close, expected_full, max_abs, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -50,8 +50,7 @@ def test_chunk_over_several_partitions():
     got = _run(wl)
     cu = wl.cu_q_lens
     for s in range(3):
-        err = max_abs(got[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s))
-        assert err <= TOL["bf16"], (s, err)
+        check_close(got[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s), "bf16", s)
 
 
 def test_tail_rows_never_leak():
