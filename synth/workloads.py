@@ -29,7 +29,11 @@ verifying a 4-token draft: 4 causal query rows per sequence) and
 8-token drafts) -- speculative decoding's verification pass ("M.65 Inference
 serving", speculative decoding: a draft of N = 4-8 tokens verified in one
 forward pass); ``mixed_prefill_small`` (the mixed batch scaled down for
-profiling).
+profiling); ``prefill_chunk`` (the mixed batch's chunk without its decode
+rows: the tensor-core kernel alone).
+
+fp8 workloads carry per-KV-head scales for K and for V (``fp8_scales``):
+amax / 448 over every value of that head and tensor in the workload.
 
 For every sequence the step's "new" tokens (the last ``q_len`` positions) are
 the ones appended by the cache write in the step; all earlier positions are
