@@ -16,7 +16,13 @@
 //    group; the two tiles of a pair share every K/V tile as well.  Both Q tiles
 //    land in shared memory with one 3-D TMA load each.
 //  * K/V tiles of 64 keys = 4 physical blocks, gathered through the block
-//    table by 2-D TMA loads (128-byte swizzle) into a 4-stage ring (warp 8).
+//    table by TMA loads (128-byte swizzle) into a 4-stage ring (warp 8): K as
+//    two 2-D boxes per block (each 64-dim half of the tile's keys contiguous, as
+//    the QK^T operand needs), V as one 3-D box per block holding both halves.
+//  * Chunks whose rows x heads fit one 128-row tile (speculative drafts) take a
+//    second layout: one query tile per CTA, tiles of 128 keys (N = 128 QK^T
+//    products, half the instructions per key for the single issuer), three
+//    stages, and two producer warps (K and V).
 //  * S[128x64] = Q K^T and O[128x128] += P V run as tcgen05.mma (K=16 steps),
 //    one issuing warp per query tile (warps 9 and 10).  S is double-buffered
 //    per tile in tensor memory, so QK^T of tile j+2 runs while the softmax
@@ -68,24 +74,47 @@ constexpr float RESCALE_LOG2 = 8.0f;
 // cache: e4m3 staging stages of (K 8 KiB, V 8 KiB)) | barriers.  P lives in
 // tensor memory.
 constexpr uint32_t SQ = 0, Q_TILE = 32768;
-constexpr uint32_t SKV = 65536, KV_STAGE_BYTES = 32768, V_OFF = 16384, KV_HALF = 8192;
+constexpr uint32_t KV_STAGE_BYTES = 32768, V_OFF = 16384, KV_HALF = 8192;   // the 64-key layout
 constexpr uint32_t F8_STAGE_BYTES = 16384, F8_V_OFF = 8192;
 // bf16 cache: warps 0-3 softmax of query tile 0, 4-7 softmax of query tile 1, 8 TMA
 // producer, 9 and 10 MMA issuers of query tile 0 and 1.  fp8 cache: in addition
 // warps 11-14 widen each e4m3 K/V tile to f16 operand tiles (the products then
 // run in kind::f16 with f16 operands: e4m3 -> f16 is exact, and Q is converted
 // to f16 once in shared memory).
-template <bool FP8>
+//
+// BIG (bf16 cache, chunks whose rows x heads fit one 128-row tile, such as the
+// drafts of speculative decoding): one query tile per CTA -- warps 0-3 softmax,
+// 4 producer of K, 5 issuer, 6 producer of V -- and tiles of 128 keys.  With one query tile the
+// tensor memory holds two S buffers of 128 columns next to O, so each QK^T
+// product is N = 128: half the product instructions per key, which is what a
+// CTA with a single issuer waits on.  Three stages of 64 KiB keep the same
+// bytes in flight as four of 32 KiB.
+template <bool FP8, bool BIG = false>
 struct Lay {
-    static constexpr int THREADS = FP8 ? 480 : 352;
-    static constexpr int KV_STAGES = FP8 ? 3 : 4;
+    static constexpr int BNK = BIG ? 128 : 64;               // keys per KV tile
+    static constexpr int NG = BIG ? 1 : 2;                   // query tiles per CTA
+    static constexpr int W_PROD = 4 * NG;                    // the TMA producer warp
+    static constexpr int W_MMA = W_PROD + 1;                 // the first MMA issuer warp
+    static constexpr int W_WIDEN = W_MMA + NG;               // fp8 cache: the first widening warp
+    // BIG: a second producer warp issues the V boxes; a CTA with one issuer is
+    // bound by how fast its loads leave, and two warps issue them faster than one
+    static constexpr int W_PROD2 = BIG ? W_WIDEN : -1;
+    static constexpr int THREADS = 32 * (W_WIDEN + (FP8 ? 4 : 0) + (BIG ? 1 : 0));
+    static constexpr int KV_STAGES = BIG ? 3 : (FP8 ? 3 : 4);
+    static constexpr uint32_t KV_HALF = BNK * 128;           // one 64-dim half of a K or V tile
+    static constexpr uint32_t V_OFF = 2 * KV_HALF;
+    static constexpr uint32_t KV_STAGE_BYTES = 4 * KV_HALF;  // K and V
     static constexpr int F8_STAGES = FP8 ? 3 : 0;
+    static constexpr uint32_t SKV = NG * 32768;               // K/V stages follow the Q tiles
     static constexpr uint32_t SF8 = SKV + KV_STAGES * KV_STAGE_BYTES;
     static constexpr uint32_t SBAR = SF8 + F8_STAGES * F8_STAGE_BYTES;
-    static constexpr int SMEM_BYTES = SBAR + 512;
+    // + 1 KiB: the dynamic shared memory is aligned to 1 KiB at run time
+    static constexpr int SMEM_BYTES = SBAR + 512 + 1024;
+    static constexpr uint32_t S_COLS = 2 * BNK;               // two S buffers per query tile
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+    static_assert(NG * (S_COLS + 128) <= 512, "tensor memory");
+    static_assert(!(FP8 && BIG), "the 128-key layout is for the bf16 cache");
 };
-static_assert(SKV >= 2 * 32768, "shared-memory layout overlaps");
 // barriers (room for the larger of the two layouts)
 enum {
     B_KVF = 0,                      // + stage: K and V operand tiles ready
@@ -110,6 +139,7 @@ constexpr uint32_t idesc(int n, bool b_mn_major)
            ((uint32_t)(BM >> 4) << 24);
 }
 constexpr uint32_t IDESC_S = idesc(BN, false);    // S[128 x 64] = Q K^T, K K-major
+constexpr uint32_t IDESC_S128 = idesc(128, false); // S[128 x 128] = Q K^T (128-key tiles)
 constexpr uint32_t IDESC_PV = idesc(D, true);     // O[128 x 128] += P V, V MN-major
 // the same with f16 A and B (fp8 cache widened to f16)
 constexpr uint32_t F16_OPS = (1u << 7) | (1u << 10);
@@ -127,6 +157,8 @@ struct PrefillParams {
     float *part_ml;      // [rows][Hq][max_splits][2]
     int max_blocks, num_seqs, hq, hkv, group, num_blocks, total_rows;
     int tiles_per_split, max_splits;
+    int item_tiles;      // query tiles per CTA: 2 (a pair), or 1 (the 128-key layout)
+    int tile_keys;       // keys per KV tile: 64, or 128 (the 128-key layout)
     float scale_log2;
     const float *k_scale;  // fp8 cache: [Hkv] (folded into the softmax scale)
     const float *v_scale;  // fp8 cache: [Hkv] (applied to O)
@@ -168,7 +200,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
             const int n = b - a, L = p.context_lens[s];
             if (n >= 2) {
                 if (a < 0 || b > p.total_rows || L < n || L > p.max_blocks * BS) flag(ST_BAD_LEN);
-                else tiles = ((n + tpt - 1) / tpt + 1) / 2;    // pairs of 128-row query tiles
+                else tiles = ((n + tpt - 1) / tpt + p.item_tiles - 1) / p.item_tiles;   // CTAs along x
             } else if (n < 0) {
                 flag(ST_BAD_LEN);
             }
@@ -204,16 +236,20 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
 
 // (the fp8 variant declares 512 threads so that registers stay <= 128, which 15
 // warps need on an SM partition holding four of them)
-template <bool FP8>
-__global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
+template <bool FP8, bool BIG>
+__global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p)
 {
-    constexpr int KV_STAGES = Lay<FP8>::KV_STAGES, F8_STAGES = Lay<FP8>::F8_STAGES;
+    using LY = Lay<FP8, BIG>;
+    constexpr int KV_STAGES = LY::KV_STAGES, F8_STAGES = LY::F8_STAGES;
+    constexpr int BN = LY::BNK;                                   // keys per KV tile
+    constexpr uint32_t SKV = LY::SKV, KV_STAGE_BYTES = LY::KV_STAGE_BYTES, V_OFF = LY::V_OFF,
+                       KV_HALF = LY::KV_HALF;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = smem_raw;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay<FP8>::SBAR);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + LY::SBAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     auto bar = [&](int i) -> uint32_t { return smem_u32(bars + i); };
@@ -232,12 +268,13 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
         if (p.tile_off[mid] <= x) lo = mid;
         else hi = mid;
     }
-    const int s = lo, pair = x - p.tile_off[s];
+    const int s = lo, item = x - p.tile_off[s];
     const int row0 = p.cu_q_lens[s], n = p.cu_q_lens[s + 1] - row0, L = p.context_lens[s];
     const int G = p.group, tpt = BM / G;
     const int tiles = (n + tpt - 1) / tpt;
-    const bool has1 = 2 * pair + 1 < tiles;      // the pair's second query tile exists
-    const int last = has1 ? 2 * pair + 1 : 2 * pair;
+    const int t0q = BIG ? item : 2 * item;       // the CTA's first query tile
+    const bool has1 = !BIG && t0q + 1 < tiles;   // the pair's second query tile exists
+    const int last = has1 ? t0q + 1 : t0q;
     const int kmax = L - n + min(n, (last + 1) * tpt);   // keys visible to the pair's last row
     const int KT = (kmax + BN - 1) / BN;
     // the pair's keys in nsplit partitions of (nearly) equal length, at most
@@ -290,17 +327,18 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
     // TMEM columns per query tile gi: two S buffers of 64 fp32 columns at
     // 128 gi + 64 b (P overwrites the first 32 of a buffer with bf16 pairs once its
     // S has been read), O at 256 + 128 gi
-    auto tS = [&](int gi, int b) -> uint32_t { return tmem + gi * 128 + b * BN; };
-    auto tO = [&](int gi) -> uint32_t { return tmem + 256 + gi * D; };
+    auto tS = [&](int gi, int b) -> uint32_t { return tmem + gi * LY::S_COLS + b * BN; };
+    auto tO = [&](int gi) -> uint32_t { return tmem + LY::NG * LY::S_COLS + gi * D; };
 
-    if (warp == 8) {
+    if (warp == LY::W_PROD || warp == LY::W_PROD2) {
+        const int role = warp == LY::W_PROD ? 0 : 1;   // 0: K boxes + expect; 1 (BIG): V boxes
         // ======================= TMA producer
         const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks;
         const int nblk = (L + BS - 1) / BS;
-        if (lane == 0) {
+        if (lane == 0 && role == 0) {
             mbar_arrive_expect_tx(bar(B_Q), (has1 ? 4 : 2) * 16384);
             for (int gi = 0; gi < (has1 ? 2 : 1); ++gi) {
-                const int zq = row0 + (2 * pair + gi) * tpt;
+                const int zq = row0 + (t0q + gi) * tpt;
                 tma_load_3d(sbase + SQ + gi * Q_TILE, &qmap, 0, g * G, zq, bar(B_Q));
                 tma_load_3d(sbase + SQ + gi * Q_TILE + 16384, &qmap, 64, g * G, zq, bar(B_Q));
             }
@@ -334,7 +372,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                 __syncwarp();
                 if (valid) {
                     const int y = (id * p.hkv + g) * BS;
-                    const uint32_t dst = sbase + Lay<FP8>::SF8 + st * F8_STAGE_BYTES + kv * F8_V_OFF + blk8 * 2048;
+                    const uint32_t dst = sbase + LY::SF8 + st * F8_STAGE_BYTES + kv * F8_V_OFF + blk8 * 2048;
                     tma_load_2d(dst, kv ? &vmap : &kmap, 0, y, bar(B_F8F + st));
                 }
                 issued = jj + 1;
@@ -344,14 +382,22 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                     (void)mbar_wait_bounded(bar(B_F8F + jj % F8_STAGES), (jj / F8_STAGES) & 1);
             }
         }
-        // bf16 cache: lanes 0-15 each load one 2 KiB box per tile, lane = 4 x block
-        // of the tile + operand (K dims 0-63, K 64-127, V 0-63, V 64-127), so the
-        // tile's 16 loads leave in one instruction; each lane's block id for the
-        // next tile is read while the producer waits for the stage to free up
-        const int blk = (lane >> 2) & 3, opnd = lane & 3;
+        // bf16 cache: one lane per box, so a tile's loads leave in one instruction.
+        // K: two 2 KiB boxes per block (dims 0-63 and 64-127; the QK^T operand needs
+        // each half of all the tile's keys contiguous), lanes 0 .. 2 NB - 1, lane =
+        // 2 x block + half.  V: one 4 KiB box per block holding both halves (a 3-D
+        // tensor map), lanes 2 NB .. 3 NB - 1.  NB = blocks per tile (4 or 8).  Each
+        // lane's block id for the next tile is read while the producer waits for
+        // the stage to free up.
+        constexpr int NB = BN / BS, K_LANES = 2 * NB;
+        const int BOX_LANES = BIG ? (role == 0 ? K_LANES : NB) : 3 * NB;
+        const bool is_v = BIG ? role == 1 : lane >= K_LANES;
+        const int blk = BIG ? (role == 1 ? lane & (NB - 1) : (lane >> 1) & (NB - 1))
+                            : (is_v ? (lane - K_LANES) & (NB - 1) : (lane >> 1) & (NB - 1));
+        const int opnd = lane & 1;
         auto block_id = [&](int jj) -> int32_t {
             const int b = (j0 + jj) * (BN / BS) + blk;
-            return (!FP8 && lane < 16 && jj < T && b < nblk) ? __ldg(bt + b) : -1;
+            return (!FP8 && lane < BOX_LANES && jj < T && b < nblk) ? __ldg(bt + b) : -1;
         };
         int32_t next_id = block_id(0);
         for (int jj = 0; jj < T && !FP8; ++jj) {
@@ -360,24 +406,27 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
             next_id = block_id(jj + 1);
             if (jj >= KV_STAGES && !wait_w(bar(B_KVE + st), ((jj - KV_STAGES) / KV_STAGES) & 1)) break;
             const int j = j0 + jj;
-            const bool in = lane < 16 && j * (BN / BS) + blk < nblk;
+            const bool in = lane < BOX_LANES && j * (BN / BS) + blk < nblk;
             const bool valid = in && id >= 0 && id < p.num_blocks;
-            if (in && !valid && opnd == 0) flag(ST_BAD_BLOCK);
+            if (in && !valid && is_v) flag(ST_BAD_BLOCK);
             const unsigned vm = __ballot_sync(0xffffffffu, valid);
-            if (lane == 0) {
+            if (lane == 0 && role == 0) {
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar(B_KVF + st), __popc(vm) * 2048);
+                constexpr unsigned K_MASK = (1u << K_LANES) - 1u;
+                // BIG: the V warp loads one 4 KiB box per valid block (2 K lanes each)
+                const unsigned vbytes = BIG ? __popc(vm & K_MASK & 0x55555555u) * 4096 : __popc(vm & ~K_MASK) * 4096;
+                mbar_arrive_expect_tx(bar(B_KVF + st), __popc(vm & K_MASK) * 2048 + vbytes);
             }
             __syncwarp();
             if (valid) {
                 const int y = (id * p.hkv + g) * BS;
-                const uint32_t dst = sbase + SKV + st * KV_STAGE_BYTES + (opnd >> 1) * V_OFF + (opnd & 1) * KV_HALF +
-                                     blk * 2048;
-                tma_load_2d(dst, (opnd >> 1) ? &vmap : &kmap, (opnd & 1) * 64, y, bar(B_KVF + st));
+                const uint32_t stg = sbase + SKV + st * KV_STAGE_BYTES;
+                if (is_v) tma_load_3d(stg + V_OFF + blk * 4096, &vmap, 0, y, 0, bar(B_KVF + st));
+                else tma_load_2d(stg + opnd * KV_HALF + blk * 2048, &kmap, opnd * 64, y, bar(B_KVF + st));
             }
             issued = jj + 1;
             const int first = L - j * BN;            // first row of the tile at or past L
-            if (first < BN) {
+            if (first < BN && role == 0) {
                 // keys >= L: their V rows may hold anything (never written, or not
                 // loaded); P is 0 there but 0 * NaN is NaN, so zero them once the
                 // tile has landed, before any PV product reads it
@@ -385,7 +434,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                 const uint32_t vb = sbase + SKV + st * KV_STAGE_BYTES + V_OFF;
                 for (int c = lane; c < (BN - first) * 16; c += 32) {
                     const int r = first + (c >> 4), h = (c >> 3) & 1, ch = c & 7;
-                    st_shared_v4(vb + h * KV_HALF + r * 128 + ch * 16, 0u, 0u, 0u, 0u);
+                    st_shared_v4(vb + (r >> 4) * 4096 + h * 2048 + (r & 15) * 128 + ch * 16, 0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -397,16 +446,19 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
             for (int jj = max(0, issued - KV_STAGES); jj < issued; ++jj)
                 (void)mbar_wait_bounded(bar(B_KVF + jj % KV_STAGES), (jj / KV_STAGES) & 1);
         }
-    } else if (warp == 9 || warp == 10) {
-        // ======================= MMA issuers: warp 9 for query tile 0, warp 10 for tile 1
-        const int gi = warp - 9;
+    } else if (warp >= LY::W_MMA && warp < LY::W_MMA + LY::NG) {
+        // ======================= MMA issuers: one warp per query tile
+        const int gi = warp - LY::W_MMA;
         if (gi == 0 || has1) {
             // shared-memory descriptors of stage 0; other stages and K steps are
             // constant byte offsets added to the start-address field (in 16-byte
             // units; shared memory is < 256 KiB, so the 14-bit field never carries)
             const uint64_t qdesc = sdesc_sw128(sbase + SQ + gi * Q_TILE, 16, 1024);
             const uint64_t kdesc0 = sdesc_sw128(sbase + SKV, 16, 1024);
-            const uint64_t vdesc0 = sdesc_sw128(sbase + SKV + V_OFF, KV_HALF, 1024);
+            // V: bf16 cache [block][64-dim half][16 keys] (one 3-D box per block); fp8
+            // cache [half][block][16 keys] (written by the widening warps)
+            constexpr uint32_t V_LBO = FP8 ? KV_HALF : 2048, V_KSTEP = FP8 ? 2048 : 4096;
+            const uint64_t vdesc0 = sdesc_sw128(sbase + SKV + V_OFF, V_LBO, 1024);
             const uint32_t to = tO(gi);
             // S = Q K^T for KV tile jj into S buffer jj % 2: A = Q, B = K (K-major)
             auto issue_s = [&](int jj) {
@@ -418,7 +470,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                     for (int kk = 0; kk < 8; ++kk)   // D = 128 in steps of 16: 4 per 64-wide half
                         umma_f16(ts, qdesc + (uint64_t)((((kk >> 2) * 16384) + (kk & 3) * 32) >> 4),
                                  kd + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4),
-                                 FP8 ? IDESC_S16 : IDESC_S, kk > 0);
+                                 FP8 ? IDESC_S16 : (BIG ? IDESC_S128 : IDESC_S), kk > 0);
                     umma_commit(bar(B_S + 2 * gi + (jj & 1)));
                 }
                 __syncwarp();
@@ -430,8 +482,8 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                     const uint64_t vd = vdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
                     const uint32_t ts = tS(gi, jj & 1);
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)   // 64 keys in steps of 16
-                        umma_f16_ts(to, ts + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), FP8 ? IDESC_PV16 : IDESC_PV,
+                    for (int kk = 0; kk < BN / 16; ++kk)   // the tile's keys in steps of 16
+                        umma_f16_ts(to, ts + kk * 8, vd + (uint64_t)((kk * V_KSTEP) >> 4), FP8 ? IDESC_PV16 : IDESC_PV,
                                     (jj > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(bar(B_PVD + gi));
                     // the stage is released once both issuers' MMAs reading it are done
@@ -468,7 +520,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
             __syncwarp();
             (void)mbar_wait_bounded(bar(B_DRAIN + gi), 0);
         }
-    } else if (warp >= 11) {
+    } else if (warp >= LY::W_WIDEN) {
         // ======================= fp8 cache: widen each e4m3 K/V tile to f16 operand
         // tiles (exact), in the operand stages' 128-byte-swizzled layout; keys at
         // or past L and blocks outside the pool become zeros
@@ -478,7 +530,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
             // lanes of a warp take consecutive keys, so the 8 lanes of each
             // quarter-warp access 8 distinct 16-byte bank groups (the 128-byte
             // swizzle XORs the chunk with the key's low 3 bits)
-            const int ct = threadIdx.x - 11 * 32;      // 0..127
+            const int ct = threadIdx.x - LY::W_WIDEN * 32;      // 0..127
             const int row = ct & (BN - 1), c0 = ct >> 6;
             const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks;
             // the row's key of tile jj lies inside the context and its block in the
@@ -496,7 +548,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                 next_ok = row_ok(jj + 1);
                 if (!wait_w(bar(B_F8F + s8), (jj / F8_STAGES) & 1)) break;
                 if (jj >= KV_STAGES && !wait_w(bar(B_KVE + st), ((jj - KV_STAGES) / KV_STAGES) & 1)) break;
-                const uint32_t src = sbase + Lay<FP8>::SF8 + s8 * F8_STAGE_BYTES + row * 128;
+                const uint32_t src = sbase + LY::SF8 + s8 * F8_STAGE_BYTES + row * 128;
                 const uint32_t dst = sbase + SKV + st * KV_STAGE_BYTES + row * 128;
                 // all eight 16-byte loads first, then the conversions and stores
                 uint32_t w[2][4][4];
@@ -536,7 +588,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
         const int gi = warp >> 2;                  // which query tile of the pair
         if (gi == 0 || has1) {
             const int r = threadIdx.x - gi * 128;  // row of the tile, 0..127
-            const int i0 = (2 * pair + gi) * tpt, i1 = min(n, i0 + tpt);
+            const int i0 = (t0q + gi) * tpt, i1 = min(n, i0 + tpt);
             const int i = i0 + r / G;
             const int head = g * G + r % G;
             const bool row_valid = i < i1;
@@ -574,7 +626,9 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                 if (!wait_w(bar(B_S + 2 * gi + (jj & 1)), (jj >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 float sv[BN];
-                tmem_ld64(tS(gi, jj & 1) + lane_base, sv);
+#pragma unroll
+                for (int h = 0; h < BN / 64; ++h)
+                    tmem_ld64(tS(gi, jj & 1) + lane_base + 64 * h, *reinterpret_cast<float(*)[64]>(sv + 64 * h));
                 // raw scores; the scale (> 0) is applied inside the exponent's FFMA,
                 // so the max is taken on the raw values
                 if (t0 + BN - 1 > pos_min) {             // diagonal tile: causal mask
@@ -636,7 +690,9 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
                 }
                 // P in bf16 pairs over the first 32 columns of the S buffer (the A
                 // operand of PV)
-                tmem_st32u(tS(gi, jj & 1) + lane_base, pw);
+#pragma unroll
+                for (int h = 0; h < BN / 64; ++h)
+                    tmem_st32u(tS(gi, jj & 1) + lane_base + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(pw + 32 * h));
                 tmem_wait_st();
                 tc_fence_before();
                 // one P barrier per S buffer: a warp reaches buffer b's next phase only
@@ -673,7 +729,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8>::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc(tmem, 512);   // (both layouts allocate all 512 columns)
 }
 
 // Log-sum-exp merge of prefill partitions: one warp per (query row, head).
@@ -695,11 +751,11 @@ __global__ void __launch_bounds__(128) prefill_reduce_kernel(const PrefillParams
     if (n < 2 || L < n || L > p.max_blocks * BS) return;
     const int tpt = BM / p.group;
     const int i = row - row0, mt = i / tpt;
-    // the CTA that computed this row covered the key range of its tile pair
+    // the CTA that computed this row covered the key range of its query tiles
     const int tiles = (n + tpt - 1) / tpt;
-    const int last = min(tiles - 1, (mt / 2) * 2 + 1);
+    const int last = min(tiles - 1, (mt / p.item_tiles) * p.item_tiles + p.item_tiles - 1);
     const int i1 = min(n, (last + 1) * tpt);
-    const int KT = (L - n + i1 + BN - 1) / BN;
+    const int KT = (L - n + i1 + p.tile_keys - 1) / p.tile_keys;
     const int ns = (KT + p.tiles_per_split - 1) / p.tiles_per_split;
     if (ns <= 1) return;
     const size_t base = ((size_t)row * p.hq + h) * p.max_splits;
@@ -707,8 +763,8 @@ __global__ void __launch_bounds__(128) prefill_reduce_kernel(const PrefillParams
         lse_merge_warp(p.part_ml + base * 2, p.part_o + base * D, ns, lane);
 }
 
-constexpr int TILES_PER_SPLIT = 16384 / BN;   // 16,384 keys per partition at most
-constexpr int MIN_TILES_PER_SPLIT = 1024 / BN; // 1,024 keys at least
+constexpr int MAX_SPLIT_KEYS = 16384;           // keys per partition at most
+constexpr int MIN_SPLIT_KEYS = 1024;            // and at least
 constexpr int64_t NUM_SMS = 152;               // a chunk CTA holds a whole SM: waves of 152
 constexpr double CTA_FIXED_TILES = 4.0;        // a CTA's Q load, set-up and epilogue, in tile-times
 // HBM bytes moved while a CTA works through one 64-key tile (~0.86 us at ~6.5 TB/s)
@@ -749,14 +805,20 @@ namespace {
 // ceil(ceil(max_q_len / tpt) / 2) pairs of query tiles.  Equal partitions alone
 // can leave a last wave almost empty (768 CTAs = 5.05 waves), which the model
 // avoids by taking one more partition.  Returns the partition length in tiles.
-int plan_tiles_per_split(int32_t total_q, int32_t max_q_len, int32_t hq, int32_t hkv, int max_kv_tiles)
+int plan_tiles_per_split(int32_t total_q, int32_t max_q_len, int32_t hq, int32_t hkv, int max_kv_tiles,
+                         bool big)
 {
     const int G = std::max(1, hq / std::max(1, hkv)), tpt = std::max(1, BM / G);
     const int64_t chunks = std::max<int64_t>(1, (int64_t)total_q / std::max(1, max_q_len));
-    const int64_t pairs = chunks * (((int64_t)max_q_len + tpt - 1) / tpt + 1) / 2;
-    const int64_t problems = std::max<int64_t>(1, pairs * std::max(1, hkv));
+    const int item = big ? 1 : 2;                       // query tiles per CTA
+    const int64_t items = chunks * ((((int64_t)max_q_len + tpt - 1) / tpt + item - 1) / item);
+    const int64_t problems = std::max<int64_t>(1, items * std::max(1, hkv));
     const int W = std::max(1, max_kv_tiles);
-    const double merge_per_split = (double)total_q * hq * (D + 2) * 4.0 * 2.0 / BYTES_PER_TILE_TIME;
+    const int tile_keys = big ? 128 : 64;              // W and the result are in tiles of tile_keys
+    const int TILES_PER_SPLIT = MAX_SPLIT_KEYS / tile_keys, MIN_TILES_PER_SPLIT = MIN_SPLIT_KEYS / tile_keys;
+    const double CTA_FIXED = CTA_FIXED_TILES * 64.0 / tile_keys;
+    const double merge_per_split =
+        (double)total_q * hq * (D + 2) * 4.0 * 2.0 / (BYTES_PER_TILE_TIME * tile_keys / 64.0);
     const int s_lo = (W + TILES_PER_SPLIT - 1) / TILES_PER_SPLIT;
     // (the partition count is the grid's z extent: at most 65,535)
     const int s_hi = std::max(s_lo, std::min(65535, (W + MIN_TILES_PER_SPLIT - 1) / MIN_TILES_PER_SPLIT));
@@ -764,7 +826,7 @@ int plan_tiles_per_split(int32_t total_q, int32_t max_q_len, int32_t hq, int32_t
         const int len = (W + s - 1) / s;
         const int splits = (W + len - 1) / len;        // what the kernel makes of len
         const int64_t waves = (problems * splits + NUM_SMS - 1) / NUM_SMS;
-        return (double)waves * (len + CTA_FIXED_TILES) + (splits > 1 ? splits * merge_per_split : 0.0);
+        return (double)waves * (len + CTA_FIXED) + (splits > 1 ? splits * merge_per_split : 0.0);
     };
     double best = cost(s_lo);
     for (int s = s_lo + 1; s <= s_hi; ++s) best = std::min(best, cost(s));
@@ -779,13 +841,14 @@ int plan_tiles_per_split(int32_t total_q, int32_t max_q_len, int32_t hq, int32_t
 }
 
 Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq, int32_t hkv, int32_t max_blocks,
-               int32_t num_splits)
+               int32_t num_splits, bool big)
 {
     Plan pl{};
     auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
     pl.decode_bytes = up(pkv_decode::workspace_bytes(num_seqs, hq, max_blocks, num_splits));
-    const int max_kv_tiles = (max_blocks * BS + BN - 1) / BN;
-    pl.tiles_per_split = plan_tiles_per_split(total_q, max_q_len, hq, hkv, max_kv_tiles);
+    const int tile_keys = big ? 128 : 64;
+    const int max_kv_tiles = (max_blocks * BS + tile_keys - 1) / tile_keys;
+    pl.tiles_per_split = plan_tiles_per_split(total_q, max_q_len, hq, hkv, max_kv_tiles, big);
     pl.max_splits = max_q_len >= 2 ? (max_kv_tiles + pl.tiles_per_split - 1) / pl.tiles_per_split : 0;
     size_t off = pl.decode_bytes;
     pl.part_o_off = off;
@@ -812,6 +875,13 @@ constexpr int64_t MULTI_MAX_COLS = PKV_MULTI_MAX_COLS;
 bool use_multi(int32_t max_q_len, int32_t hq, int32_t hkv)
 {
     return max_q_len >= 2 && hkv >= 1 && (int64_t)max_q_len * (hq / hkv) <= MULTI_MAX_COLS;
+}
+
+// The 128-key layout (one query tile per CTA) when every chunk's rows x heads
+// fit one 128-row tile; bf16 cache.
+bool use_big(kv_dtype dt, int32_t max_q_len, int32_t hq, int32_t hkv)
+{
+    return dt == KV_BF16 && hkv >= 1 && (int64_t)max_q_len * (hq / hkv) <= BM;
 }
 }  // namespace
 
@@ -887,8 +957,12 @@ size_t paged_attention_chunked_prefill_workspace_size(int32_t num_seqs, int32_t 
     if (num_seqs < 1 || total_q_tokens < 1 || max_q_len < 1 || num_q_heads < 1 || max_blocks_per_seq < 1 ||
         num_kv_heads < 1)
         return 0;
+    // (the size query has no cache type: room for the plan of either layout)
     size_t t = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq,
-                         num_splits).total;
+                         num_splits, false).total;
+    if (use_big(KV_BF16, max_q_len, num_q_heads, num_kv_heads))
+        t = std::max(t, make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads,
+                                  max_blocks_per_seq, num_splits, true).total);
     if (use_multi(max_q_len, num_q_heads, num_kv_heads))
         t = std::max(t, pkv_decode::workspace_bytes_multi(total_q_tokens, num_seqs, num_q_heads, max_blocks_per_seq,
                                                           num_splits));
@@ -908,8 +982,9 @@ int32_t paged_attention_launch_count(int32_t num_seqs, int32_t total_q_tokens, i
     const int32_t decode = 1 + (s > 1 ? 1 : 0);
     if (max_q_len < 2 || use_multi(max_q_len, num_q_heads, num_kv_heads)) return decode;
     // the decode rows, the tile-count prefix, the chunk tiles and their merge
+    // (the plan of a bf16 cache)
     const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq,
-                              num_splits);
+                              num_splits, use_big(KV_BF16, max_q_len, num_q_heads, num_kv_heads));
     return decode + 2 + (pl.max_splits > 1 ? 1 : 0);
 }
 
@@ -943,8 +1018,9 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
                                k_scale, v_scale, num_splits, workspace, workspace_bytes, st, max_q_len, true);
     }
     if (dtype == KV_FP8_E4M3 && (!k_scale || !v_scale)) return KV_ERR_INVALID;
+    const bool big = use_big(dtype, max_q_len, num_q_heads, num_kv_heads);
     const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq,
-                              num_splits);
+                              num_splits, big);
     if (pl.total && (!workspace || workspace_bytes < pl.total || !pkv_host::aligned(workspace, 256)))
         return KV_ERR_INVALID;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -992,6 +1068,8 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     p.scale_log2 = scale * LOG2E;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.item_tiles = big ? 1 : 2;
+    p.tile_keys = big ? 128 : 64;
     CUtensorMap qm, km, vm;
     const int tpt = BM / G;
     if (!pkv_host::encode_tmap_3d(&qm, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, num_q_heads, total_q_tokens,
@@ -1000,9 +1078,18 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
         return KV_ERR_CUDA;
     if (!pkv_decode::make_maps(k_cache, v_cache, num_blocks, num_kv_heads, dtype, &km, &vm)) return KV_ERR_CUDA;
     const bool fp8 = dtype == KV_FP8_E4M3;
-    if ((fp8 ? pkv_host::ensure_dynamic_smem<prefill_kernel<true>>(Lay<true>::SMEM_BYTES)
-             : pkv_host::ensure_dynamic_smem<prefill_kernel<false>>(Lay<false>::SMEM_BYTES)) != cudaSuccess)
+    // bf16 chunk tiles: the V of one (block, head) as one 3-D box holding both
+    // 64-dim halves ([half][16 keys][64 dims] in shared memory): dims (64 dims,
+    // rows, halves), strides (row 256 B, half 128 B)
+    if (!fp8 && !pkv_host::encode_tmap_3d(&vm, v_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64,
+                                          (uint64_t)num_blocks * num_kv_heads * BS, 2, (uint64_t)D * 2, 128,
+                                          64, BS, 2, CU_TENSOR_MAP_SWIZZLE_128B))
         return KV_ERR_CUDA;
+    const cudaError_t smem_ok =
+        big   ? pkv_host::ensure_dynamic_smem<prefill_kernel<false, true>>(Lay<false, true>::SMEM_BYTES)
+        : fp8 ? pkv_host::ensure_dynamic_smem<prefill_kernel<true, false>>(Lay<true>::SMEM_BYTES)
+              : pkv_host::ensure_dynamic_smem<prefill_kernel<false, false>>(Lay<false>::SMEM_BYTES);
+    if (smem_ok != cudaSuccess) return KV_ERR_CUDA;
     tile_prefix_kernel<<<1, 1024, 0, st>>>(p);
     // grid.x bounds the number of query tiles: sum over chunks of ceil(n/tpt)
     const int64_t tiles_ub = (total_q_tokens + tpt - 1) / tpt + std::min<int64_t>(num_seqs, total_q_tokens / 2);
@@ -1010,10 +1097,13 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     dim3 grid((unsigned)tiles_ub, num_kv_heads, p.max_splits);
     Trace *tr = trace_for_call();
     if (tr) cudaEventRecord(tr->start, st);
-    if (fp8)
-        prefill_kernel<true><<<grid, Lay<true>::THREADS, Lay<true>::SMEM_BYTES, st>>>(qm, km, vm, p);
+    if (big)
+        prefill_kernel<false, true>
+            <<<grid, Lay<false, true>::THREADS, Lay<false, true>::SMEM_BYTES, st>>>(qm, km, vm, p);
+    else if (fp8)
+        prefill_kernel<true, false><<<grid, Lay<true>::THREADS, Lay<true>::SMEM_BYTES, st>>>(qm, km, vm, p);
     else
-        prefill_kernel<false><<<grid, Lay<false>::THREADS, Lay<false>::SMEM_BYTES, st>>>(qm, km, vm, p);
+        prefill_kernel<false, false><<<grid, Lay<false>::THREADS, Lay<false>::SMEM_BYTES, st>>>(qm, km, vm, p);
     if (tr) {
         cudaEventRecord(tr->stop, st);
         tr->recorded = true;
