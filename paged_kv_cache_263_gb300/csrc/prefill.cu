@@ -153,6 +153,9 @@ struct PrefillParams {
     const int32_t *context_lens;
     const int32_t *block_tables;
     int32_t *tile_off;   // [num_seqs + 1] pairs of query tiles per sequence, prefix sums
+    int2 *order;         // work items (x, partition << 16 | KV head), longest first
+    int32_t *order_count;
+    int items_cap;       // query items the order array has room for (x 1 KV head x 1 partition)
     float *part_o;       // [rows][Hq][max_splits][128]
     float *part_ml;      // [rows][Hq][max_splits][2]
     int max_blocks, num_seqs, hq, hkv, group, num_blocks, total_rows;
@@ -165,6 +168,43 @@ struct PrefillParams {
 };
 
 __device__ __forceinline__ void flag(uint32_t bits) { atomicOr(&g_status, bits); }
+
+// One CTA's work: query item x (a pair of query tiles, or one tile in the
+// 128-key layout) of some chunk sequence, and key partition `split` of the keys
+// its rows see.  The keys are cut into nsplit partitions of (nearly) equal
+// length, at most tiles_per_split KV tiles each, so that no short partition
+// trails the grid.  False when the partition is empty.
+struct Work {
+    int s, item, row0, n, L, t0q, KT, nsplit, j0, T;
+    bool has1;
+};
+__device__ __forceinline__ bool locate(const PrefillParams &p, int x, int split, int item_tiles, int tile_keys,
+                                       Work &w)
+{
+    int lo = 0, hi = p.num_seqs;                 // tile_off[lo] <= x < tile_off[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.tile_off[mid] <= x) lo = mid;
+        else hi = mid;
+    }
+    w.s = lo;
+    w.item = x - p.tile_off[lo];
+    w.row0 = p.cu_q_lens[lo];
+    w.n = p.cu_q_lens[lo + 1] - w.row0;
+    w.L = p.context_lens[lo];
+    const int tpt = BM / p.group;
+    const int tiles = (w.n + tpt - 1) / tpt;
+    w.t0q = item_tiles * w.item;                  // the CTA's first query tile
+    w.has1 = item_tiles == 2 && w.t0q + 1 < tiles;   // the pair's second query tile exists
+    const int last = w.has1 ? w.t0q + 1 : w.t0q;
+    const int kmax = w.L - w.n + min(w.n, (last + 1) * tpt);   // keys visible to the last row
+    w.KT = (kmax + tile_keys - 1) / tile_keys;
+    w.nsplit = (w.KT + p.tiles_per_split - 1) / p.tiles_per_split;
+    const int tps = (w.KT + w.nsplit - 1) / w.nsplit;   // ceil(KT / tps) == nsplit
+    w.j0 = split * tps;
+    w.T = min(w.KT, w.j0 + tps) - w.j0;
+    return w.j0 < w.KT;
+}
 
 // bounded wait that also gives up as soon as another role has aborted
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag)
@@ -232,6 +272,80 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         __syncthreads();
     }
     if (threadIdx.x == 0) p.tile_off[0] = 0;
+    __syncthreads();
+
+    // ---- the work items in launch order, longest first.  A chunk CTA holds a
+    // whole SM, so the grid runs in waves; launched in grid order, a long item
+    // that starts in the last wave sets the makespan (ragged speculative drafts).
+    // Longest-processing-time-first list order instead: items are bucketed by
+    // length relative to the longest partition (NBKT buckets) and sorted stably,
+    // so that within a bucket they keep the grid order (item fastest, then KV
+    // head, then partition), under which concurrent CTAs share their keys in L2.
+    // Each warp takes a contiguous segment of the slots; a slot's rank is its
+    // bucket's start + the earlier warps' counts in that bucket + its rank in
+    // its own warp's segment, so the order is deterministic.
+    constexpr int NBKT = 32;
+    static_assert(NBKT == 32, "one warp scans the buckets");
+    __shared__ int32_t cnt[32][NBKT];
+    __shared__ int32_t bstart[NBKT];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    // query items over all chunks; more than the host's bound only with chunk
+    // metadata that overlaps (flagged), and then the excess is left out
+    const int X = min(carry, p.items_cap);
+    if (threadIdx.x == 0 && carry > p.items_cap) flag(ST_BAD_LEN);
+    const long long nslot = (long long)X * p.hkv * p.max_splits;
+    const long long seg = (nslot + nw - 1) / nw;
+    const long long s0 = (long long)w * seg, s1 = min(nslot, s0 + seg);
+    for (int i = threadIdx.x; i < 32 * NBKT; i += blockDim.x) cnt[i / NBKT][i % NBKT] = 0;
+    __syncthreads();
+    auto bucket_of = [&](long long e, int2 &ent) -> int {
+        const int x = (int)(e % X);
+        const long long r = e / X;
+        const int g = (int)(r % p.hkv), split = (int)(r / p.hkv);
+        Work wk;
+        if (!locate(p, x, split, p.item_tiles, p.tile_keys, wk)) return -1;
+        ent = make_int2(x, (split << 16) | g);
+        return min(NBKT - 1, (int)(((long long)(p.tiles_per_split - wk.T) * NBKT) / p.tiles_per_split));
+    };
+    for (long long b0 = s0; b0 < s1; b0 += 32) {
+        int2 ent;
+        const int bk = b0 + lane < s1 ? bucket_of(b0 + lane, ent) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, bk);
+        if (bk >= 0 && lane == __ffs(peers) - 1) cnt[w][bk] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    if (threadIdx.x < NBKT) {                     // per bucket: earlier warps' counts
+        int run = 0;
+        for (int i = 0; i < nw; ++i) {
+            const int t = cnt[i][threadIdx.x];
+            cnt[i][threadIdx.x] = run;
+            run += t;
+        }
+        bstart[threadIdx.x] = run;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {                       // exclusive scan of the bucket totals
+        const int tot = bstart[lane];
+        int v = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += t;
+        }
+        bstart[lane] = v - tot;
+        if (lane == 31) p.order_count[0] = v;
+    }
+    __syncthreads();
+    for (long long b0 = s0; b0 < s1; b0 += 32) {
+        int2 ent;
+        const int bk = b0 + lane < s1 ? bucket_of(b0 + lane, ent) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, bk);
+        if (bk >= 0) p.order[bstart[bk] + cnt[w][bk] + __popc(peers & ((1u << lane) - 1u))] = ent;
+        __syncwarp();
+        if (bk >= 0 && lane == __ffs(peers) - 1) cnt[w][bk] += __popc(peers);
+        __syncwarp();
+    }
 }
 
 // (the fp8 variant declares 512 threads so that registers stay <= 128, which 15
@@ -259,32 +373,18 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
         return __all_sync(0xffffffffu, wait_bar(b, parity, abort_flag));
     };
 
-    // ---- which pair of query tiles / KV head / partition
-    const int x = blockIdx.x, g = blockIdx.y, split = blockIdx.z;
-    if (x >= p.tile_off[p.num_seqs]) return;
-    int lo = 0, hi = p.num_seqs;                 // tile_off[lo] <= x < tile_off[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (p.tile_off[mid] <= x) lo = mid;
-        else hi = mid;
-    }
-    const int s = lo, item = x - p.tile_off[s];
-    const int row0 = p.cu_q_lens[s], n = p.cu_q_lens[s + 1] - row0, L = p.context_lens[s];
+    // ---- which query item / KV head / partition: the CTA's place in the
+    // longest-first order that tile_prefix_kernel wrote
+    if ((int)blockIdx.x >= p.order_count[0]) return;
+    const int2 ent = p.order[blockIdx.x];
+    const int x = ent.x, g = ent.y & 0xffff, split = (int)((unsigned)ent.y >> 16);
+    Work wk;
+    if (!locate(p, x, split, BIG ? 1 : 2, BN, wk)) return;
+    const int s = wk.s, row0 = wk.row0, n = wk.n, L = wk.L;
     const int G = p.group, tpt = BM / G;
-    const int tiles = (n + tpt - 1) / tpt;
-    const int t0q = BIG ? item : 2 * item;       // the CTA's first query tile
-    const bool has1 = !BIG && t0q + 1 < tiles;   // the pair's second query tile exists
-    const int last = has1 ? t0q + 1 : t0q;
-    const int kmax = L - n + min(n, (last + 1) * tpt);   // keys visible to the pair's last row
-    const int KT = (kmax + BN - 1) / BN;
-    // the pair's keys in nsplit partitions of (nearly) equal length, at most
-    // tiles_per_split tiles each, so that no short partition trails the grid
-    const int nsplit = (KT + p.tiles_per_split - 1) / p.tiles_per_split;
-    const int tps = (KT + nsplit - 1) / nsplit;   // ceil(KT / tps) == nsplit
-    const int j0 = split * tps;
-    if (j0 >= KT) return;
-    const int j1 = min(KT, j0 + tps);
-    const int T = j1 - j0;
+    const int t0q = wk.t0q;
+    const bool has1 = wk.has1;
+    const int j0 = wk.j0, T = wk.T, nsplit = wk.nsplit;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (sbase & 1023u) {
         // the 128-byte swizzle needs 1024-byte aligned tiles; never observed, but
@@ -771,8 +871,9 @@ constexpr double CTA_FIXED_TILES = 4.0;        // a CTA's Q load, set-up and epi
 constexpr double BYTES_PER_TILE_TIME = 5.6e6;
 
 struct Plan {
-    size_t decode_bytes, part_o_off, part_ml_off, tile_off_off, total;
+    size_t decode_bytes, part_o_off, part_ml_off, tile_off_off, order_off, total;
     int max_splits, tiles_per_split;
+    int64_t items_ub;    // bounds the query items: sum over chunks of ceil(n / tpt)
 };
 
 }  // namespace
@@ -857,6 +958,13 @@ Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq,
     if (pl.max_splits > 1) off += up((size_t)total_q * hq * pl.max_splits * 2 * sizeof(float));
     pl.tile_off_off = off;
     if (max_q_len >= 2) off += up((size_t)(num_seqs + 1) * sizeof(int32_t));
+    // the work items in launch order (x, partition and head packed in an int2),
+    // then their count
+    const int G = std::max(1, hq / std::max(1, hkv)), tpt = std::max(1, BM / G);
+    pl.items_ub = ((int64_t)total_q + tpt - 1) / tpt + std::min<int64_t>(num_seqs, total_q / 2);
+    pl.order_off = off;
+    if (max_q_len >= 2)
+        off += up((size_t)pl.items_ub * hkv * std::max(1, pl.max_splits) * sizeof(int2)) + up(sizeof(int32_t));
     pl.total = off;
     return pl;
 }
@@ -1054,6 +1162,10 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     p.context_lens = context_lens;
     p.block_tables = block_tables;
     p.tile_off = reinterpret_cast<int32_t *>(ws + pl.tile_off_off);
+    p.order = reinterpret_cast<int2 *>(ws + pl.order_off);
+    p.items_cap = (int)std::min<int64_t>(pl.items_ub, INT32_MAX);
+    p.order_count = reinterpret_cast<int32_t *>(
+        ws + pl.order_off + ((pl.items_ub * num_kv_heads * std::max(1, pl.max_splits) * sizeof(int2) + 255) & ~size_t(255)));
     p.part_o = pl.max_splits > 1 ? reinterpret_cast<float *>(ws + pl.part_o_off) : nullptr;
     p.part_ml = pl.max_splits > 1 ? reinterpret_cast<float *>(ws + pl.part_ml_off) : nullptr;
     p.max_blocks = max_blocks_per_seq;
@@ -1090,11 +1202,12 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
         : fp8 ? pkv_host::ensure_dynamic_smem<prefill_kernel<true, false>>(Lay<true>::SMEM_BYTES)
               : pkv_host::ensure_dynamic_smem<prefill_kernel<false, false>>(Lay<false>::SMEM_BYTES);
     if (smem_ok != cudaSuccess) return KV_ERR_CUDA;
+    // one CTA per work item (query item, KV head, partition), in the order that
+    // tile_prefix_kernel writes; the grid bounds their number
+    const int64_t ctas_ub = pl.items_ub * num_kv_heads * p.max_splits;
+    if (ctas_ub > INT32_MAX || p.max_splits > 65535 || num_kv_heads > 65535) return KV_ERR_UNSUPPORTED;
     tile_prefix_kernel<<<1, 1024, 0, st>>>(p);
-    // grid.x bounds the number of query tiles: sum over chunks of ceil(n/tpt)
-    const int64_t tiles_ub = (total_q_tokens + tpt - 1) / tpt + std::min<int64_t>(num_seqs, total_q_tokens / 2);
-    if (tiles_ub > INT32_MAX || p.max_splits > 65535) return KV_ERR_UNSUPPORTED;
-    dim3 grid((unsigned)tiles_ub, num_kv_heads, p.max_splits);
+    dim3 grid((unsigned)ctas_ub);
     Trace *tr = trace_for_call();
     if (tr) cudaEventRecord(tr->start, st);
     if (big)
