@@ -74,7 +74,6 @@ constexpr float RESCALE_LOG2 = 8.0f;
 // cache: e4m3 staging stages of (K 8 KiB, V 8 KiB)) | barriers.  P lives in
 // tensor memory.
 constexpr uint32_t SQ = 0, Q_TILE = 32768;
-constexpr uint32_t KV_STAGE_BYTES = 32768, V_OFF = 16384, KV_HALF = 8192;   // the 64-key layout
 constexpr uint32_t F8_STAGE_BYTES = 16384, F8_V_OFF = 8192;
 // bf16 cache: warps 0-3 softmax of query tile 0, 4-7 softmax of query tile 1, 8 TMA
 // producer, 9 and 10 MMA issuers of query tile 0 and 1.  fp8 cache: in addition
@@ -108,29 +107,40 @@ struct Lay {
     static constexpr uint32_t SKV = NG * 32768;               // K/V stages follow the Q tiles
     static constexpr uint32_t SF8 = SKV + KV_STAGES * KV_STAGE_BYTES;
     static constexpr uint32_t SBAR = SF8 + F8_STAGES * F8_STAGE_BYTES;
-    // + 1 KiB: the dynamic shared memory is aligned to 1 KiB at run time
-    static constexpr int SMEM_BYTES = SBAR + 512 + 1024;
+    // barriers, the TMEM address, the abort flag and the work-item slots; + 1 KiB:
+    // the dynamic shared memory is aligned to 1 KiB at run time
+    static constexpr int SMEM_BYTES = SBAR + 1024 + 1024;
     static constexpr uint32_t S_COLS = 2 * BNK;               // two S buffers per query tile
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(NG * (S_COLS + 128) <= 512, "tensor memory");
     static_assert(!(FP8 && BIG), "the 128-key layout is for the bf16 cache");
 };
+// work items a CTA's producer may have fetched ahead of its slowest warp
+constexpr int NSLOT = 4;
 // barriers (room for the larger of the two layouts)
 enum {
     B_KVF = 0,                      // + stage: K and V operand tiles ready
     B_KVE = B_KVF + 4,              // + stage: every MMA reading the stage is done
-    B_Q = B_KVE + 4,                // both Q tiles landed
-    B_QC = B_Q + 1,                 // + group: fp8 cache: the group's Q tile is in f16
+    B_Q = B_KVE + 4,                // the item's Q tiles landed
+    B_QFREE = B_Q + 1,              // every QK^T product of the item finished (one per issuer)
+    B_QC = B_QFREE + 1,             // + group: fp8 cache: the group's Q tile is in f16
     B_S = B_QC + 2,                 // + 2*group + buffer: an S tile of the group is in TMEM
     B_P = B_S + 4,                  // + 2*group + buffer: the group's P is in TMEM (128 arrivals)
     B_PVD = B_P + 4,                // + group: the group's latest PV product finished
-    B_DRAIN = B_PVD + 2,            // + group: every MMA of the group's issuer finished
-    B_TAIL = B_DRAIN + 2,           // bf16 cache: the V rows past the context are zeroed
-    B_F8F = B_TAIL + 1,             // + staging stage: fp8 cache: e4m3 K and V landed
+    B_DRAIN = B_PVD + 2,            // + group: every MMA of the group's item finished
+    B_TAIL = B_DRAIN + 2,           // + stage: bf16 cache: the V rows past the context are zeroed
+    B_F8F = B_TAIL + 4,             // + staging stage: fp8 cache: e4m3 K and V landed
     B_F8E = B_F8F + 3,              // + staging stage: fp8 cache: the stage was widened
-    NBAR = B_F8E + 3
+    B_IFULL = B_F8E + 3,            // + slot: the producer wrote a work item into the slot
+    B_IEMPTY = B_IFULL + NSLOT,     // + slot: every other warp has read it
+    NBAR = B_IEMPTY + NSLOT
 };
-static_assert(NBAR * 8 + 8 <= 512, "barrier area");
+// a work item as the producer hands it to the other warps (valid = 0: no more)
+struct ItemSlot {
+    int s, row0, n, L, t0q, has1, j0, T, nsplit, g, split, valid, pad[4];
+};
+constexpr uint32_t SLOT_OFF = 512;   // within the barrier area
+static_assert(NBAR * 8 + 8 <= SLOT_OFF && SLOT_OFF + NSLOT * sizeof(ItemSlot) <= 1024, "barrier area");
 
 // instruction descriptors, kind::f16: fp32 accumulate, bf16 A and B, M=128
 constexpr uint32_t idesc(int n, bool b_mn_major)
@@ -153,13 +163,16 @@ struct PrefillParams {
     const int32_t *context_lens;
     const int32_t *block_tables;
     int32_t *tile_off;   // [num_seqs + 1] pairs of query tiles per sequence, prefix sums
-    int2 *order;         // work items (x, partition << 16 | KV head), longest first
-    int32_t *order_count;
+    int4 *order;         // work items, longest first: two int4 each (see tile_prefix_kernel)
+    int32_t *row_info;   // [rows] key partitions of the row's query item (0: not a chunk row)
+    int32_t *order_count;  // [0] items listed, [1] items taken so far (the CTAs' counter), [2] any cut
     int items_cap;       // query items the order array has room for (x 1 KV head x 1 partition)
     float *part_o;       // [rows][Hq][max_splits][128]
     float *part_ml;      // [rows][Hq][max_splits][2]
     int max_blocks, num_seqs, hq, hkv, group, num_blocks, total_rows;
-    int tiles_per_split, max_splits;
+    int tiles_per_split, max_splits;   // the shortest partition length allowed; room for partitions
+    int num_sms;
+    float bytes_per_tile;              // HBM bytes the GPU moves in one KV tile's time
     int item_tiles;      // query tiles per CTA: 2 (a pair), or 1 (the 128-key layout)
     int tile_keys;       // keys per KV tile: 64, or 128 (the 128-key layout)
     float scale_log2;
@@ -172,26 +185,29 @@ __device__ __forceinline__ void flag(uint32_t bits) { atomicOr(&g_status, bits);
 // One CTA's work: query item x (a pair of query tiles, or one tile in the
 // 128-key layout) of some chunk sequence, and key partition `split` of the keys
 // its rows see.  The keys are cut into nsplit partitions of (nearly) equal
-// length, at most tiles_per_split KV tiles each, so that no short partition
-// trails the grid.  False when the partition is empty.
+// length, at most tiles_per_split KV tiles each.  False when the partition is
+// empty.
 struct Work {
     int s, item, row0, n, L, t0q, KT, nsplit, j0, T;
     bool has1;
 };
-__device__ __forceinline__ bool locate(const PrefillParams &p, int x, int split, int item_tiles, int tile_keys,
-                                       Work &w)
+// (toff, cu, cl: the query items' prefix sums, cu_q_lens and context_lens, in
+// global or shared memory)
+__device__ __forceinline__ bool locate(const PrefillParams &p, const int32_t *toff, const int32_t *cu,
+                                       const int32_t *cl, int x, int split, int item_tiles, int tile_keys,
+                                       int tiles_per_split, Work &w)
 {
-    int lo = 0, hi = p.num_seqs;                 // tile_off[lo] <= x < tile_off[hi]
+    int lo = 0, hi = p.num_seqs;                 // toff[lo] <= x < toff[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (p.tile_off[mid] <= x) lo = mid;
+        if (toff[mid] <= x) lo = mid;
         else hi = mid;
     }
     w.s = lo;
-    w.item = x - p.tile_off[lo];
-    w.row0 = p.cu_q_lens[lo];
-    w.n = p.cu_q_lens[lo + 1] - w.row0;
-    w.L = p.context_lens[lo];
+    w.item = x - toff[lo];
+    w.row0 = cu[lo];
+    w.n = cu[lo + 1] - w.row0;
+    w.L = cl[lo];
     const int tpt = BM / p.group;
     const int tiles = (w.n + tpt - 1) / tpt;
     w.t0q = item_tiles * w.item;                  // the CTA's first query tile
@@ -199,7 +215,7 @@ __device__ __forceinline__ bool locate(const PrefillParams &p, int x, int split,
     const int last = w.has1 ? w.t0q + 1 : w.t0q;
     const int kmax = w.L - w.n + min(w.n, (last + 1) * tpt);   // keys visible to the last row
     w.KT = (kmax + tile_keys - 1) / tile_keys;
-    w.nsplit = (w.KT + p.tiles_per_split - 1) / p.tiles_per_split;
+    w.nsplit = (w.KT + tiles_per_split - 1) / tiles_per_split;
     const int tps = (w.KT + w.nsplit - 1) / w.nsplit;   // ceil(KT / tps) == nsplit
     w.j0 = split * tps;
     w.T = min(w.KT, w.j0 + tps) - w.j0;
@@ -224,30 +240,128 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-// per-sequence query-tile counts -> prefix sums; validates chunk metadata
+// The chunk kernel's work list, one CTA of 1024 threads:
+//  1. per sequence (a thread each): the chunk metadata validated, its query
+//     items counted (then a block-wide scan), and its share of the partition
+//     length estimates below;
+//  2. the partition length;
+//  3. per query row, the number of key partitions its item is cut into (for
+//     the merge kernel); the work items' bucket counts;
+//  4. the work items in launch order.
+// Sequence data is staged in shared memory when there are at most PREFIX_SMAX
+// sequences, so that the searches cost no global-memory round trips.
+//
+// The partition length.  The host's plan (tiles_per_split) is the shortest
+// allowed: the workspace holds that many partitions.  Here the real key ranges
+// are known, and a longer length (fewer partitions) is taken where a makespan
+// estimate favours it.  The CTAs take the items longest first, so the grid ends
+// about max(longest item, S / m + shortest item / 2) after it starts (S: all
+// items' tiles, m: SMs); each item adds a fixed cost, and a cut key range adds
+// its partial results' write and merge (and the merge kernel's start).  The
+// candidates are the host's length and uncut; every item of a sequence is taken
+// to see as many keys as its last one.
+constexpr int PREFIX_SMAX = 2048;
 __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
 {
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t carry;
-    const int tpt = BM / p.group;
-    if (threadIdx.x == 0) carry = 0;
+    __shared__ int32_t sh_toff[PREFIX_SMAX + 1], sh_cu[PREFIX_SMAX + 1], sh_cl[PREFIX_SMAX];
+    // per candidate (0: the host's length, 1: uncut): items, longest and shortest
+    // partition; the cut ranges' rows x partitions; all items' tiles (summed a
+    // warp at a time: shared-memory atomics on one word serialise a warp)
+    __shared__ unsigned int c_items[2];
+    __shared__ int c_tmax[2], c_tmin[2];
+    __shared__ float c_mrows, s_tiles;
+    __shared__ int s_tps;
+    constexpr int NBKT = 32;
+    static_assert(NBKT == 32, "one warp scans the buckets");
+    __shared__ int32_t cnt[32][NBKT];
+    __shared__ int32_t bstart[NBKT];
+    // the chunk kernel (launched with programmatic serialisation) may set up its
+    // CTAs meanwhile; it waits for this grid before it reads the work list
+    griddep_launch_dependents();
+    const bool staged = p.num_seqs <= PREFIX_SMAX;
+    const int tpt = BM / p.group, tk = p.tile_keys, tps0 = max(1, p.tiles_per_split);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (threadIdx.x < 2) {
+        c_items[threadIdx.x] = 0u;
+        c_tmax[threadIdx.x] = 0;
+        c_tmin[threadIdx.x] = INT_MAX;
+    }
+    for (int i = threadIdx.x; i < 32 * NBKT; i += blockDim.x) cnt[i / NBKT][i % NBKT] = 0;
+    if (threadIdx.x == 0) {
+        carry = 0;
+        s_tiles = 0.f;
+        c_mrows = 0.f;
+        sh_toff[0] = 0;
+    }
     __syncthreads();
+
+    // ---- 1. per sequence
     for (int base = 0; base < p.num_seqs; base += blockDim.x) {
         const int s = base + threadIdx.x;
-        int tiles = 0;
+        int tiles = 0, n = 0, L = 0;
         if (s < p.num_seqs) {
             const int a = p.cu_q_lens[s], b = p.cu_q_lens[s + 1];
-            const int n = b - a, L = p.context_lens[s];
+            n = b - a;
+            L = p.context_lens[s];
             if (n >= 2) {
                 if (a < 0 || b > p.total_rows || L < n || L > p.max_blocks * BS) flag(ST_BAD_LEN);
-                else tiles = ((n + tpt - 1) / tpt + p.item_tiles - 1) / p.item_tiles;   // CTAs along x
+                else tiles = ((n + tpt - 1) / tpt + p.item_tiles - 1) / p.item_tiles;   // query items
             } else if (n < 0) {
                 flag(ST_BAD_LEN);
             }
+            if (staged) {
+                sh_cu[s] = a;
+                sh_cl[s] = L;
+                if (s == p.num_seqs - 1) sh_cu[s + 1] = b;
+            }
         }
-        // block-wide inclusive scan
+        {
+            // this sequence's share of the estimates (zeros for no chunk), summed
+            // over the warp, then one shared-memory update per warp
+            unsigned it0 = 0u, it1 = 0u;
+            int mx0 = 0, mn0 = INT_MAX, mx1 = 0, mn1 = INT_MAX;
+            float tl = 0.f, mr = 0.f;
+            if (tiles > 0) {
+                const int KT = (L + tk - 1) / tk;
+                // the items' tiles: item x sees L - n + min(n, (x + 1) r) keys, r rows per item
+                const float r = (float)(tpt * p.item_tiles);
+                tl = (tiles * (float)(L - n) + r * 0.5f * (tiles - 1) * tiles + n) / tk;
+                const int ns = (KT + tps0 - 1) / tps0, len = (KT + ns - 1) / ns;
+                it0 = (unsigned)(tiles * ns);
+                mx0 = len;
+                mn0 = KT - (ns - 1) * len;
+                if (ns > 1) mr = (float)n * ns;
+                it1 = (unsigned)tiles;
+                mx1 = mn1 = KT;
+            }
+            if (__any_sync(0xffffffffu, tiles > 0)) {
+                it0 = __reduce_add_sync(0xffffffffu, it0);
+                it1 = __reduce_add_sync(0xffffffffu, it1);
+                mx0 = __reduce_max_sync(0xffffffffu, mx0);
+                mx1 = __reduce_max_sync(0xffffffffu, mx1);
+                mn0 = __reduce_min_sync(0xffffffffu, mn0);
+                mn1 = __reduce_min_sync(0xffffffffu, mn1);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    tl += __shfl_xor_sync(0xffffffffu, tl, o);
+                    mr += __shfl_xor_sync(0xffffffffu, mr, o);
+                }
+                if (lane == 0) {
+                    atomicAdd(&c_items[0], it0);
+                    atomicAdd(&c_items[1], it1);
+                    atomicMax(&c_tmax[0], mx0);
+                    atomicMax(&c_tmax[1], mx1);
+                    atomicMin(&c_tmin[0], mn0);
+                    atomicMin(&c_tmin[1], mn1);
+                    atomicAdd(&s_tiles, tl);
+                    atomicAdd(&c_mrows, mr);
+                }
+            }
+        }
+        // block-wide inclusive scan of the item counts
         int v = tiles;
-        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             int t = __shfl_up_sync(0xffffffffu, v, o);
@@ -256,7 +370,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         if (lane == 31) warp_sums[w] = v;
         __syncthreads();
         if (w == 0) {
-            int x = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+            int x = lane < nw ? warp_sums[lane] : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 int t = __shfl_up_sync(0xffffffffu, x, o);
@@ -266,82 +380,131 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         }
         __syncthreads();
         const int incl = v + (w > 0 ? warp_sums[w - 1] : 0) + carry;
-        if (s < p.num_seqs) p.tile_off[s + 1] = incl;
+        if (s < p.num_seqs) {
+            p.tile_off[s + 1] = incl;
+            if (staged) sh_toff[s + 1] = incl;
+        }
         __syncthreads();
         if (threadIdx.x == blockDim.x - 1) carry = incl;
         __syncthreads();
     }
-    if (threadIdx.x == 0) p.tile_off[0] = 0;
-    __syncthreads();
 
-    // ---- the work items in launch order, longest first.  A chunk CTA holds a
-    // whole SM, so the grid runs in waves; launched in grid order, a long item
-    // that starts in the last wave sets the makespan (ragged speculative drafts).
-    // Longest-processing-time-first list order instead: items are bucketed by
-    // length relative to the longest partition (NBKT buckets) and sorted stably,
-    // so that within a bucket they keep the grid order (item fastest, then KV
-    // head, then partition), under which concurrent CTAs share their keys in L2.
-    // Each warp takes a contiguous segment of the slots; a slot's rank is its
-    // bucket's start + the earlier warps' counts in that bucket + its rank in
-    // its own warp's segment, so the order is deterministic.
-    constexpr int NBKT = 32;
-    static_assert(NBKT == 32, "one warp scans the buckets");
-    __shared__ int32_t cnt[32][NBKT];
-    __shared__ int32_t bstart[NBKT];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    // ---- 2. the partition length
+    if (threadIdx.x == 0) {
+        p.tile_off[0] = 0;
+        const float m = (float)p.num_sms, S = s_tiles * p.hkv;
+        // a partial result (130 floats per head) is written and read once
+        const float per_row_split = (float)p.hq * 130.f * 4.f * 2.f / p.bytes_per_tile;
+        const float merge_start = 3.f * 64.f / tk;   // the merge kernel's start, in tile-times
+        constexpr float ITEM_TILES = 0.5f;           // per item: its Q load and epilogue
+        auto est = [&](int k, float merge) {
+            return fmaxf((float)c_tmax[k], S / m + 0.5f * (float)c_tmin[k]) +
+                   (float)c_items[k] * p.hkv * ITEM_TILES / m + merge;
+        };
+        const bool cut0 = c_mrows > 0.f;
+        int pick = tps0, cut = cut0 ? 1 : 0;
+        if (cut0 && est(1, 0.f) <= est(0, c_mrows * per_row_split + merge_start)) {
+            pick = max(tps0, c_tmax[1]);             // uncut: every range in one partition
+            cut = 0;
+        }
+        s_tps = pick;
+        p.order_count[2] = cut;                      // the merge kernel has work
+    }
+    __syncthreads();
+    const int tps = s_tps;
+    const int32_t *toff = staged ? sh_toff : p.tile_off;
+    const int32_t *cu = staged ? sh_cu : p.cu_q_lens;
+    const int32_t *cl = staged ? sh_cl : p.context_lens;
     // query items over all chunks; more than the host's bound only with chunk
     // metadata that overlaps (flagged), and then the excess is left out
     const int X = min(carry, p.items_cap);
     if (threadIdx.x == 0 && carry > p.items_cap) flag(ST_BAD_LEN);
+
+    // ---- 3. per query row: its item's partition count (0 for rows outside any
+    // chunk); and the work items' bucket counts
+    for (int row = threadIdx.x; row < p.total_rows; row += blockDim.x) {
+        int lo = 0, hi = p.num_seqs;                 // cu[lo] <= row < cu[hi]
+        int ns = 0;
+        if (row < cu[p.num_seqs]) {
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (cu[mid] <= row) lo = mid;
+                else hi = mid;
+            }
+            const int a = cu[lo], n = cu[lo + 1] - a, L = cl[lo];
+            if (n >= 2 && a >= 0 && row >= a && L >= n && L <= p.max_blocks * BS) {
+                const int i = row - a, mt = i / tpt, tiles = (n + tpt - 1) / tpt;
+                const int last = min(tiles - 1, (mt / p.item_tiles) * p.item_tiles + p.item_tiles - 1);
+                const int KT = (L - n + min(n, (last + 1) * tpt) + tk - 1) / tk;
+                ns = (KT + tps - 1) / tps;
+            }
+        }
+        p.row_info[row] = ns;
+    }
+    // The work items in launch order, longest first: the CTAs take them one
+    // after another, so a long item taken last would set the makespan (ragged
+    // speculative drafts).  Longest-processing-time-first list order instead:
+    // items are bucketed by length relative to the partition length (NBKT
+    // buckets) and sorted stably, so that within a bucket they keep the order
+    // item fastest, then KV head, then partition, under which concurrent CTAs
+    // share their keys in L2.  Each warp takes a contiguous segment of the
+    // slots; a slot's rank is its bucket's start + the earlier warps' counts in
+    // that bucket + its rank in its own warp's segment, so the order is
+    // deterministic.  An entry (two int4) holds everything a CTA needs:
+    //   s, row0, n, L | j0, T | nsplit << 16, KV head | partition << 16, t0q | has1 << 30
+    // (the slot count is below 2^31: the host bounds the grid by it)
     const long long nslot = (long long)X * p.hkv * p.max_splits;
     const long long seg = (nslot + nw - 1) / nw;
     const long long s0 = (long long)w * seg, s1 = min(nslot, s0 + seg);
-    for (int i = threadIdx.x; i < 32 * NBKT; i += blockDim.x) cnt[i / NBKT][i % NBKT] = 0;
-    __syncthreads();
-    auto bucket_of = [&](long long e, int2 &ent) -> int {
-        const int x = (int)(e % X);
-        const long long r = e / X;
-        const int g = (int)(r % p.hkv), split = (int)(r / p.hkv);
+    auto bucket_of = [&](long long e, int4 &e0, int4 &e1) -> int {
+        const unsigned eu = (unsigned)e, r = eu / (unsigned)X;
+        const int x = (int)(eu - r * (unsigned)X);
+        const int g = (int)(r % (unsigned)p.hkv), split = (int)(r / (unsigned)p.hkv);
         Work wk;
-        if (!locate(p, x, split, p.item_tiles, p.tile_keys, wk)) return -1;
-        ent = make_int2(x, (split << 16) | g);
-        return min(NBKT - 1, (int)(((long long)(p.tiles_per_split - wk.T) * NBKT) / p.tiles_per_split));
+        if (!locate(p, toff, cu, cl, x, split, p.item_tiles, tk, tps, wk)) return -1;
+        e0 = make_int4(wk.s, wk.row0, wk.n, wk.L);
+        e1 = make_int4(wk.j0, wk.T | (wk.nsplit << 16), g | (split << 16), wk.t0q | (wk.has1 ? 1 << 30 : 0));
+        return min(NBKT - 1, (int)(((long long)max(0, tps - wk.T) * NBKT) / tps));
     };
     for (long long b0 = s0; b0 < s1; b0 += 32) {
-        int2 ent;
-        const int bk = b0 + lane < s1 ? bucket_of(b0 + lane, ent) : -1;
+        int4 e0, e1;
+        const int bk = b0 + lane < s1 ? bucket_of(b0 + lane, e0, e1) : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, bk);
         if (bk >= 0 && lane == __ffs(peers) - 1) cnt[w][bk] += __popc(peers);
         __syncwarp();
     }
     __syncthreads();
-    if (threadIdx.x < NBKT) {                     // per bucket: earlier warps' counts
+    if (w == 0) {
+        // per bucket (a lane each): the earlier warps' counts, then the buckets' starts
         int run = 0;
         for (int i = 0; i < nw; ++i) {
-            const int t = cnt[i][threadIdx.x];
-            cnt[i][threadIdx.x] = run;
+            const int t = cnt[i][lane];
+            cnt[i][lane] = run;
             run += t;
         }
-        bstart[threadIdx.x] = run;
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {                       // exclusive scan of the bucket totals
-        const int tot = bstart[lane];
-        int v = tot;
+        int v = run;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int t = __shfl_up_sync(0xffffffffu, v, o);
             if (lane >= o) v += t;
         }
-        bstart[lane] = v - tot;
-        if (lane == 31) p.order_count[0] = v;
+        bstart[lane] = v - run;
+        if (lane == 31) {
+            p.order_count[0] = v;
+            p.order_count[1] = 0;                 // the persistent CTAs' fetch counter
+        }
     }
     __syncthreads();
+    // ---- 4. the entries
     for (long long b0 = s0; b0 < s1; b0 += 32) {
-        int2 ent;
-        const int bk = b0 + lane < s1 ? bucket_of(b0 + lane, ent) : -1;
+        int4 e0, e1;
+        const int bk = b0 + lane < s1 ? bucket_of(b0 + lane, e0, e1) : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, bk);
-        if (bk >= 0) p.order[bstart[bk] + cnt[w][bk] + __popc(peers & ((1u << lane) - 1u))] = ent;
+        if (bk >= 0) {
+            const int pos = bstart[bk] + cnt[w][bk] + __popc(peers & ((1u << lane) - 1u));
+            p.order[2 * pos] = e0;
+            p.order[2 * pos + 1] = e1;
+        }
         __syncwarp();
         if (bk >= 0 && lane == __ffs(peers) - 1) cnt[w][bk] += __popc(peers);
         __syncwarp();
@@ -350,6 +513,15 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
 
 // (the fp8 variant declares 512 threads so that registers stay <= 128, which 15
 // warps need on an SM partition holding four of them)
+//
+// Persistent: the grid holds one CTA per SM, and each CTA takes work items
+// (query item, KV head, partition) from the longest-first list that
+// tile_prefix_kernel wrote, one after another through an atomic counter, until
+// the list is used up.  The producer warp fetches an item and hands it to the
+// other warps through a ring of NSLOT shared-memory slots; the K/V stage ring,
+// the S buffers and every barrier phase run on across items, so the next item's
+// Q and first K/V tiles load, and its first QK^T products run, while the
+// softmax warps still finish the item before.
 template <bool FP8, bool BIG>
 __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -360,32 +532,23 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
     constexpr int BN = LY::BNK;                                   // keys per KV tile
     constexpr uint32_t SKV = LY::SKV, KV_STAGE_BYTES = LY::KV_STAGE_BYTES, V_OFF = LY::V_OFF,
                        KV_HALF = LY::KV_HALF;
+    constexpr int NWARPS = LY::THREADS / 32;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + LY::SBAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile ItemSlot *slots = reinterpret_cast<volatile ItemSlot *>(smem + LY::SBAR + SLOT_OFF);
     auto bar = [&](int i) -> uint32_t { return smem_u32(bars + i); };
     // warp-uniform wait: every role below runs warp-collective instructions
     // (ballots, tcgen05.ld/st), so a warp leaves a loop only as a whole
     auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
         return __all_sync(0xffffffffu, wait_bar(b, parity, abort_flag));
     };
-
-    // ---- which query item / KV head / partition: the CTA's place in the
-    // longest-first order that tile_prefix_kernel wrote
-    if ((int)blockIdx.x >= p.order_count[0]) return;
-    const int2 ent = p.order[blockIdx.x];
-    const int x = ent.x, g = ent.y & 0xffff, split = (int)((unsigned)ent.y >> 16);
-    Work wk;
-    if (!locate(p, x, split, BIG ? 1 : 2, BN, wk)) return;
-    const int s = wk.s, row0 = wk.row0, n = wk.n, L = wk.L;
-    const int G = p.group, tpt = BM / G;
-    const int t0q = wk.t0q;
-    const bool has1 = wk.has1;
-    const int j0 = wk.j0, T = wk.T, nsplit = wk.nsplit;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.group, tpt = BM / G;
+    griddep_launch_dependents();   // the merge kernel may be scheduled; it waits for this grid
     if (sbase & 1023u) {
         // the 128-byte swizzle needs 1024-byte aligned tiles; never observed, but
         // refuse rather than compute with a wrong layout
@@ -396,13 +559,15 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < KV_STAGES; ++i) {
             mbar_init(bar(B_KVF + i), FP8 ? 128 : 1);   // fp8: the widening warps arrive
-            mbar_init(bar(B_KVE + i), has1 ? 2 : 1);   // one release per MMA issuer
+            mbar_init(bar(B_KVE + i), LY::NG);          // one release per MMA issuer
+            mbar_init(bar(B_TAIL + i), 1);
         }
         for (int i = 0; i < F8_STAGES; ++i) {
             mbar_init(bar(B_F8F + i), 1);
             mbar_init(bar(B_F8E + i), 128);
         }
         mbar_init(bar(B_Q), 1);
+        mbar_init(bar(B_QFREE), LY::NG);
         for (int i = 0; i < 2; ++i) mbar_init(bar(B_QC + i), 128);
         for (int i = 0; i < 4; ++i) {
             mbar_init(bar(B_S + i), 1);
@@ -412,7 +577,10 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
             mbar_init(bar(B_PVD + i), 1);
             mbar_init(bar(B_DRAIN + i), 1);
         }
-        mbar_init(bar(B_TAIL), 1);
+        for (int i = 0; i < NSLOT; ++i) {
+            mbar_init(bar(B_IFULL + i), 1);
+            mbar_init(bar(B_IEMPTY + i), NWARPS - 1);   // every warp but the producer
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -424,64 +592,41 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // TMEM columns per query tile gi: two S buffers of 64 fp32 columns at
-    // 128 gi + 64 b (P overwrites the first 32 of a buffer with bf16 pairs once its
-    // S has been read), O at 256 + 128 gi
+    // TMEM columns per query tile gi: two S buffers of BN fp32 columns at
+    // S_COLS gi + BN b (P overwrites the first BN/2 of a buffer with 16-bit pairs
+    // once its S has been read), O after all S buffers, 128 columns per tile
     auto tS = [&](int gi, int b) -> uint32_t { return tmem + gi * LY::S_COLS + b * BN; };
     auto tO = [&](int gi) -> uint32_t { return tmem + LY::NG * LY::S_COLS + gi * D; };
+    // the k-th work item of this CTA, as every warp but the producer reads it
+    // (false: the list is used up, or the CTA gave up)
+    auto read_item = [&](int k, ItemSlot &it) -> bool {
+        const int sl = k % NSLOT;
+        if (!wait_w(bar(B_IFULL + sl), (k / NSLOT) & 1)) return false;
+        it.s = slots[sl].s;
+        it.row0 = slots[sl].row0;
+        it.n = slots[sl].n;
+        it.L = slots[sl].L;
+        it.t0q = slots[sl].t0q;
+        it.has1 = slots[sl].has1;
+        it.j0 = slots[sl].j0;
+        it.T = slots[sl].T;
+        it.nsplit = slots[sl].nsplit;
+        it.g = slots[sl].g;
+        it.split = slots[sl].split;
+        it.valid = slots[sl].valid;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_IEMPTY + sl));
+        return it.valid != 0;
+    };
+    // a tile whose keys run past the context (only ever an item's last tile):
+    // its V rows there are zeroed before PV reads them (bf16 cache)
+    auto has_tail = [&](const ItemSlot &it) -> bool { return (it.j0 + it.T) * BN > it.L; };
 
     if (warp == LY::W_PROD || warp == LY::W_PROD2) {
-        const int role = warp == LY::W_PROD ? 0 : 1;   // 0: K boxes + expect; 1 (BIG): V boxes
-        // ======================= TMA producer
-        const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks;
-        const int nblk = (L + BS - 1) / BS;
-        if (lane == 0 && role == 0) {
-            mbar_arrive_expect_tx(bar(B_Q), (has1 ? 4 : 2) * 16384);
-            for (int gi = 0; gi < (has1 ? 2 : 1); ++gi) {
-                const int zq = row0 + (t0q + gi) * tpt;
-                tma_load_3d(sbase + SQ + gi * Q_TILE, &qmap, 0, g * G, zq, bar(B_Q));
-                tma_load_3d(sbase + SQ + gi * Q_TILE + 16384, &qmap, 64, g * G, zq, bar(B_Q));
-            }
-        }
-        int issued = 0;
-        if constexpr (FP8) {
-            // e4m3 K and V of each block (one 2 KiB box each) into a staging stage;
-            // the widening warps turn it into the operand tiles
-            // lanes 0-7 each load one box per tile: lane = 2 x block + (K | V); the
-            // block ids of the next tile are read during the wait for a free stage
-            const int blk8 = (lane >> 1) & 3, kv = lane & 1;
-            auto block_id8 = [&](int jj) -> int32_t {
-                const int b = (j0 + jj) * (BN / BS) + blk8;
-                return (lane < 8 && jj < T && b < nblk) ? __ldg(bt + b) : -1;
-            };
-            int32_t next_id = block_id8(0);
-            for (int jj = 0; jj < T; ++jj) {
-                const int st = jj % F8_STAGES;
-                const int32_t id = next_id;
-                next_id = block_id8(jj + 1);
-                if (jj >= F8_STAGES && !wait_w(bar(B_F8E + st), ((jj - F8_STAGES) / F8_STAGES) & 1)) break;
-                const int j = j0 + jj;
-                const bool in = lane < 8 && j * (BN / BS) + blk8 < nblk;
-                const bool valid = in && id >= 0 && id < p.num_blocks;
-                if (in && !valid && kv == 0) flag(ST_BAD_BLOCK);
-                const unsigned vm = __ballot_sync(0xffffffffu, valid);
-                if (lane == 0) {
-                    fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(bar(B_F8F + st), __popc(vm) * 2048);
-                }
-                __syncwarp();
-                if (valid) {
-                    const int y = (id * p.hkv + g) * BS;
-                    const uint32_t dst = sbase + LY::SF8 + st * F8_STAGE_BYTES + kv * F8_V_OFF + blk8 * 2048;
-                    tma_load_2d(dst, kv ? &vmap : &kmap, 0, y, bar(B_F8F + st));
-                }
-                issued = jj + 1;
-            }
-            if (*abort_flag) {
-                for (int jj = max(0, issued - F8_STAGES); jj < issued; ++jj)
-                    (void)mbar_wait_bounded(bar(B_F8F + jj % F8_STAGES), (jj / F8_STAGES) & 1);
-            }
-        }
+        // ======================= TMA producer.  Role 0 fetches the work items,
+        // loads Q and the K boxes and arms each stage's barrier; role 1 (the
+        // 128-key layout) issues the V boxes.
+        const int role = warp == LY::W_PROD ? 0 : 1;
         // bf16 cache: one lane per box, so a tile's loads leave in one instruction.
         // K: two 2 KiB boxes per block (dims 0-63 and 64-127; the QK^T operand needs
         // each half of all the tile's keys contiguous), lanes 0 .. 2 NB - 1, lane =
@@ -495,131 +640,306 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
         const int blk = BIG ? (role == 1 ? lane & (NB - 1) : (lane >> 1) & (NB - 1))
                             : (is_v ? (lane - K_LANES) & (NB - 1) : (lane >> 1) & (NB - 1));
         const int opnd = lane & 1;
-        auto block_id = [&](int jj) -> int32_t {
-            const int b = (j0 + jj) * (BN / BS) + blk;
-            return (!FP8 && lane < BOX_LANES && jj < T && b < nblk) ? __ldg(bt + b) : -1;
-        };
-        int32_t next_id = block_id(0);
-        for (int jj = 0; jj < T && !FP8; ++jj) {
-            const int st = jj % KV_STAGES;
-            const int32_t id = next_id;
-            next_id = block_id(jj + 1);
-            if (jj >= KV_STAGES && !wait_w(bar(B_KVE + st), ((jj - KV_STAGES) / KV_STAGES) & 1)) break;
-            const int j = j0 + jj;
-            const bool in = lane < BOX_LANES && j * (BN / BS) + blk < nblk;
-            const bool valid = in && id >= 0 && id < p.num_blocks;
-            if (in && !valid && is_v) flag(ST_BAD_BLOCK);
-            const unsigned vm = __ballot_sync(0xffffffffu, valid);
-            if (lane == 0 && role == 0) {
-                fence_proxy_async_smem();
-                constexpr unsigned K_MASK = (1u << K_LANES) - 1u;
-                // BIG: the V warp loads one 4 KiB box per valid block (2 K lanes each)
-                const unsigned vbytes = BIG ? __popc(vm & K_MASK & 0x55555555u) * 4096 : __popc(vm & ~K_MASK) * 4096;
-                mbar_arrive_expect_tx(bar(B_KVF + st), __popc(vm & K_MASK) * 2048 + vbytes);
-            }
-            __syncwarp();
-            if (valid) {
-                const int y = (id * p.hkv + g) * BS;
-                const uint32_t stg = sbase + SKV + st * KV_STAGE_BYTES;
-                if (is_v) tma_load_3d(stg + V_OFF + blk * 4096, &vmap, 0, y, 0, bar(B_KVF + st));
-                else tma_load_2d(stg + opnd * KV_HALF + blk * 2048, &kmap, opnd * 64, y, bar(B_KVF + st));
-            }
-            issued = jj + 1;
-            const int first = L - j * BN;            // first row of the tile at or past L
-            if (first < BN && role == 0) {
-                // keys >= L: their V rows may hold anything (never written, or not
-                // loaded); P is 0 there but 0 * NaN is NaN, so zero them once the
-                // tile has landed, before any PV product reads it
-                if (!wait_w(bar(B_KVF + st), (jj / KV_STAGES) & 1)) break;
-                const uint32_t vb = sbase + SKV + st * KV_STAGE_BYTES + V_OFF;
-                for (int c = lane; c < (BN - first) * 16; c += 32) {
-                    const int r = first + (c >> 4), h = (c >> 3) & 1, ch = c & 7;
-                    st_shared_v4(vb + (r >> 4) * 4096 + h * 2048 + (r & 15) * 128 + ch * 16, 0u, 0u, 0u, 0u);
+        // fp8 cache: lanes 0-7 each load one 2 KiB box per tile: lane = 2 x block + (K | V)
+        const int blk8 = (lane >> 1) & 3, kv = lane & 1;
+        int u = 0;          // K/V tiles issued so far: the position in the stage rings
+        int kq = 0;         // items whose Q tiles were loaded
+        bool failed = false;
+        // the work list (and everything before it on the stream) is complete;
+        // the other warps learn of each item through the slots, after this wait
+        griddep_wait();
+        for (int k = 0; !failed; ++k) {
+            ItemSlot it;
+            if (role == 0) {
+                const int sl = k % NSLOT;
+                if (k >= NSLOT && !wait_w(bar(B_IEMPTY + sl), (k / NSLOT - 1) & 1)) break;
+                // the next listed item (tile_prefix_kernel wrote all its fields);
+                // every listed partition is non-empty, but a CTA never trusts that
+                // to keep its pipelines in step
+                it.valid = 0;
+                while (true) {
+                    int idx = 0;
+                    if (lane == 0) idx = atomicAdd(p.order_count + 1, 1);
+                    idx = __shfl_sync(0xffffffffu, idx, 0);
+                    if (idx >= p.order_count[0]) break;
+                    const int4 e0 = p.order[2 * idx], e1 = p.order[2 * idx + 1];
+                    it.s = e0.x;
+                    it.row0 = e0.y;
+                    it.n = e0.z;
+                    it.L = e0.w;
+                    it.j0 = e1.x;
+                    it.T = e1.y & 0xffff;
+                    it.nsplit = (int)((unsigned)e1.y >> 16);
+                    it.g = e1.z & 0xffff;
+                    it.split = (int)((unsigned)e1.z >> 16);
+                    it.t0q = e1.w & ((1 << 30) - 1);
+                    it.has1 = (e1.w >> 30) & 1;
+                    if (it.T > 0) {
+                        it.valid = 1;
+                        break;
+                    }
                 }
-                fence_proxy_async_smem();
+                if (lane == 0) {
+                    slots[sl].s = it.s;
+                    slots[sl].row0 = it.row0;
+                    slots[sl].n = it.n;
+                    slots[sl].L = it.L;
+                    slots[sl].t0q = it.t0q;
+                    slots[sl].has1 = it.has1;
+                    slots[sl].j0 = it.j0;
+                    slots[sl].T = it.T;
+                    slots[sl].nsplit = it.nsplit;
+                    slots[sl].g = it.g;
+                    slots[sl].split = it.split;
+                    slots[sl].valid = it.valid;
+                    mbar_arrive(bar(B_IFULL + sl));
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_TAIL));
+                if (!it.valid) break;
+                // Q of the item, once every QK^T product of the item before finished
+                if (kq > 0 && !wait_w(bar(B_QFREE), (kq - 1) & 1)) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(B_Q), (it.has1 ? 4 : 2) * 16384);
+                    for (int gi = 0; gi < (it.has1 ? 2 : 1); ++gi) {
+                        const int zq = it.row0 + (it.t0q + gi) * tpt;
+                        tma_load_3d(sbase + SQ + gi * Q_TILE, &qmap, 0, it.g * G, zq, bar(B_Q));
+                        tma_load_3d(sbase + SQ + gi * Q_TILE + 16384, &qmap, 64, it.g * G, zq, bar(B_Q));
+                    }
+                }
+                ++kq;
+            } else if (!read_item(k, it)) {
+                break;
+            }
+            const int32_t *bt = p.block_tables + (size_t)it.s * p.max_blocks;
+            const int nblk = (it.L + BS - 1) / BS;
+            const int j0 = it.j0, T = it.T, L = it.L;
+            if constexpr (FP8) {
+                // e4m3 K and V of each block (one 2 KiB box each) into a staging stage;
+                // the widening warps turn it into the operand tiles.  The block ids of
+                // the next tile are read during the wait for a free stage.
+                auto block_id8 = [&](int jj) -> int32_t {
+                    const int b = (j0 + jj) * (BN / BS) + blk8;
+                    return (lane < 8 && jj < T && b < nblk) ? __ldg(bt + b) : -1;
+                };
+                int32_t next_id = block_id8(0);
+                for (int jj = 0; jj < T; ++jj, ++u) {
+                    const int st = u % F8_STAGES;
+                    const int32_t id = next_id;
+                    next_id = block_id8(jj + 1);
+                    if (u >= F8_STAGES && !wait_w(bar(B_F8E + st), ((u - F8_STAGES) / F8_STAGES) & 1)) {
+                        failed = true;
+                        break;
+                    }
+                    const int j = j0 + jj;
+                    const bool in = lane < 8 && j * (BN / BS) + blk8 < nblk;
+                    const bool valid = in && id >= 0 && id < p.num_blocks;
+                    if (in && !valid && kv == 0) flag(ST_BAD_BLOCK);
+                    const unsigned vm = __ballot_sync(0xffffffffu, valid);
+                    if (lane == 0) {
+                        fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(bar(B_F8F + st), __popc(vm) * 2048);
+                    }
+                    __syncwarp();
+                    if (valid) {
+                        const int y = (id * p.hkv + it.g) * BS;
+                        const uint32_t dst = sbase + LY::SF8 + st * F8_STAGE_BYTES + kv * F8_V_OFF + blk8 * 2048;
+                        tma_load_2d(dst, kv ? &vmap : &kmap, 0, y, bar(B_F8F + st));
+                    }
+                }
+            } else {
+                auto block_id = [&](int jj) -> int32_t {
+                    const int b = (j0 + jj) * (BN / BS) + blk;
+                    return (lane < BOX_LANES && jj < T && b < nblk) ? __ldg(bt + b) : -1;
+                };
+                int32_t next_id = block_id(0);
+                for (int jj = 0; jj < T; ++jj, ++u) {
+                    const int st = u % KV_STAGES;
+                    const int32_t id = next_id;
+                    next_id = block_id(jj + 1);
+                    if (u >= KV_STAGES && !wait_w(bar(B_KVE + st), ((u - KV_STAGES) / KV_STAGES) & 1)) {
+                        failed = true;
+                        break;
+                    }
+                    const int j = j0 + jj;
+                    const bool in = lane < BOX_LANES && j * (BN / BS) + blk < nblk;
+                    const bool valid = in && id >= 0 && id < p.num_blocks;
+                    if (in && !valid && is_v) flag(ST_BAD_BLOCK);
+                    const unsigned vm = __ballot_sync(0xffffffffu, valid);
+                    if (lane == 0 && role == 0) {
+                        fence_proxy_async_smem();
+                        constexpr unsigned K_MASK = (1u << K_LANES) - 1u;
+                        // BIG: the V warp loads one 4 KiB box per valid block (2 K lanes each)
+                        const unsigned vbytes =
+                            BIG ? __popc(vm & K_MASK & 0x55555555u) * 4096 : __popc(vm & ~K_MASK) * 4096;
+                        mbar_arrive_expect_tx(bar(B_KVF + st), __popc(vm & K_MASK) * 2048 + vbytes);
+                    }
+                    __syncwarp();
+                    if (valid) {
+                        const int y = (id * p.hkv + it.g) * BS;
+                        const uint32_t stg = sbase + SKV + st * KV_STAGE_BYTES;
+                        if (is_v) tma_load_3d(stg + V_OFF + blk * 4096, &vmap, 0, y, 0, bar(B_KVF + st));
+                        else tma_load_2d(stg + opnd * KV_HALF + blk * 2048, &kmap, opnd * 64, y, bar(B_KVF + st));
+                    }
+                    const int first = L - j * BN;            // first row of the tile at or past L
+                    if (first < BN && role == 0) {
+                        // keys >= L: their V rows may hold anything (never written, or not
+                        // loaded); P is 0 there but 0 * NaN is NaN, so zero them once the
+                        // tile has landed, before any PV product reads it
+                        if (!wait_w(bar(B_KVF + st), (u / KV_STAGES) & 1)) {
+                            failed = true;
+                            ++u;
+                            break;
+                        }
+                        const uint32_t vb = sbase + SKV + st * KV_STAGE_BYTES + V_OFF;
+                        for (int c = lane; c < (BN - first) * 16; c += 32) {
+                            const int r = first + (c >> 4), h = (c >> 3) & 1, ch = c & 7;
+                            st_shared_v4(vb + (r >> 4) * 4096 + h * 2048 + (r & 15) * 128 + ch * 16, 0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(B_TAIL + st));
+                    }
+                }
             }
         }
-        if (!FP8 && *abort_flag) {
+        if (*abort_flag) {
             // let loads already in flight land before the CTA exits
-            for (int jj = max(0, issued - KV_STAGES); jj < issued; ++jj)
-                (void)mbar_wait_bounded(bar(B_KVF + jj % KV_STAGES), (jj / KV_STAGES) & 1);
+            constexpr int RING = FP8 ? F8_STAGES : KV_STAGES;
+            for (int uu = max(0, u - RING); uu < u; ++uu)
+                (void)mbar_wait_bounded(bar((FP8 ? B_F8F : B_KVF) + uu % RING), (uu / RING) & 1);
+            if (role == 0 && kq > 0) (void)mbar_wait_bounded(bar(B_Q), (kq - 1) & 1);
         }
     } else if (warp >= LY::W_MMA && warp < LY::W_MMA + LY::NG) {
         // ======================= MMA issuers: one warp per query tile
         const int gi = warp - LY::W_MMA;
-        if (gi == 0 || has1) {
-            // shared-memory descriptors of stage 0; other stages and K steps are
-            // constant byte offsets added to the start-address field (in 16-byte
-            // units; shared memory is < 256 KiB, so the 14-bit field never carries)
-            const uint64_t qdesc = sdesc_sw128(sbase + SQ + gi * Q_TILE, 16, 1024);
-            const uint64_t kdesc0 = sdesc_sw128(sbase + SKV, 16, 1024);
-            // V: bf16 cache [block][64-dim half][16 keys] (one 3-D box per block); fp8
-            // cache [half][block][16 keys] (written by the widening warps)
-            constexpr uint32_t V_LBO = FP8 ? KV_HALF : 2048, V_KSTEP = FP8 ? 2048 : 4096;
-            const uint64_t vdesc0 = sdesc_sw128(sbase + SKV + V_OFF, V_LBO, 1024);
-            const uint32_t to = tO(gi);
-            // S = Q K^T for KV tile jj into S buffer jj % 2: A = Q, B = K (K-major)
-            auto issue_s = [&](int jj) {
+        // shared-memory descriptors of stage 0; other stages and K steps are
+        // constant byte offsets added to the start-address field (in 16-byte
+        // units; shared memory is < 256 KiB, so the 14-bit field never carries)
+        const uint64_t qdesc = sdesc_sw128(sbase + SQ + gi * Q_TILE, 16, 1024);
+        const uint64_t kdesc0 = sdesc_sw128(sbase + SKV, 16, 1024);
+        // V: bf16 cache [block][64-dim half][16 keys] (one 3-D box per block); fp8
+        // cache [half][block][16 keys] (written by the widening warps)
+        constexpr uint32_t V_LBO = FP8 ? KV_HALF : 2048, V_KSTEP = FP8 ? 2048 : 4096;
+        const uint64_t vdesc0 = sdesc_sw128(sbase + SKV + V_OFF, V_LBO, 1024);
+        const uint32_t to = tO(gi);
+        // running positions, carried across items: the stage and phase parity of
+        // the next K/V tile; the S buffer and its phase parity of this group's next
+        // tile; items the group computed (drain and fp8 Q phases)
+        int stg = 0;
+        uint32_t kph = 0;
+        int sbuf = 0;
+        uint32_t sph = 0;
+        int kg = 0;
+        unsigned tailpar = 0;   // phase parity of each stage's tail barrier
+        auto adv = [](int &st, uint32_t &ph) {
+            if (++st == KV_STAGES) {
+                st = 0;
+                ph ^= 1u;
+            }
+        };
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            ItemSlot it;
+            if (!read_item(k, it)) break;
+            const int T = it.T;
+            const int st0 = stg;
+            const uint32_t ph0 = kph;
+            {   // the ring position after the item's tiles
+                const int tot = stg + T;
+                stg = tot % KV_STAGES;
+                kph ^= (uint32_t)(tot / KV_STAGES) & 1u;
+            }
+            // the tail tile (if any) is the item's last; both issuers follow its parity
+            const int tail_st = (st0 + T - 1) % KV_STAGES;
+            const bool tail = !FP8 && has_tail(it);
+            if (gi == 1 && !it.has1) {                 // no second query tile in this item
+                if (tail) tailpar ^= 1u << tail_st;
+                continue;
+            }
+            // the partner issuer's releases, when the item has no second query tile
+            const bool rel2 = LY::NG == 2 && !it.has1;
+            // S = Q K^T for the tile in stage st into S buffer b: A = Q, B = K (K-major)
+            auto issue_s = [&](int st, int b, bool last) {
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint64_t kd = kdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
-                    const uint32_t ts = tS(gi, jj & 1);
+                    const uint64_t kd = kdesc0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4);
+                    const uint32_t ts = tS(gi, b);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)   // D = 128 in steps of 16: 4 per 64-wide half
                         umma_f16(ts, qdesc + (uint64_t)((((kk >> 2) * 16384) + (kk & 3) * 32) >> 4),
                                  kd + (uint64_t)((((kk >> 2) * KV_HALF) + (kk & 3) * 32) >> 4),
                                  FP8 ? IDESC_S16 : (BIG ? IDESC_S128 : IDESC_S), kk > 0);
-                    umma_commit(bar(B_S + 2 * gi + (jj & 1)));
+                    umma_commit(bar(B_S + 2 * gi + b));
+                    if (last) {
+                        // the item's last QK^T product: its Q tiles may be replaced once done
+                        umma_commit(bar(B_QFREE));
+                        if (rel2) umma_commit(bar(B_QFREE));
+                    }
                 }
                 __syncwarp();
             };
-            // O += P V for KV tile jj: A = P from TMEM, B = V (MN-major) from smem
-            auto issue_pv = [&](int jj) {
+            // O += P V for the tile in stage st: A = P from TMEM (S buffer b), B = V
+            // (MN-major) from smem
+            auto issue_pv = [&](int st, int b, bool first) {
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint64_t vd = vdesc0 + (uint64_t)(((jj % KV_STAGES) * KV_STAGE_BYTES) >> 4);
-                    const uint32_t ts = tS(gi, jj & 1);
+                    const uint64_t vd = vdesc0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4);
+                    const uint32_t ts = tS(gi, b);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)   // the tile's keys in steps of 16
                         umma_f16_ts(to, ts + kk * 8, vd + (uint64_t)((kk * V_KSTEP) >> 4), FP8 ? IDESC_PV16 : IDESC_PV,
-                                    (jj > 0 || kk > 0) ? 1u : 0u);
+                                    (first && kk == 0) ? 0u : 1u);
                     umma_commit(bar(B_PVD + gi));
                     // the stage is released once both issuers' MMAs reading it are done
-                    umma_commit(bar(B_KVE + jj % KV_STAGES));
+                    umma_commit(bar(B_KVE + st));
+                    if (rel2) umma_commit(bar(B_KVE + st));
                 }
                 __syncwarp();
             };
-            // a tile holding keys >= L is read by PV only after the producer zeroed them
-            // (fp8 cache: the widening warps write those rows as zeros)
-            auto tail_ready = [&](int jj) -> bool {
-                return FP8 || (j0 + jj + 1) * BN <= L || wait_w(bar(B_TAIL), 0);
-            };
             // S of the first two tiles up front; afterwards S(jj+2) follows PV(jj), so
-            // each softmax finds its S computed while it worked on the tile before
+            // each softmax finds its S computed while it worked on the tile before.
+            // PV(jj-2) of the item before (or of this one) read the S buffer that
+            // S(jj) overwrites; this thread issued it first, and P(jj-2) had arrived.
             // fp8 cache: Q is used once the softmax warps have turned it into f16
-            bool ok = FP8 ? wait_w(bar(B_QC + gi), 0) : wait_w(bar(B_Q), 0);
+            ok = FP8 ? wait_w(bar(B_QC + gi), kg & 1) : wait_w(bar(B_Q), k & 1);
+            int sx = st0;                              // the next tile to compute S for
+            uint32_t px = ph0;                         // its KVF phase parity
             for (int jj = 0; ok && jj < min(2, T); ++jj) {
-                if (!wait_w(bar(B_KVF + jj), 0)) { ok = false; break; }
-                issue_s(jj);
+                if (!wait_w(bar(B_KVF + sx), px)) { ok = false; break; }
+                issue_s(sx, sbuf ^ jj, jj == T - 1);
+                adv(sx, px);
             }
+            int spv = st0;                             // the PV tile's stage
             for (int jj = 0; jj < T && ok; ++jj) {
-                if (!wait_w(bar(B_P + 2 * gi + (jj & 1)), (jj >> 1) & 1) || !tail_ready(jj)) { ok = false; break; }
-                // in issue order: PV(jj) reads P from S buffer jj % 2 before S(jj+2)
-                // overwrites it
-                issue_pv(jj);
-                if (jj + 2 < T) {
-                    const int sn = (jj + 2) % KV_STAGES;
-                    if (!wait_w(bar(B_KVF + sn), ((jj + 2) / KV_STAGES) & 1)) { ok = false; break; }
-                    issue_s(jj + 2);
+                if (!wait_w(bar(B_P + 2 * gi + sbuf), sph)) { ok = false; break; }
+                // a tile holding keys >= L is read by PV only after the producer zeroed
+                // them (fp8 cache: the widening warps write those rows as zeros)
+                if (tail && jj == T - 1) {
+                    if (!wait_w(bar(B_TAIL + tail_st), (tailpar >> tail_st) & 1)) { ok = false; break; }
+                    tailpar ^= 1u << tail_st;
                 }
+                // in issue order: PV(jj) reads P from its S buffer before S(jj+2)
+                // overwrites it
+                issue_pv(spv, sbuf, jj == 0);
+                if (jj + 2 < T) {
+                    if (!wait_w(bar(B_KVF + sx), px)) { ok = false; break; }
+                    issue_s(sx, sbuf, jj + 2 == T - 1);
+                    adv(sx, px);
+                }
+                if (++spv == KV_STAGES) spv = 0;
+                sbuf ^= 1;
+                if (sbuf == 0) sph ^= 1u;
             }
-            // every MMA this issuer started has finished before TMEM is released
+            // the item's every MMA finished: the softmax warps may read O
             if (lane == 0) umma_commit(bar(B_DRAIN + gi));
             __syncwarp();
-            (void)mbar_wait_bounded(bar(B_DRAIN + gi), 0);
+            ++kg;
         }
+        // every MMA this issuer started has finished before TMEM is released: its
+        // last item's drain phase (a further commit could complete together with
+        // that phase while the softmax warps still wait on it, and the two phases
+        // would alias their parity)
+        if (kg > 0) (void)mbar_wait_bounded(bar(B_DRAIN + gi), (kg - 1) & 1);
     } else if (warp >= LY::W_WIDEN) {
         // ======================= fp8 cache: widen each e4m3 K/V tile to f16 operand
         // tiles (exact), in the operand stages' 128-byte-swizzled layout; keys at
@@ -632,63 +952,82 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
             // swizzle XORs the chunk with the key's low 3 bits)
             const int ct = threadIdx.x - LY::W_WIDEN * 32;      // 0..127
             const int row = ct & (BN - 1), c0 = ct >> 6;
-            const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks;
-            // the row's key of tile jj lies inside the context and its block in the
-            // pool (read one tile ahead, during the waits)
-            auto row_ok = [&](int jj) -> bool {
-                const int key = (j0 + jj) * BN + row;
-                if (jj >= T || key >= L) return false;
-                const int32_t id = __ldg(bt + key / BS);
-                return id >= 0 && id < p.num_blocks;
-            };
-            bool next_ok = row_ok(0);
-            for (int jj = 0; jj < T; ++jj) {
-                const int s8 = jj % F8_STAGES, st = jj % KV_STAGES;
-                const bool valid = next_ok;
-                next_ok = row_ok(jj + 1);
-                if (!wait_w(bar(B_F8F + s8), (jj / F8_STAGES) & 1)) break;
-                if (jj >= KV_STAGES && !wait_w(bar(B_KVE + st), ((jj - KV_STAGES) / KV_STAGES) & 1)) break;
-                const uint32_t src = sbase + LY::SF8 + s8 * F8_STAGE_BYTES + row * 128;
-                const uint32_t dst = sbase + SKV + st * KV_STAGE_BYTES + row * 128;
-                // all eight 16-byte loads first, then the conversions and stores
-                uint32_t w[2][4][4];
-#pragma unroll
-                for (int which = 0; which < 2; ++which)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int c = c0 + 2 * k;
-                        if (valid)
-                            lds128(src + which * F8_V_OFF + ((c ^ (row & 7)) << 4), w[which][k][0], w[which][k][1],
-                                   w[which][k][2], w[which][k][3]);
-                        else
-                            w[which][k][0] = w[which][k][1] = w[which][k][2] = w[which][k][3] = 0u;
+            int u = 0;      // tiles of the CTA's items so far: the stage ring positions
+            bool failed = false;
+            for (int k = 0; !failed; ++k) {
+                ItemSlot it;
+                if (!read_item(k, it)) break;
+                const int32_t *bt = p.block_tables + (size_t)it.s * p.max_blocks;
+                const int j0 = it.j0, T = it.T, L = it.L;
+                // the row's key of tile jj lies inside the context and its block in the
+                // pool (read one tile ahead, during the waits)
+                auto row_ok = [&](int jj) -> bool {
+                    const int key = (j0 + jj) * BN + row;
+                    if (jj >= T || key >= L) return false;
+                    const int32_t id = __ldg(bt + key / BS);
+                    return id >= 0 && id < p.num_blocks;
+                };
+                bool next_ok = row_ok(0);
+                for (int jj = 0; jj < T; ++jj, ++u) {
+                    const int s8 = u % F8_STAGES, st = u % KV_STAGES;
+                    const bool valid = next_ok;
+                    next_ok = row_ok(jj + 1);
+                    if (!wait_w(bar(B_F8F + s8), (u / F8_STAGES) & 1) ||
+                        (u >= KV_STAGES && !wait_w(bar(B_KVE + st), ((u - KV_STAGES) / KV_STAGES) & 1))) {
+                        failed = true;
+                        break;
                     }
+                    const uint32_t src = sbase + LY::SF8 + s8 * F8_STAGE_BYTES + row * 128;
+                    const uint32_t dst = sbase + SKV + st * KV_STAGE_BYTES + row * 128;
+                    // all eight 16-byte loads first, then the conversions and stores
+                    uint32_t w[2][4][4];
 #pragma unroll
-                for (int which = 0; which < 2; ++which)
+                    for (int which = 0; which < 2; ++which)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int c = c0 + 2 * k;
-                        const uint32_t base = dst + which * V_OFF + (c >> 2) * KV_HALF;
-                        const int q0 = (2 * c) & 7, q1 = (2 * c + 1) & 7;   // d 16c .. +7 and 16c+8 .. +15
-                        const uint32_t *x = w[which][k];
-                        st_shared_v4(base + ((q0 ^ (row & 7)) << 4), e4m3x2_to_f16x2(x[0] & 0xffffu),
-                                     e4m3x2_to_f16x2(x[0] >> 16), e4m3x2_to_f16x2(x[1] & 0xffffu),
-                                     e4m3x2_to_f16x2(x[1] >> 16));
-                        st_shared_v4(base + ((q1 ^ (row & 7)) << 4), e4m3x2_to_f16x2(x[2] & 0xffffu),
-                                     e4m3x2_to_f16x2(x[2] >> 16), e4m3x2_to_f16x2(x[3] & 0xffffu),
-                                     e4m3x2_to_f16x2(x[3] >> 16));
-                    }
-                fence_proxy_async_smem();
-                mbar_arrive(bar(B_KVF + st));
-                mbar_arrive(bar(B_F8E + s8));
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const int c = c0 + 2 * kk;
+                            if (valid)
+                                lds128(src + which * F8_V_OFF + ((c ^ (row & 7)) << 4), w[which][kk][0],
+                                       w[which][kk][1], w[which][kk][2], w[which][kk][3]);
+                            else
+                                w[which][kk][0] = w[which][kk][1] = w[which][kk][2] = w[which][kk][3] = 0u;
+                        }
+#pragma unroll
+                    for (int which = 0; which < 2; ++which)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const int c = c0 + 2 * kk;
+                            const uint32_t base = dst + which * V_OFF + (c >> 2) * KV_HALF;
+                            const int q0 = (2 * c) & 7, q1 = (2 * c + 1) & 7;   // d 16c .. +7 and 16c+8 .. +15
+                            const uint32_t *x = w[which][kk];
+                            st_shared_v4(base + ((q0 ^ (row & 7)) << 4), e4m3x2_to_f16x2(x[0] & 0xffffu),
+                                         e4m3x2_to_f16x2(x[0] >> 16), e4m3x2_to_f16x2(x[1] & 0xffffu),
+                                         e4m3x2_to_f16x2(x[1] >> 16));
+                            st_shared_v4(base + ((q1 ^ (row & 7)) << 4), e4m3x2_to_f16x2(x[2] & 0xffffu),
+                                         e4m3x2_to_f16x2(x[2] >> 16), e4m3x2_to_f16x2(x[3] & 0xffffu),
+                                         e4m3x2_to_f16x2(x[3] >> 16));
+                        }
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(B_KVF + st));
+                    mbar_arrive(bar(B_F8E + s8));
+                }
             }
         }
     } else {
         // ======================= softmax warpgroups: thread = query row = TMEM lane
         const int gi = warp >> 2;                  // which query tile of the pair
-        if (gi == 0 || has1) {
-            const int r = threadIdx.x - gi * 128;  // row of the tile, 0..127
-            const int i0 = (t0q + gi) * tpt, i1 = min(n, i0 + tpt);
+        const int r = threadIdx.x - gi * 128;      // row of the tile, 0..127
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        int cs = 0;         // tiles the group computed: S buffers, P and PV phases
+        int kg = 0;         // items the group computed: drain (and fp8 Q) phases
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            ItemSlot it;
+            if (!read_item(k, it)) break;
+            if (gi == 1 && !it.has1) continue;     // no second query tile in this item
+            const int n = it.n, L = it.L, j0 = it.j0, T = it.T, g = it.g, row0 = it.row0;
+            const int split = it.split, nsplit = it.nsplit;
+            const int i0 = (it.t0q + gi) * tpt, i1 = min(n, i0 + tpt);
             const int i = i0 + r / G;
             const int head = g * G + r % G;
             const bool row_valid = i < i1;
@@ -697,16 +1036,14 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
             // sees a key at or beyond L
             const int pos = row_valid ? L - n + i : L - n + i1 - 1;
             const int pos_min = L - n + i0;
-            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
             float m_ref = -INFINITY, l = 0.f;
-            bool ok = true;
             // fp8 cache: the k scale folds into the softmax scale, the v scale into O
             const float sl = FP8 ? p.scale_log2 * __ldg(p.k_scale + g) : p.scale_log2;
             const float vsc = FP8 ? __ldg(p.v_scale + g) : 1.f;
             if constexpr (FP8) {
                 // the group's Q tile, bf16 -> f16 in place (exact for these values'
                 // range but the smallest subnormals), before its first product
-                ok = wait_w(bar(B_Q), 0);
+                ok = wait_w(bar(B_Q), k & 1);
                 if (ok) {
                     const uint32_t qt = sbase + SQ + gi * Q_TILE;
                     for (int c = r; c < Q_TILE / 16; c += 128) {
@@ -723,12 +1060,13 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
             }
             for (int jj = 0; jj < T && ok; ++jj) {
                 const int t0 = (j0 + jj) * BN;
-                if (!wait_w(bar(B_S + 2 * gi + (jj & 1)), (jj >> 1) & 1)) { ok = false; break; }
+                const int sb = (cs + jj) & 1;           // the tile's S buffer
+                if (!wait_w(bar(B_S + 2 * gi + sb), ((cs + jj) >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 float sv[BN];
 #pragma unroll
                 for (int h = 0; h < BN / 64; ++h)
-                    tmem_ld64(tS(gi, jj & 1) + lane_base + 64 * h, *reinterpret_cast<float(*)[64]>(sv + 64 * h));
+                    tmem_ld64(tS(gi, sb) + lane_base + 64 * h, *reinterpret_cast<float(*)[64]>(sv + 64 * h));
                 // raw scores; the scale (> 0) is applied inside the exponent's FFMA,
                 // so the max is taken on the raw values
                 if (t0 + BN - 1 > pos_min) {             // diagonal tile: causal mask
@@ -777,7 +1115,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
                 // rescaled only once PV(jj-1) has accumulated into it; PV(jj) waits
                 // for this warp's P, so it cannot start before the rescale is done.
                 if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                    if (!wait_w(bar(B_PVD + gi), (jj - 1) & 1)) { ok = false; break; }
+                    if (!wait_w(bar(B_PVD + gi), (cs + jj - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -792,17 +1130,19 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
                 // operand of PV)
 #pragma unroll
                 for (int h = 0; h < BN / 64; ++h)
-                    tmem_st32u(tS(gi, jj & 1) + lane_base + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(pw + 32 * h));
+                    tmem_st32u(tS(gi, sb) + lane_base + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(pw + 32 * h));
                 tmem_wait_st();
                 tc_fence_before();
                 // one P barrier per S buffer: a warp reaches buffer b's next phase only
                 // after S(jj+2) completed, which the issuer started only once all 128
                 // rows had arrived for this phase -- arrivals never mix two tiles
-                mbar_arrive(bar(B_P + 2 * gi + (jj & 1)));
+                mbar_arrive(bar(B_P + 2 * gi + sb));
             }
-            // every MMA of the group has finished (a one-phase barrier: PV(T-2) may
-            // still run here, so a parity wait on the per-tile barrier could alias)
-            if (ok && wait_w(bar(B_DRAIN + gi), 0)) {
+            // every MMA of the group's item has finished (the issuer's per-item drain
+            // commit: PV(T-2) may still run here, so a parity wait on the per-tile
+            // barrier could alias)
+            if (ok && !wait_w(bar(B_DRAIN + gi), kg & 1)) ok = false;
+            if (ok) {
                 tc_fence_after();
                 const size_t rh = (size_t)(row0 + (row_valid ? i : i0)) * p.hq + head;
                 const size_t pi = rh * p.max_splits + split;
@@ -824,6 +1164,8 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
                     p.part_ml[pi * 2 + 1] = l;
                 }
             }
+            cs += T;
+            ++kg;
         }
     }
     tc_fence_before();
@@ -833,34 +1175,23 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
 }
 
 // Log-sum-exp merge of prefill partitions: one warp per (query row, head).
+// (grid-stride; nothing to do when tile_prefix_kernel cut no key range)
 __global__ void __launch_bounds__(128) prefill_reduce_kernel(const PrefillParams p)
 {
-    const long wid = (long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    griddep_wait();   // launched with programmatic serialisation after the chunk kernel
+    if (p.order_count[2] == 0) return;
     const int lane = threadIdx.x & 31;
-    if (wid >= (long)p.total_rows * p.hq) return;
-    const int row = (int)(wid / p.hq), h = (int)(wid % p.hq);
-    if (row >= p.cu_q_lens[p.num_seqs]) return;
-    int lo = 0, hi = p.num_seqs;                  // cu[lo] <= row < cu[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (p.cu_q_lens[mid] <= row) lo = mid;
-        else hi = mid;
+    const long nw = (long)p.total_rows * p.hq;
+    for (long wid = (long)blockIdx.x * 4 + (threadIdx.x >> 5); wid < nw; wid += (long)gridDim.x * 4) {
+        const int row = (int)(wid / p.hq), h = (int)(wid % p.hq);
+        // the partitions of the query item the row belongs to (tile_prefix_kernel
+        // wrote them; 0 for rows outside any chunk)
+        const int ns = min(p.row_info[row], p.max_splits);
+        if (ns <= 1) continue;
+        const size_t base = ((size_t)row * p.hq + h) * p.max_splits;
+        reinterpret_cast<float4 *>(p.out + ((size_t)row * p.hq + h) * D)[lane] =
+            lse_merge_warp(p.part_ml + base * 2, p.part_o + base * D, ns, lane);
     }
-    const int s = lo;
-    const int row0 = p.cu_q_lens[s], n = p.cu_q_lens[s + 1] - row0, L = p.context_lens[s];
-    if (n < 2 || L < n || L > p.max_blocks * BS) return;
-    const int tpt = BM / p.group;
-    const int i = row - row0, mt = i / tpt;
-    // the CTA that computed this row covered the key range of its query tiles
-    const int tiles = (n + tpt - 1) / tpt;
-    const int last = min(tiles - 1, (mt / p.item_tiles) * p.item_tiles + p.item_tiles - 1);
-    const int i1 = min(n, (last + 1) * tpt);
-    const int KT = (L - n + i1 + p.tile_keys - 1) / p.tile_keys;
-    const int ns = (KT + p.tiles_per_split - 1) / p.tiles_per_split;
-    if (ns <= 1) return;
-    const size_t base = ((size_t)row * p.hq + h) * p.max_splits;
-    reinterpret_cast<float4 *>(p.out + ((size_t)row * p.hq + h) * D)[lane] =
-        lse_merge_warp(p.part_ml + base * 2, p.part_o + base * D, ns, lane);
 }
 
 constexpr int MAX_SPLIT_KEYS = 16384;           // keys per partition at most
@@ -871,7 +1202,7 @@ constexpr double CTA_FIXED_TILES = 4.0;        // a CTA's Q load, set-up and epi
 constexpr double BYTES_PER_TILE_TIME = 5.6e6;
 
 struct Plan {
-    size_t decode_bytes, part_o_off, part_ml_off, tile_off_off, order_off, total;
+    size_t decode_bytes, part_o_off, part_ml_off, tile_off_off, order_off, row_info_off, total;
     int max_splits, tiles_per_split;
     int64_t items_ub;    // bounds the query items: sum over chunks of ceil(n / tpt)
 };
@@ -958,13 +1289,15 @@ Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq,
     if (pl.max_splits > 1) off += up((size_t)total_q * hq * pl.max_splits * 2 * sizeof(float));
     pl.tile_off_off = off;
     if (max_q_len >= 2) off += up((size_t)(num_seqs + 1) * sizeof(int32_t));
-    // the work items in launch order (x, partition and head packed in an int2),
-    // then their count
+    // the work items in launch order (two int4 each), then their count and the
+    // CTAs' fetch counter; then each query row's partition count
     const int G = std::max(1, hq / std::max(1, hkv)), tpt = std::max(1, BM / G);
     pl.items_ub = ((int64_t)total_q + tpt - 1) / tpt + std::min<int64_t>(num_seqs, total_q / 2);
     pl.order_off = off;
     if (max_q_len >= 2)
-        off += up((size_t)pl.items_ub * hkv * std::max(1, pl.max_splits) * sizeof(int2)) + up(sizeof(int32_t));
+        off += up((size_t)pl.items_ub * hkv * std::max(1, pl.max_splits) * 2 * sizeof(int4)) + up(4 * sizeof(int32_t));
+    pl.row_info_off = off;
+    if (max_q_len >= 2) off += up((size_t)total_q * sizeof(int32_t));
     pl.total = off;
     return pl;
 }
@@ -1004,6 +1337,16 @@ struct SideStream {
 constexpr int MAX_DEVICES = 64;
 std::mutex g_side_mu;
 SideStream g_side[MAX_DEVICES];
+
+// SMs of the current device (the persistent chunk grid's size)
+int num_sms()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return (int)NUM_SMS;
+    return n;
+}
 
 SideStream *side_stream()
 {
@@ -1162,10 +1505,11 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     p.context_lens = context_lens;
     p.block_tables = block_tables;
     p.tile_off = reinterpret_cast<int32_t *>(ws + pl.tile_off_off);
-    p.order = reinterpret_cast<int2 *>(ws + pl.order_off);
+    p.order = reinterpret_cast<int4 *>(ws + pl.order_off);
+    p.row_info = reinterpret_cast<int32_t *>(ws + pl.row_info_off);
     p.items_cap = (int)std::min<int64_t>(pl.items_ub, INT32_MAX);
     p.order_count = reinterpret_cast<int32_t *>(
-        ws + pl.order_off + ((pl.items_ub * num_kv_heads * std::max(1, pl.max_splits) * sizeof(int2) + 255) & ~size_t(255)));
+        ws + pl.order_off + ((pl.items_ub * num_kv_heads * std::max(1, pl.max_splits) * 2 * sizeof(int4) + 255) & ~size_t(255)));
     p.part_o = pl.max_splits > 1 ? reinterpret_cast<float *>(ws + pl.part_o_off) : nullptr;
     p.part_ml = pl.max_splits > 1 ? reinterpret_cast<float *>(ws + pl.part_ml_off) : nullptr;
     p.max_blocks = max_blocks_per_seq;
@@ -1182,6 +1526,8 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     p.v_scale = v_scale;
     p.item_tiles = big ? 1 : 2;
     p.tile_keys = big ? 128 : 64;
+    p.num_sms = num_sms();
+    p.bytes_per_tile = (float)(BYTES_PER_TILE_TIME * p.tile_keys / 64.0);
     CUtensorMap qm, km, vm;
     const int tpt = BM / G;
     if (!pkv_host::encode_tmap_3d(&qm, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, num_q_heads, total_q_tokens,
@@ -1207,16 +1553,24 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     const int64_t ctas_ub = pl.items_ub * num_kv_heads * p.max_splits;
     if (ctas_ub > INT32_MAX || p.max_splits > 65535 || num_kv_heads > 65535) return KV_ERR_UNSUPPORTED;
     tile_prefix_kernel<<<1, 1024, 0, st>>>(p);
-    dim3 grid((unsigned)ctas_ub);
+    // persistent: one CTA per SM (a CTA holds a whole SM), at most one per work item
+    dim3 grid((unsigned)std::min<int64_t>(ctas_ub, num_sms()));
     Trace *tr = trace_for_call();
     if (tr) cudaEventRecord(tr->start, st);
+    // programmatic serialisation: the CTAs' set-up overlaps tile_prefix_kernel
+    // (trace events between the two only make the launch plain)
+    const bool pdl = !tr;
+    cudaError_t le;
     if (big)
-        prefill_kernel<false, true>
-            <<<grid, Lay<false, true>::THREADS, Lay<false, true>::SMEM_BYTES, st>>>(qm, km, vm, p);
+        le = pkv_host::launch_ex(prefill_kernel<false, true>, grid, dim3(Lay<false, true>::THREADS),
+                                 Lay<false, true>::SMEM_BYTES, st, pdl, qm, km, vm, p);
     else if (fp8)
-        prefill_kernel<true, false><<<grid, Lay<true>::THREADS, Lay<true>::SMEM_BYTES, st>>>(qm, km, vm, p);
+        le = pkv_host::launch_ex(prefill_kernel<true, false>, grid, dim3(Lay<true>::THREADS), Lay<true>::SMEM_BYTES,
+                                 st, pdl, qm, km, vm, p);
     else
-        prefill_kernel<false, false><<<grid, Lay<false>::THREADS, Lay<false>::SMEM_BYTES, st>>>(qm, km, vm, p);
+        le = pkv_host::launch_ex(prefill_kernel<false, false>, grid, dim3(Lay<false>::THREADS),
+                                 Lay<false>::SMEM_BYTES, st, pdl, qm, km, vm, p);
+    if (le != cudaSuccess) return KV_ERR_CUDA;
     if (tr) {
         cudaEventRecord(tr->stop, st);
         tr->recorded = true;
@@ -1224,8 +1578,10 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
     if (p.max_splits > 1) {
         const int64_t warps = (int64_t)total_q_tokens * num_q_heads;
-        prefill_reduce_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, st>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
+        if (pkv_host::launch_ex(prefill_reduce_kernel,
+                                dim3((unsigned)std::min<int64_t>((warps + 3) / 4, (int64_t)p.num_sms * 16)), dim3(128),
+                                0, st, !tr, p) != cudaSuccess)
+            return KV_ERR_CUDA;
     }
     return KV_OK;
 }
