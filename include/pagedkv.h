@@ -341,19 +341,25 @@ PAGEDKV_API kv_status paged_attention_decode_static_scratch(
  * (n_s >= 2) take the tensor-core (tcgen05) kernel, and the decode rows run on
  * a stream the library owns (one per device), forked from `stream` with an
  * event and joined back into it before the call returns: work enqueued on
- * `stream` afterwards sees the whole output.  Short chunks -- max_q_len x
- * (num_q_heads / num_kv_heads) <= 16, e.g. a speculative draft of 4 tokens
- * under a GQA group of 4 ([P3] speculative decoding, N = 4-8) -- run instead
- * with the whole batch in the decode kernel, whose CTA then covers all rows of
- * a sequence so each K/V tile is read once.  With an fp8 cache the chunks run
+ * `stream` afterwards sees the whole output.  When total_q_tokens = num_seqs x
+ * max_q_len every query is max_q_len rows long, so there are no decode rows and
+ * no side stream (a query of 1 row is then flagged as out of range).  Short
+ * chunks -- max_q_len x (num_q_heads / num_kv_heads) <= 8, e.g. a speculative
+ * draft of 2 tokens under a GQA group of 4 ([P3] speculative decoding) -- run
+ * instead with the whole batch in the decode kernel, whose CTA then covers all
+ * rows of a sequence so each K/V tile is read once; longer drafts (N = 4-8)
+ * take the tensor-core kernel.  With an fp8 cache the chunks run
  * on the tensor cores as well: each e4m3 K/V tile is widened exactly to f16
  * operands, Q is rounded to f16 once (the query range of the decode call above
  * applies), and the products accumulate in fp32.
- * A chunk's keys are cut into equal partitions of at most 16,384 keys, merged
- * with the same log-sum-exp reduction; the library picks their number from the
- * batch shape (num_splits applies to the decode rows), so a row's last bits
- * may differ between batches of different shapes, never with the physical
- * placement of the blocks.
+ * The tensor-core kernel runs one CTA per SM over a work list the library
+ * builds on the device (query tile, KV head and key partition, longest first).
+ * A chunk's keys are cut into equal partitions of at most 16,384 keys, or left
+ * whole, merged with the same log-sum-exp reduction; the library picks the
+ * partition length from the batch shape and the context lengths (num_splits
+ * applies to the decode rows), so a row's last bits may differ between batches
+ * of different shapes or lengths, never with the physical placement of the
+ * blocks.
  *
  *  out, q          device [total_q_tokens][num_q_heads][128] (fp32 / bf16)
  *  cu_q_lens       device int32 [num_seqs+1], cu_q_lens[0] = 0, non-decreasing,

@@ -173,6 +173,7 @@ struct PrefillParams {
     int tiles_per_split, max_splits;   // the shortest partition length allowed; room for partitions
     int num_sms;
     float bytes_per_tile;              // HBM bytes the GPU moves in one KV tile's time
+    int rows1;                         // the call runs decode rows (queries of 1); else a 1 is flagged
     int item_tiles;      // query tiles per CTA: 2 (a pair), or 1 (the 128-key layout)
     int tile_keys;       // keys per KV tile: 64, or 128 (the 128-key layout)
     float scale_log2;
@@ -280,6 +281,9 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     // the chunk kernel (launched with programmatic serialisation) may set up its
     // CTAs meanwhile; it waits for this grid before it reads the work list
     griddep_launch_dependents();
+    // (launched with programmatic serialisation itself when the caller's stream
+    // ran a kernel just before: nothing is read or written before this)
+    griddep_wait();
     const bool staged = p.num_seqs <= PREFIX_SMAX;
     const int tpt = BM / p.group, tk = p.tile_keys, tps0 = max(1, p.tiles_per_split);
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
             if (n >= 2) {
                 if (a < 0 || b > p.total_rows || L < n || L > p.max_blocks * BS) flag(ST_BAD_LEN);
                 else tiles = ((n + tpt - 1) / tpt + p.item_tiles - 1) / p.item_tiles;   // query items
-            } else if (n < 0) {
+            } else if (n < 0 || (n == 1 && !p.rows1)) {
                 flag(ST_BAD_LEN);
             }
             if (staged) {
@@ -466,9 +470,18 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         e1 = make_int4(wk.j0, wk.T | (wk.nsplit << 16), g | (split << 16), wk.t0q | (wk.has1 ? 1 << 30 : 0));
         return min(NBKT - 1, (int)(((long long)max(0, tps - wk.T) * NBKT) / tps));
     };
+    // (a warp's first 32 slots -- all of them in small batches -- are kept in
+    // registers for the second pass)
+    int4 f_e0 = make_int4(0, 0, 0, 0), f_e1 = f_e0;
+    int f_bk = -1;
     for (long long b0 = s0; b0 < s1; b0 += 32) {
         int4 e0, e1;
         const int bk = b0 + lane < s1 ? bucket_of(b0 + lane, e0, e1) : -1;
+        if (b0 == s0) {
+            f_e0 = e0;
+            f_e1 = e1;
+            f_bk = bk;
+        }
         const unsigned peers = __match_any_sync(0xffffffffu, bk);
         if (bk >= 0 && lane == __ffs(peers) - 1) cnt[w][bk] += __popc(peers);
         __syncwarp();
@@ -497,8 +510,8 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     __syncthreads();
     // ---- 4. the entries
     for (long long b0 = s0; b0 < s1; b0 += 32) {
-        int4 e0, e1;
-        const int bk = b0 + lane < s1 ? bucket_of(b0 + lane, e0, e1) : -1;
+        int4 e0 = f_e0, e1 = f_e1;
+        const int bk = b0 == s0 ? f_bk : (b0 + lane < s1 ? bucket_of(b0 + lane, e0, e1) : -1);
         const unsigned peers = __match_any_sync(0xffffffffu, bk);
         if (bk >= 0) {
             const int pos = bstart[bk] + cnt[w][bk] + __popc(peers & ((1u << lane) - 1u));
@@ -1306,10 +1319,11 @@ Plan make_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len, int32_t hq,
 // are memory-bound like decode: when every sequence's rows x the group's heads
 // fit in MULTI_MAX_COLS columns, the whole batch runs in the decode kernel's
 // multi-row mode, which streams each K/V tile once for all the rows of its
-// sequence.  Measured on GB300: one column group (16 columns) beats the
-// tensor-core kernel; several groups sharing tiles through L2 do not.
+// sequence.  That is up to one MMA column tile (8 columns); measured on GB300,
+// 16 columns (4-token drafts at G = 4) ran at 0.752 of HBM there against 0.775
+// in the persistent tensor-core kernel.
 #ifndef PKV_MULTI_MAX_COLS
-#define PKV_MULTI_MAX_COLS 16
+#define PKV_MULTI_MAX_COLS 8
 #endif
 constexpr int64_t MULTI_MAX_COLS = PKV_MULTI_MAX_COLS;
 
@@ -1432,11 +1446,12 @@ int32_t paged_attention_launch_count(int32_t num_seqs, int32_t total_q_tokens, i
     pkv_decode::plan_splits(max_blocks_per_seq, num_splits, num_seqs, num_q_heads, &pb, &s);
     const int32_t decode = 1 + (s > 1 ? 1 : 0);
     if (max_q_len < 2 || use_multi(max_q_len, num_q_heads, num_kv_heads)) return decode;
-    // the decode rows, the tile-count prefix, the chunk tiles and their merge
-    // (the plan of a bf16 cache)
+    // the decode rows (none when every query is max_q_len long), the work list,
+    // the chunk tiles and their merge (the plan of a bf16 cache)
     const Plan pl = make_plan(num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, max_blocks_per_seq,
                               num_splits, use_big(KV_BF16, max_q_len, num_q_heads, num_kv_heads));
-    return decode + 2 + (pl.max_splits > 1 ? 1 : 0);
+    const bool rows1 = (int64_t)total_q_tokens != (int64_t)num_seqs * max_q_len;
+    return (rows1 ? decode : 0) + 2 + (pl.max_splits > 1 ? 1 : 0);
 }
 
 kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32_t *cu_q_lens,
@@ -1483,18 +1498,30 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     };
     if (max_q_len < 2) return decode_rows(st, true);   // decode rows only
     // decode rows (n = 1) on the side stream, forked from and joined into the
-    // caller's stream; the chunk tiles run on the caller's stream meanwhile
-    std::lock_guard<std::mutex> side_lock(g_side_mu);
-    SideStream *side = side_stream();
-    if (!side) return KV_ERR_CUDA;
-    if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
-        return KV_ERR_CUDA;
-    kv_status rs = decode_rows(side->stream, false);   // fed by an event, not a kernel
-    if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return KV_ERR_CUDA;
+    // caller's stream; the chunk tiles run on the caller's stream meanwhile.
+    // There are none when total_q_tokens = num_seqs x max_q_len (every query is
+    // max_q_len long; tile_prefix_kernel flags a row of 1 then).
+    const bool rows1 = (int64_t)total_q_tokens != (int64_t)num_seqs * max_q_len;
+    std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
+    SideStream *side = nullptr;
+    kv_status rs = KV_OK;
+    if (rows1) {
+        side_lock.lock();
+        side = side_stream();
+        if (!side) return KV_ERR_CUDA;
+        if (cudaEventRecord(side->fork, st) != cudaSuccess ||
+            cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+            return KV_ERR_CUDA;
+        rs = decode_rows(side->stream, false);   // fed by an event, not a kernel
+        if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return KV_ERR_CUDA;
+    }
     struct Join {   // the caller's stream waits for the decode rows however this call ends
         cudaStream_t st;
         SideStream *side;
-        ~Join() { cudaStreamWaitEvent(st, side->join, 0); }
+        ~Join()
+        {
+            if (side) cudaStreamWaitEvent(st, side->join, 0);
+        }
     } join{st, side};
     if (rs != KV_OK) return rs;
     // prefill chunks (n >= 2)
@@ -1527,6 +1554,7 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     p.item_tiles = big ? 1 : 2;
     p.tile_keys = big ? 128 : 64;
     p.num_sms = num_sms();
+    p.rows1 = rows1 ? 1 : 0;
     p.bytes_per_tile = (float)(BYTES_PER_TILE_TIME * p.tile_keys / 64.0);
     CUtensorMap qm, km, vm;
     const int tpt = BM / G;
@@ -1552,7 +1580,8 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     // tile_prefix_kernel writes; the grid bounds their number
     const int64_t ctas_ub = pl.items_ub * num_kv_heads * p.max_splits;
     if (ctas_ub > INT32_MAX || p.max_splits > 65535 || num_kv_heads > 65535) return KV_ERR_UNSUPPORTED;
-    tile_prefix_kernel<<<1, 1024, 0, st>>>(p);
+    if (pkv_host::launch_ex(tile_prefix_kernel, dim3(1), dim3(1024), 0, st, !rows1, p) != cudaSuccess)
+        return KV_ERR_CUDA;
     // persistent: one CTA per SM (a CTA holds a whole SM), at most one per work item
     dim3 grid((unsigned)std::min<int64_t>(ctas_ub, num_sms()));
     Trace *tr = trace_for_call();

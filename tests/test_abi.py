@@ -218,21 +218,27 @@ def test_host_validation_before_launch():
 def test_launch_count_follows_the_plan():
     """The kernels a call enqueues, from the host plan alone: decode (+ merge
     when the context is partitioned), short chunks in the multi-row decode
-    mode, longer chunks adding the tile prefix, the chunk kernel and its merge."""
+    mode, longer chunks adding the work list, the chunk kernel and its merge --
+    and no decode rows when every query is max_q_len long."""
     n = pkv.paged_attention_launch_count
     assert n(0, 0, 1, 8, 2, 100, 0) == 0                  # nothing to do
     assert n(4, 4, 1, 8, 2, 1, 0) == 1                    # one block: one partition, no merge
     assert n(4, 4, 1, 8, 2, 100, 1) == 1                  # one forced partition
     assert n(4, 4, 1, 8, 2, 100, 4) == 2                  # four partitions: merge
-    assert n(4, 16, 4, 16, 4, 100, 1) == 1                # 4 rows x G 4 = 16 columns: multi-row mode
-    assert n(4, 16, 4, 16, 4, 100, 4) == 2
-    assert n(4, 20, 5, 16, 4, 60, 1) == 1 + 2             # 5 x 4 columns: chunk tiles; 960 keys, one partition
+    assert n(4, 8, 2, 16, 4, 100, 1) == 1                 # 2 rows x G 4 = 8 columns: multi-row mode
+    assert n(4, 8, 2, 16, 4, 100, 4) == 2
+    # 4 rows x G 4 = 16 columns: chunk tiles; 4 x 4 rows leave no decode rows
+    assert n(4, 16, 4, 16, 4, 60, 1) == 2                 # 960 keys: one partition
+    assert n(4, 17, 4, 16, 4, 60, 1) == 1 + 2             # 17 rows: a decode row too
+    assert n(4, 20, 5, 16, 4, 60, 1) == 2                 # 5 x 4 columns; 960 keys, one partition
     # a small batch shortens the chunk partitions to 1,024 keys: 1,600 keys take two
-    assert n(4, 20, 5, 16, 4, 100, 1) == 1 + 3
-    assert n(1, 100, 100, 8, 2, 1, 1) == 1 + 2            # 16 keys: one partition of the chunk's keys
+    assert n(4, 20, 5, 16, 4, 100, 1) == 3
+    assert n(1, 100, 100, 8, 2, 1, 1) == 2                # 16 keys: one partition of the chunk's keys
     # 32,768 keys exceed the longest chunk partition (16,384): the chunk merge runs
-    assert n(1, 100, 100, 8, 2, 2048, 1) == 1 + 3
-    assert n(1, 100, 100, 8, 2, 2048, 4) == 2 + 3
+    assert n(1, 100, 100, 8, 2, 2048, 1) == 3
+    assert n(1, 100, 100, 8, 2, 2048, 4) == 3             # (num_splits is for decode rows: none)
+    assert n(2, 101, 100, 8, 2, 2048, 1) == 1 + 3         # a decode row beside the chunk
+    assert n(2, 101, 100, 8, 2, 2048, 4) == 2 + 3
 
 
 def test_bounded_wait_selftest_refuses_bad_limits():

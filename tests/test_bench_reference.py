@@ -106,9 +106,9 @@ def test_launches_per_step_from_the_library_plan():
     from synth.workloads import make_workload
     expect = {"llama8b": 3,          # write, decode, LSE merge
               "tiny": 3,
-              "spec_verify": 3,      # write, multi-row decode, merge
-              "mixed_prefill": 6,    # write, decode rows + merge, tile prefix, chunk kernel, chunk merge
-              "spec_verify8": 6}
+              "spec_verify": 4,      # write, work list, chunk kernel, chunk merge (no decode rows)
+              "mixed_prefill": 6,    # write, decode rows + merge, work list, chunk kernel, chunk merge
+              "spec_verify8": 4}
     for name, n in expect.items():
         assert b._launches_per_step(pkv, make_workload(name)) == n, name
 

@@ -86,9 +86,10 @@ def test_decode_uses_each_heads_own_k_and_v_scale(hq, hkv, splits):
     _check(wl)
 
 
-@pytest.mark.parametrize("hq,hkv,n", [(8, 2, 2), (8, 2, 4), (32, 8, 4), (16, 8, 8)])
+@pytest.mark.parametrize("hq,hkv,n", [(8, 2, 2), (32, 8, 2), (16, 8, 4), (8, 8, 8), (8, 2, 4), (16, 8, 8)])
 def test_multi_row_mode_uses_each_heads_own_k_and_v_scale(hq, hkv, n):
-    # max_q_len * G <= 16: the short chunks run in the decode kernel's multi-row mode
+    # max_q_len * G <= 8: the short chunks run in the decode kernel's multi-row
+    # mode; 16 columns (the last two cases) take the tensor-core kernel
     lens = [n, n + 1, 30, 300, 1500]
     wl = small_workload(1200 + hq + n, lens=lens, q_lens=[n] * len(lens), hq=hq, hkv=hkv, kv_dtype="fp8",
                         fp8_scale_factors=DISTINCT_FP8_FACTORS)

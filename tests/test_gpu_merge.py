@@ -91,9 +91,9 @@ def test_graph_replays_merge_bitwise():
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
 def test_multi_row_merge_with_garbage_workspace(kv_dtype):
-    """Short chunks (rows x G <= 16) run in the decode kernel's multi-row mode;
+    """Short chunks (rows x G <= 8) run in the decode kernel's multi-row mode;
     their per-row partials merge the same way."""
-    wl = small_workload(505, lens=[2500, 700, 4000], q_lens=[4, 2, 4], hq=16, hkv=4, kv_dtype=kv_dtype,
+    wl = small_workload(505, lens=[2500, 700, 4000], q_lens=[2, 1, 2], hq=16, hkv=4, kv_dtype=kv_dtype,
                         num_splits=4)
     dw = DeviceWorkload(wl)
     dw.workspace.fill_(0xC3)

@@ -115,9 +115,10 @@ def test_mixed_prefill_workload_sampled():
                                          (64, 8, 8, "fp8")])
 def test_spec_verify_shapes_small(hq, hkv, n, dt):
     """Speculative verification: every sequence checks an n-token draft, n causal
-    rows each ("M.65 Inference serving", speculative decoding, N = 4-8).  Short
-    chunks run in the decode kernel's multi-row mode; a 17-token context with a
-    4-row chunk leaves some rows no visible key in the last block."""
+    rows each ("M.65 Inference serving", speculative decoding, N = 4-8).  Up to
+    8 columns (rows x G) the chunks run in the decode kernel's multi-row mode,
+    beyond that in the tensor-core kernel; a 17-token context with a 4-row
+    chunk leaves some rows no visible key in the last block."""
     lens = [n, 40, 300, 1025, 16, 17, 4096]
     qlens = [n] * len(lens)
     qlens[1] = 1                                  # a decode row in the same batch
@@ -167,11 +168,12 @@ def test_calls_from_several_streams_and_a_captured_graph():
 
 
 @pytest.mark.parametrize("qlens,dt", [([5, 0, 1, 0], "bf16"), ([4, 0, 1, 0], "bf16"), ([4, 0, 1, 0], "fp8"),
-                                      ([40, 0, 1, 0], "fp8")])
+                                      ([40, 0, 1, 0], "fp8"), ([2, 0, 1, 0], "bf16"), ([2, 0, 1, 0], "fp8")])
 def test_sequences_with_no_query_rows(qlens, dt):
     """A sequence may contribute no rows to a mixed batch (cu_q_lens repeats a
-    value): the tensor-core path (5 rows x G 4, and 40 rows over an fp8 cache)
-    and the multi-row mode (4 x 4) all skip it and get every other row right."""
+    value): the tensor-core path (5 or 4 rows x G 4, and 40 rows over an fp8
+    cache) and the multi-row mode (2 x 4) all skip it and get every other row
+    right."""
     wl = small_workload(1200 + sum(qlens), lens=[100, 50, 300, 17], q_lens=qlens, hq=16, hkv=4, kv_dtype=dt)
     _, _, ref = expected_full(wl)
     _, got = _run(wl)
