@@ -98,7 +98,12 @@ struct Lay {
     // BIG: a second producer warp issues the V boxes; a CTA with one issuer is
     // bound by how fast its loads leave, and two warps issue them faster than one
     static constexpr int W_PROD2 = BIG ? W_WIDEN : -1;
-    static constexpr int THREADS = 32 * (W_WIDEN + (FP8 ? 4 : 0) + (BIG ? 1 : 0));
+    // BIG: a warp zeroes the V rows past the context in an item's last tile once
+    // it has landed, so that the producer never waits for a load to land (short
+    // items come one after another); the 64-key bf16 layout's producer does it
+    // itself, between items that are long
+    static constexpr int W_TAIL = BIG ? W_PROD2 + 1 : -1;
+    static constexpr int THREADS = 32 * (W_WIDEN + (FP8 ? 4 : 0) + (BIG ? 2 : 0));
     static constexpr int KV_STAGES = BIG ? 3 : (FP8 ? 3 : 4);
     static constexpr uint32_t KV_HALF = BNK * 128;           // one 64-dim half of a K or V tile
     static constexpr uint32_t V_OFF = 2 * KV_HALF;
@@ -133,7 +138,8 @@ enum {
     B_F8E = B_F8F + 3,              // + staging stage: fp8 cache: the stage was widened
     B_IFULL = B_F8E + 3,            // + slot: the producer wrote a work item into the slot
     B_IEMPTY = B_IFULL + NSLOT,     // + slot: every other warp has read it
-    NBAR = B_IEMPTY + NSLOT
+    B_TGO = B_IEMPTY + NSLOT,       // + stage: bf16 cache: an item's last tile, past the context, landed
+    NBAR = B_TGO + 4
 };
 // a work item as the producer hands it to the other warps (valid = 0: no more)
 struct ItemSlot {
@@ -193,34 +199,56 @@ struct Work {
     bool has1;
 };
 // (toff, cu, cl: the query items' prefix sums, cu_q_lens and context_lens, in
-// global or shared memory)
+// global or shared memory; s_hint: the item's sequence if known, else -1;
+// tpt_log2, tk_log2: log2 of the query rows per tile and of the keys per tile)
 __device__ __forceinline__ bool locate(const PrefillParams &p, const int32_t *toff, const int32_t *cu,
-                                       const int32_t *cl, int x, int split, int item_tiles, int tile_keys,
-                                       int tiles_per_split, Work &w)
+                                       const int32_t *cl, int x, int split, int item_tiles, int tpt_log2,
+                                       int tk_log2, int tiles_per_split, Work &w, int s_hint = -1)
 {
-    int lo = 0, hi = p.num_seqs;                 // toff[lo] <= x < toff[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (toff[mid] <= x) lo = mid;
-        else hi = mid;
+    int lo = s_hint;
+    if (lo < 0) {
+        lo = 0;
+        int hi = p.num_seqs;                     // toff[lo] <= x < toff[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (toff[mid] <= x) lo = mid;
+            else hi = mid;
+        }
     }
     w.s = lo;
     w.item = x - toff[lo];
     w.row0 = cu[lo];
     w.n = cu[lo + 1] - w.row0;
     w.L = cl[lo];
-    const int tpt = BM / p.group;
-    const int tiles = (w.n + tpt - 1) / tpt;
+    const int tpt = 1 << tpt_log2;
+    const int tiles = (w.n + tpt - 1) >> tpt_log2;
     w.t0q = item_tiles * w.item;                  // the CTA's first query tile
     w.has1 = item_tiles == 2 && w.t0q + 1 < tiles;   // the pair's second query tile exists
     const int last = w.has1 ? w.t0q + 1 : w.t0q;
     const int kmax = w.L - w.n + min(w.n, (last + 1) * tpt);   // keys visible to the last row
-    w.KT = (kmax + tile_keys - 1) / tile_keys;
+    w.KT = (kmax + (1 << tk_log2) - 1) >> tk_log2;
     w.nsplit = (w.KT + tiles_per_split - 1) / tiles_per_split;
     const int tps = (w.KT + w.nsplit - 1) / w.nsplit;   // ceil(KT / tps) == nsplit
     w.j0 = split * tps;
     w.T = min(w.KT, w.j0 + tps) - w.j0;
     return w.j0 < w.KT;
+}
+
+// bounded wait for a warp that waits long and has nothing else to do: it
+// sleeps between polls, leaving its scheduler's issue slots to the other warps
+__device__ __forceinline__ bool wait_bar_lazy(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+{
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(256);
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            flag(ST_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
 }
 
 // bounded wait that also gives up as soon as another role has aborted
@@ -262,18 +290,20 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // candidates are the host's length and uncut; every item of a sequence is taken
 // to see as many keys as its last one.
 constexpr int PREFIX_SMAX = 2048;
+constexpr int PREFIX_XMAX = 8192;   // query items whose sequence is tabled in shared memory
 __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
 {
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t carry;
     __shared__ int32_t sh_toff[PREFIX_SMAX + 1], sh_cu[PREFIX_SMAX + 1], sh_cl[PREFIX_SMAX];
+    __shared__ uint16_t sh_xs[PREFIX_XMAX];     // query item -> its sequence (num_seqs <= 65,535)
     // per candidate (0: the host's length, 1: uncut): items, longest and shortest
     // partition; the cut ranges' rows x partitions; all items' tiles (summed a
     // warp at a time: shared-memory atomics on one word serialise a warp)
     __shared__ unsigned int c_items[2];
     __shared__ int c_tmax[2], c_tmin[2];
     __shared__ float c_mrows, s_tiles;
-    __shared__ int s_tps;
+    __shared__ int s_tps, s_nsmax;
     constexpr int NBKT = 32;
     static_assert(NBKT == 32, "one warp scans the buckets");
     __shared__ int32_t cnt[32][NBKT];
@@ -286,6 +316,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     griddep_wait();
     const bool staged = p.num_seqs <= PREFIX_SMAX;
     const int tpt = BM / p.group, tk = p.tile_keys, tps0 = max(1, p.tiles_per_split);
+    const int tpt_log2 = __ffs(tpt) - 1, tk_log2 = __ffs(tk) - 1;   // both powers of two
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
     if (threadIdx.x < 2) {
         c_items[threadIdx.x] = 0u;
@@ -387,6 +418,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         if (s < p.num_seqs) {
             p.tile_off[s + 1] = incl;
             if (staged) sh_toff[s + 1] = incl;
+            for (int x = incl - tiles; x < min(incl, PREFIX_XMAX); ++x) sh_xs[x] = (uint16_t)s;
         }
         __syncthreads();
         if (threadIdx.x == blockDim.x - 1) carry = incl;
@@ -412,6 +444,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
             cut = 0;
         }
         s_tps = pick;
+        s_nsmax = (max(c_tmax[1], 1) + pick - 1) / pick;   // the most partitions of any item
         p.order_count[2] = cut;                      // the merge kernel has work
     }
     __syncthreads();
@@ -437,9 +470,9 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
             }
             const int a = cu[lo], n = cu[lo + 1] - a, L = cl[lo];
             if (n >= 2 && a >= 0 && row >= a && L >= n && L <= p.max_blocks * BS) {
-                const int i = row - a, mt = i / tpt, tiles = (n + tpt - 1) / tpt;
+                const int i = row - a, mt = i >> tpt_log2, tiles = (n + tpt - 1) >> tpt_log2;
                 const int last = min(tiles - 1, (mt / p.item_tiles) * p.item_tiles + p.item_tiles - 1);
-                const int KT = (L - n + min(n, (last + 1) * tpt) + tk - 1) / tk;
+                const int KT = (L - n + min(n, (last + 1) * tpt) + tk - 1) >> tk_log2;
                 ns = (KT + tps - 1) / tps;
             }
         }
@@ -457,7 +490,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     // deterministic.  An entry (two int4) holds everything a CTA needs:
     //   s, row0, n, L | j0, T | nsplit << 16, KV head | partition << 16, t0q | has1 << 30
     // (the slot count is below 2^31: the host bounds the grid by it)
-    const long long nslot = (long long)X * p.hkv * p.max_splits;
+    const long long nslot = (long long)X * p.hkv * min(p.max_splits, s_nsmax);
     const long long seg = (nslot + nw - 1) / nw;
     const long long s0 = (long long)w * seg, s1 = min(nslot, s0 + seg);
     auto bucket_of = [&](long long e, int4 &e0, int4 &e1) -> int {
@@ -465,10 +498,12 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         const int x = (int)(eu - r * (unsigned)X);
         const int g = (int)(r % (unsigned)p.hkv), split = (int)(r / (unsigned)p.hkv);
         Work wk;
-        if (!locate(p, toff, cu, cl, x, split, p.item_tiles, tk, tps, wk)) return -1;
+        if (!locate(p, toff, cu, cl, x, split, p.item_tiles, tpt_log2, tk_log2, tps, wk,
+                    x < PREFIX_XMAX ? (int)sh_xs[x] : -1))
+            return -1;
         e0 = make_int4(wk.s, wk.row0, wk.n, wk.L);
         e1 = make_int4(wk.j0, wk.T | (wk.nsplit << 16), g | (split << 16), wk.t0q | (wk.has1 ? 1 << 30 : 0));
-        return min(NBKT - 1, (int)(((long long)max(0, tps - wk.T) * NBKT) / tps));
+        return min(NBKT - 1, (max(0, tps - wk.T) * NBKT) / tps);   // (tps x 32 < 2^31)
     };
     // (a warp's first 32 slots -- all of them in small batches -- are kept in
     // registers for the second pass)
@@ -574,6 +609,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
             mbar_init(bar(B_KVF + i), FP8 ? 128 : 1);   // fp8: the widening warps arrive
             mbar_init(bar(B_KVE + i), LY::NG);          // one release per MMA issuer
             mbar_init(bar(B_TAIL + i), 1);
+            mbar_init(bar(B_TGO + i), 1);
         }
         for (int i = 0; i < F8_STAGES; ++i) {
             mbar_init(bar(B_F8F + i), 1);
@@ -634,6 +670,18 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
     // a tile whose keys run past the context (only ever an item's last tile):
     // its V rows there are zeroed before PV reads them (bf16 cache)
     auto has_tail = [&](const ItemSlot &it) -> bool { return (it.j0 + it.T) * BN > it.L; };
+    // zeroes V rows first .. BN-1 of the landed tile in stage st (one warp), then
+    // releases its PV products (B_TAIL)
+    auto zero_tail = [&](int st, int first) {
+        const uint32_t vb = sbase + SKV + st * KV_STAGE_BYTES + V_OFF;
+        for (int c = lane; c < (BN - first) * 16; c += 32) {
+            const int r = first + (c >> 4), h = (c >> 3) & 1, ch = c & 7;
+            st_shared_v4(vb + (r >> 4) * 4096 + h * 2048 + (r & 15) * 128 + ch * 16, 0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_TAIL + st));
+    };
 
     if (warp == LY::W_PROD || warp == LY::W_PROD2) {
         // ======================= TMA producer.  Role 0 fetches the work items,
@@ -725,7 +773,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
             }
             const int32_t *bt = p.block_tables + (size_t)it.s * p.max_blocks;
             const int nblk = (it.L + BS - 1) / BS;
-            const int j0 = it.j0, T = it.T, L = it.L;
+            const int j0 = it.j0, T = it.T;
             if constexpr (FP8) {
                 // e4m3 K and V of each block (one 2 KiB box each) into a staging stage;
                 // the widening warps turn it into the operand tiles.  The block ids of
@@ -793,24 +841,16 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
                         if (is_v) tma_load_3d(stg + V_OFF + blk * 4096, &vmap, 0, y, 0, bar(B_KVF + st));
                         else tma_load_2d(stg + opnd * KV_HALF + blk * 2048, &kmap, opnd * 64, y, bar(B_KVF + st));
                     }
-                    const int first = L - j * BN;            // first row of the tile at or past L
-                    if (first < BN && role == 0) {
-                        // keys >= L: their V rows may hold anything (never written, or not
-                        // loaded); P is 0 there but 0 * NaN is NaN, so zero them once the
-                        // tile has landed, before any PV product reads it
+                    const int first = it.L - j * BN;         // first row of the tile at or past L
+                    if (!BIG && first < BN) {
+                        // the 64-key layout: this warp zeroes the V rows past the context
+                        // (see the tail warp) once the tile has landed
                         if (!wait_w(bar(B_KVF + st), (u / KV_STAGES) & 1)) {
                             failed = true;
                             ++u;
                             break;
                         }
-                        const uint32_t vb = sbase + SKV + st * KV_STAGE_BYTES + V_OFF;
-                        for (int c = lane; c < (BN - first) * 16; c += 32) {
-                            const int r = first + (c >> 4), h = (c >> 3) & 1, ch = c & 7;
-                            st_shared_v4(vb + (r >> 4) * 4096 + h * 2048 + (r & 15) * 128 + ch * 16, 0u, 0u, 0u, 0u);
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar(B_TAIL + st));
+                        zero_tail(st, first);
                     }
                 }
             }
@@ -917,8 +957,14 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
             ok = FP8 ? wait_w(bar(B_QC + gi), kg & 1) : wait_w(bar(B_Q), k & 1);
             int sx = st0;                              // the next tile to compute S for
             uint32_t px = ph0;                         // its KVF phase parity
+            // the tail tile has landed: the tail warp may zero its rows past L (it
+            // waits for this in item order, so its barrier phases cannot alias)
+            auto tail_go = [&]() {
+                if (BIG && tail && gi == 0 && lane == 0) mbar_arrive(bar(B_TGO + tail_st));
+            };
             for (int jj = 0; ok && jj < min(2, T); ++jj) {
                 if (!wait_w(bar(B_KVF + sx), px)) { ok = false; break; }
+                if (jj == T - 1) tail_go();
                 issue_s(sx, sbuf ^ jj, jj == T - 1);
                 adv(sx, px);
             }
@@ -936,6 +982,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
                 issue_pv(spv, sbuf, jj == 0);
                 if (jj + 2 < T) {
                     if (!wait_w(bar(B_KVF + sx), px)) { ok = false; break; }
+                    if (jj + 2 == T - 1) tail_go();
                     issue_s(sx, sbuf, jj + 2 == T - 1);
                     adv(sx, px);
                 }
@@ -953,6 +1000,26 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
         // that phase while the softmax warps still wait on it, and the two phases
         // would alias their parity)
         if (kg > 0) (void)mbar_wait_bounded(bar(B_DRAIN + gi), (kg - 1) & 1);
+    } else if (warp == LY::W_TAIL) {
+        // ======================= bf16 cache: an item's last tile may hold keys past
+        // the context; their V rows may hold anything (never written, or not
+        // loaded), and P is 0 there but 0 * NaN is NaN, so they are zeroed once the
+        // tile has landed, before its PV product (which waits for B_TAIL) reads it
+        // (the first issuer signals B_TGO once the tile has landed: this warp must
+        // not wait on the stage's own barrier, which it could reach two phases early)
+        int stg = 0;        // the ring position of the next item's first tile
+        unsigned tgpar = 0; // phase parity of each stage's B_TGO
+        for (int k = 0;; ++k) {
+            ItemSlot it;
+            if (!read_item(k, it)) break;
+            const int T = it.T;
+            const int st = (stg + T - 1) % KV_STAGES;  // the item's last tile
+            stg = (stg + T) % KV_STAGES;
+            if (!has_tail(it)) continue;
+            if (!__all_sync(0xffffffffu, wait_bar_lazy(bar(B_TGO + st), (tgpar >> st) & 1, abort_flag))) break;
+            tgpar ^= 1u << st;
+            zero_tail(st, it.L - (it.j0 + T - 1) * BN);
+        }
     } else if (warp >= LY::W_WIDEN) {
         // ======================= fp8 cache: widen each e4m3 K/V tile to f16 operand
         // tiles (exact), in the operand stages' 128-byte-swizzled layout; keys at
