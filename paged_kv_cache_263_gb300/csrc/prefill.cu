@@ -180,6 +180,8 @@ struct PrefillParams {
     int num_sms;
     float bytes_per_tile;              // HBM bytes the GPU moves in one KV tile's time
     int rows1;                         // the call runs decode rows (queries of 1); else a 1 is flagged
+    int grid_ctas;                     // the chunk kernel's CTAs
+    int q_box_bytes;                   // one 64-dim half of a query tile as loaded (rows x G x 128 B)
     int item_tiles;      // query tiles per CTA: 2 (a pair), or 1 (the 128-key layout)
     int tile_keys;       // keys per KV tile: 64, or 128 (the 128-key layout)
     float scale_log2;
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     __shared__ unsigned int c_items[2];
     __shared__ int c_tmax[2], c_tmin[2];
     __shared__ float c_mrows, s_tiles;
-    __shared__ int s_tps, s_nsmax;
+    __shared__ int s_tps, s_nsmax, s_cut;
     constexpr int NBKT = 32;
     static_assert(NBKT == 32, "one warp scans the buckets");
     __shared__ int32_t cnt[32][NBKT];
@@ -445,6 +447,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         }
         s_tps = pick;
         s_nsmax = (max(c_tmax[1], 1) + pick - 1) / pick;   // the most partitions of any item
+        s_cut = cut;
         p.order_count[2] = cut;                      // the merge kernel has work
     }
     __syncthreads();
@@ -458,8 +461,9 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     if (threadIdx.x == 0 && carry > p.items_cap) flag(ST_BAD_LEN);
 
     // ---- 3. per query row: its item's partition count (0 for rows outside any
-    // chunk); and the work items' bucket counts
-    for (int row = threadIdx.x; row < p.total_rows; row += blockDim.x) {
+    // chunk; not needed when no key range is cut: the merge kernel then has no
+    // work); and the work items' bucket counts
+    for (int row = threadIdx.x; s_cut && row < p.total_rows; row += blockDim.x) {
         int lo = 0, hi = p.num_seqs;                 // cu[lo] <= row < cu[hi]
         int ns = 0;
         if (row < cu[p.num_seqs]) {
@@ -539,7 +543,9 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         bstart[lane] = v - run;
         if (lane == 31) {
             p.order_count[0] = v;
-            p.order_count[1] = 0;                 // the persistent CTAs' fetch counter
+            // the persistent CTAs' fetch counter: CTA c takes item c first, the
+            // rest through the counter
+            p.order_count[1] = p.grid_ctas;
         }
     }
     __syncthreads();
@@ -718,10 +724,12 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
                 // every listed partition is non-empty, but a CTA never trusts that
                 // to keep its pipelines in step
                 it.valid = 0;
-                while (true) {
-                    int idx = 0;
-                    if (lane == 0) idx = atomicAdd(p.order_count + 1, 1);
-                    idx = __shfl_sync(0xffffffffu, idx, 0);
+                for (int tries = 0;; ++tries) {
+                    int idx = (int)blockIdx.x;           // the first item: no round trip
+                    if (k > 0 || tries > 0) {
+                        if (lane == 0) idx = atomicAdd(p.order_count + 1, 1);
+                        idx = __shfl_sync(0xffffffffu, idx, 0);
+                    }
                     if (idx >= p.order_count[0]) break;
                     const int4 e0 = p.order[2 * idx], e1 = p.order[2 * idx + 1];
                     it.s = e0.x;
@@ -760,7 +768,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
                 // Q of the item, once every QK^T product of the item before finished
                 if (kq > 0 && !wait_w(bar(B_QFREE), (kq - 1) & 1)) break;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(B_Q), (it.has1 ? 4 : 2) * 16384);
+                    mbar_arrive_expect_tx(bar(B_Q), (it.has1 ? 4 : 2) * p.q_box_bytes);
                     for (int gi = 0; gi < (it.has1 ? 2 : 1); ++gi) {
                         const int zq = it.row0 + (it.t0q + gi) * tpt;
                         tma_load_3d(sbase + SQ + gi * Q_TILE, &qmap, 0, it.g * G, zq, bar(B_Q));
@@ -1256,13 +1264,16 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
 
 // Log-sum-exp merge of prefill partitions: one warp per (query row, head).
 // (grid-stride; nothing to do when tile_prefix_kernel cut no key range)
-__global__ void __launch_bounds__(128) prefill_reduce_kernel(const PrefillParams p)
+// (512 threads: few CTAs to start and retire when there is nothing to merge)
+constexpr int MERGE_WARPS = 16;
+__global__ void __launch_bounds__(MERGE_WARPS * 32) prefill_reduce_kernel(const PrefillParams p)
 {
     griddep_wait();   // launched with programmatic serialisation after the chunk kernel
     if (p.order_count[2] == 0) return;
     const int lane = threadIdx.x & 31;
     const long nw = (long)p.total_rows * p.hq;
-    for (long wid = (long)blockIdx.x * 4 + (threadIdx.x >> 5); wid < nw; wid += (long)gridDim.x * 4) {
+    for (long wid = (long)blockIdx.x * MERGE_WARPS + (threadIdx.x >> 5); wid < nw;
+         wid += (long)gridDim.x * MERGE_WARPS) {
         const int row = (int)(wid / p.hq), h = (int)(wid % p.hq);
         // the partitions of the query item the row belongs to (tile_prefix_kernel
         // wrote them; 0 for rows outside any chunk)
@@ -1625,8 +1636,13 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     p.bytes_per_tile = (float)(BYTES_PER_TILE_TIME * p.tile_keys / 64.0);
     CUtensorMap qm, km, vm;
     const int tpt = BM / G;
+    // the 128-key layout holds one query tile per sequence (max_q_len x G <= 128):
+    // only its max_q_len rows are loaded; the tile's other rows keep what shared
+    // memory held (their scores and outputs stay in their own rows, never stored)
+    const int q_rows = big ? std::min(tpt, max_q_len) : tpt;
+    p.q_box_bytes = q_rows * G * 128;
     if (!pkv_host::encode_tmap_3d(&qm, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, num_q_heads, total_q_tokens,
-                                  (uint64_t)D * 2, (uint64_t)num_q_heads * D * 2, 64, G, tpt,
+                                  (uint64_t)D * 2, (uint64_t)num_q_heads * D * 2, 64, G, q_rows,
                                   CU_TENSOR_MAP_SWIZZLE_128B))
         return KV_ERR_CUDA;
     if (!pkv_decode::make_maps(k_cache, v_cache, num_blocks, num_kv_heads, dtype, &km, &vm)) return KV_ERR_CUDA;
@@ -1647,10 +1663,11 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     // tile_prefix_kernel writes; the grid bounds their number
     const int64_t ctas_ub = pl.items_ub * num_kv_heads * p.max_splits;
     if (ctas_ub > INT32_MAX || p.max_splits > 65535 || num_kv_heads > 65535) return KV_ERR_UNSUPPORTED;
+    p.grid_ctas = (int)std::min<int64_t>(ctas_ub, p.num_sms);
     if (pkv_host::launch_ex(tile_prefix_kernel, dim3(1), dim3(1024), 0, st, !rows1, p) != cudaSuccess)
         return KV_ERR_CUDA;
     // persistent: one CTA per SM (a CTA holds a whole SM), at most one per work item
-    dim3 grid((unsigned)std::min<int64_t>(ctas_ub, num_sms()));
+    dim3 grid((unsigned)p.grid_ctas);
     Trace *tr = trace_for_call();
     if (tr) cudaEventRecord(tr->start, st);
     // programmatic serialisation: the CTAs' set-up overlaps tile_prefix_kernel
@@ -1675,8 +1692,9 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     if (p.max_splits > 1) {
         const int64_t warps = (int64_t)total_q_tokens * num_q_heads;
         if (pkv_host::launch_ex(prefill_reduce_kernel,
-                                dim3((unsigned)std::min<int64_t>((warps + 3) / 4, (int64_t)p.num_sms * 16)), dim3(128),
-                                0, st, !tr, p) != cudaSuccess)
+                                dim3((unsigned)std::min<int64_t>((warps + MERGE_WARPS - 1) / MERGE_WARPS,
+                                                                 (int64_t)p.num_sms * 4)),
+                                dim3(MERGE_WARPS * 32), 0, st, !tr, p) != cudaSuccess)
             return KV_ERR_CUDA;
     }
     return KV_OK;
