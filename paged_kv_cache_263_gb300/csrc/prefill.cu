@@ -485,28 +485,28 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     // The work items in launch order, longest first: the CTAs take them one
     // after another, so a long item taken last would set the makespan (ragged
     // speculative drafts).  Longest-processing-time-first list order instead:
-    // items are bucketed by length relative to the partition length (NBKT
-    // buckets) and sorted stably, so that within a bucket they keep the order
-    // item fastest, then KV head, then partition, under which concurrent CTAs
-    // share their keys in L2.  Each warp takes a contiguous segment of the
-    // slots; a slot's rank is its bucket's start + the earlier warps' counts in
-    // that bucket + its rank in its own warp's segment, so the order is
+    // (query item, partition) pairs are bucketed by length relative to the
+    // partition length (NBKT buckets) and sorted stably, so that within a bucket
+    // they keep the order item fastest, then partition, under which concurrent
+    // CTAs share their keys in L2; each pair then takes hkv consecutive places,
+    // one per KV head.  Each warp takes a contiguous segment of the pairs; a
+    // pair's rank is its bucket's start + the earlier warps' counts in that
+    // bucket + its rank in its own warp's segment, so the order is
     // deterministic.  An entry (two int4) holds everything a CTA needs:
     //   s, row0, n, L | j0, T | nsplit << 16, KV head | partition << 16, t0q | has1 << 30
-    // (the slot count is below 2^31: the host bounds the grid by it)
-    const long long nslot = (long long)X * p.hkv * min(p.max_splits, s_nsmax);
+    // (the pair count x hkv is below 2^31: the host bounds the grid by it)
+    const long long nslot = (long long)X * min(p.max_splits, s_nsmax);
     const long long seg = (nslot + nw - 1) / nw;
     const long long s0 = (long long)w * seg, s1 = min(nslot, s0 + seg);
     auto bucket_of = [&](long long e, int4 &e0, int4 &e1) -> int {
-        const unsigned eu = (unsigned)e, r = eu / (unsigned)X;
-        const int x = (int)(eu - r * (unsigned)X);
-        const int g = (int)(r % (unsigned)p.hkv), split = (int)(r / (unsigned)p.hkv);
+        const unsigned eu = (unsigned)e, split = eu / (unsigned)X;
+        const int x = (int)(eu - split * (unsigned)X);
         Work wk;
-        if (!locate(p, toff, cu, cl, x, split, p.item_tiles, tpt_log2, tk_log2, tps, wk,
+        if (!locate(p, toff, cu, cl, x, (int)split, p.item_tiles, tpt_log2, tk_log2, tps, wk,
                     x < PREFIX_XMAX ? (int)sh_xs[x] : -1))
             return -1;
         e0 = make_int4(wk.s, wk.row0, wk.n, wk.L);
-        e1 = make_int4(wk.j0, wk.T | (wk.nsplit << 16), g | (split << 16), wk.t0q | (wk.has1 ? 1 << 30 : 0));
+        e1 = make_int4(wk.j0, wk.T | (wk.nsplit << 16), (int)(split << 16), wk.t0q | (wk.has1 ? 1 << 30 : 0));
         return min(NBKT - 1, (max(0, tps - wk.T) * NBKT) / tps);   // (tps x 32 < 2^31)
     };
     // (a warp's first 32 slots -- all of them in small batches -- are kept in
@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         }
         bstart[lane] = v - run;
         if (lane == 31) {
-            p.order_count[0] = v;
+            p.order_count[0] = v * p.hkv;
             // the persistent CTAs' fetch counter: CTA c takes item c first, the
             // rest through the counter
             p.order_count[1] = p.grid_ctas;
@@ -555,9 +555,11 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         const int bk = b0 == s0 ? f_bk : (b0 + lane < s1 ? bucket_of(b0 + lane, e0, e1) : -1);
         const unsigned peers = __match_any_sync(0xffffffffu, bk);
         if (bk >= 0) {
-            const int pos = bstart[bk] + cnt[w][bk] + __popc(peers & ((1u << lane) - 1u));
-            p.order[2 * pos] = e0;
-            p.order[2 * pos + 1] = e1;
+            const int pos = (bstart[bk] + cnt[w][bk] + __popc(peers & ((1u << lane) - 1u))) * p.hkv;
+            for (int g = 0; g < p.hkv; ++g) {
+                p.order[2 * (pos + g)] = e0;
+                p.order[2 * (pos + g) + 1] = make_int4(e1.x, e1.y, e1.z | g, e1.w);
+            }
         }
         __syncwarp();
         if (bk >= 0 && lane == __ffs(peers) - 1) cnt[w][bk] += __popc(peers);
