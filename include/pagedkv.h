@@ -365,7 +365,8 @@ PAGEDKV_API kv_status paged_attention_decode_static_scratch(
  *  cu_q_lens       device int32 [num_seqs+1], cu_q_lens[0] = 0, non-decreasing,
  *                  cu_q_lens[num_seqs] = total_q_tokens
  *  context_lens    device int32 [num_seqs]; includes the chunk; n_s <= len
- *  max_q_len       host int: an upper bound on every n_s (sizes the grid)
+ *  max_q_len       host int: an upper bound on every n_s (sizes the grid and the
+ *                  plan; a longer query is flagged as out of range and left out)
  *  other arguments as for paged_attention_decode; workspace must be at least
  *  paged_attention_chunked_prefill_workspace_size() bytes (one size serves
  *  both cache dtypes).

@@ -177,7 +177,9 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
         nq = b - a;
         L = p.context_lens[s];
         if (nq == 0) return;
-        if (nq < 0 || a < 0 || b > p.total_rows || nq > L || L < 1 || L > p.max_blocks * BS) {
+        // (nq x G > col_groups x CW: more rows than the caller's max_q_len allowed for)
+        if (nq < 0 || a < 0 || b > p.total_rows || nq > L || L < 1 || L > p.max_blocks * BS ||
+            nq * p.group > p.col_groups * CW) {
             if (split == 0 && cg == 0) {
                 if (threadIdx.x == 0) flag(ST_BAD_LEN);
                 if (nq > 0 && a >= 0 && b <= p.total_rows)

@@ -180,6 +180,7 @@ struct PrefillParams {
     int num_sms;
     float bytes_per_tile;              // HBM bytes the GPU moves in one KV tile's time
     int rows1;                         // the call runs decode rows (queries of 1); else a 1 is flagged
+    int max_q_len;                     // the caller's bound on every query's rows (a longer one is flagged)
     int grid_ctas;                     // the chunk kernel's CTAs
     int q_box_bytes;                   // one 64-dim half of a query tile as loaded (rows x G x 128 B)
     int item_tiles;      // query tiles per CTA: 2 (a pair), or 1 (the 128-key layout)
@@ -343,7 +344,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
             n = b - a;
             L = p.context_lens[s];
             if (n >= 2) {
-                if (a < 0 || b > p.total_rows || L < n || L > p.max_blocks * BS) flag(ST_BAD_LEN);
+                if (a < 0 || b > p.total_rows || L < n || L > p.max_blocks * BS || n > p.max_q_len) flag(ST_BAD_LEN);
                 else tiles = ((n + tpt - 1) / tpt + p.item_tiles - 1) / p.item_tiles;   // query items
             } else if (n < 0 || (n == 1 && !p.rows1)) {
                 flag(ST_BAD_LEN);
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
                 else hi = mid;
             }
             const int a = cu[lo], n = cu[lo + 1] - a, L = cl[lo];
-            if (n >= 2 && a >= 0 && row >= a && L >= n && L <= p.max_blocks * BS) {
+            if (n >= 2 && n <= p.max_q_len && a >= 0 && row >= a && L >= n && L <= p.max_blocks * BS) {
                 const int i = row - a, mt = i >> tpt_log2, tiles = (n + tpt - 1) >> tpt_log2;
                 const int last = min(tiles - 1, (mt / p.item_tiles) * p.item_tiles + p.item_tiles - 1);
                 const int KT = (L - n + min(n, (last + 1) * tpt) + tk - 1) >> tk_log2;
@@ -1635,6 +1636,7 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     p.tile_keys = big ? 128 : 64;
     p.num_sms = num_sms();
     p.rows1 = rows1 ? 1 : 0;
+    p.max_q_len = max_q_len;
     p.bytes_per_tile = (float)(BYTES_PER_TILE_TIME * p.tile_keys / 64.0);
     CUtensorMap qm, km, vm;
     const int tpt = BM / G;

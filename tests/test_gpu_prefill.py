@@ -232,3 +232,29 @@ def test_one_tile_chunk_over_many_partitions():
     cu = wl.cu_q_lens
     for s in range(3):
         assert max_abs(got[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s)) <= TOL["bf16"], s
+
+
+@pytest.mark.parametrize("qlens,max_q_len", [([1, 5], 3), ([2, 5, 2], 3), ([1, 3, 2], 2)])
+def test_queries_outside_the_declared_bound_are_flagged(qlens, max_q_len):
+    """max_q_len bounds every query.  When total_q_tokens = num_seqs x max_q_len
+    the chunk path runs no decode rows, so a 1-row query there breaks the
+    contract; so does a query longer than max_q_len (in the multi-row decode
+    mode -- max_q_len x G <= 8, the last case -- one whose columns exceed the
+    CTA's).  Each is flagged as out of range (status 5) and left out, and the
+    rows of the queries within the bound still match the oracle."""
+    wl = small_workload(1300 + sum(qlens), lens=[60, 300, 90][:len(qlens)], q_lens=qlens, hq=16, hkv=4)
+    assert max_q_len * 4 <= 8 or int(wl.q_lens.sum()) == len(qlens) * max_q_len
+    dw = DeviceWorkload(wl)
+    dw.step()
+    pkv.kv_last_device_status()                    # the step's own call used the true maximum: clean
+    dw.out.fill_(0.0)
+    pkv.paged_attention_chunked_prefill(dw.out, dw.q, dw.cu_q_lens, dw.context_lens, max_q_len, dw.k_cache,
+                                        dw.v_cache, dw.block_tables)
+    assert pkv.kv_last_device_status() == 5
+    assert pkv.kv_last_device_status_flags() & 4   # ST_BAD_LEN
+    got = dw.out.cpu().numpy().astype(np.float64)
+    cu = wl.cu_q_lens
+    multi = max_q_len * 4 <= 8
+    for s, n in enumerate(qlens):
+        if (1 if multi else 2) <= n <= max_q_len:
+            check_close(got[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s), "bf16", s)
