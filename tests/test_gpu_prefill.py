@@ -258,3 +258,17 @@ def test_queries_outside_the_declared_bound_are_flagged(qlens, max_q_len):
     for s, n in enumerate(qlens):
         if (1 if multi else 2) <= n <= max_q_len:
             check_close(got[cu[s]:cu[s + 1]], omodel.expected_rows(wl, s), "bf16", s)
+
+
+def test_large_batches_take_the_global_memory_paths():
+    """9,000 sequences, each verifying a 2-token draft (16 columns at G = 8: the
+    tensor-core kernel, one query item per sequence): more sequences than the
+    work-list kernel stages in shared memory (2,048) and more query items than
+    it tables (8,192), so it reads the chunk metadata and searches the item
+    prefix sums in global memory; every row still matches the oracle."""
+    rng = np.random.default_rng(1400)
+    lens = rng.integers(16, 120, size=9000).astype(np.int32)
+    wl = small_workload(1400, lens=lens, q_lens=np.full(9000, 2, np.int32), hq=16, hkv=2)
+    _, _, ref = expected_full(wl)
+    _, got = _run(wl)
+    check_close(got, ref, "bf16", "9,000 sequences")
