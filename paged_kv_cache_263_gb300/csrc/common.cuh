@@ -478,8 +478,16 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
 __device__ __forceinline__ float4 lse_merge_warp(const float *__restrict__ ml, const float *__restrict__ o, int ns,
                                                  int lane)
 {
-    float M = -INFINITY;
-    for (int i = lane; i < ns; i += 32) M = fmaxf(M, ml[2 * i]);
+    // the first 32 partitions' (max, sum) and the first four partitions' rows are
+    // requested together, before anything depends on them
+    float2 e0 = make_float2(-INFINITY, 0.f);
+    if (lane < ns) e0 = *reinterpret_cast<const float2 *>(ml + 2 * lane);
+    float4 pre[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        pre[u] = u < ns ? reinterpret_cast<const float4 *>(o + (size_t)u * D)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = e0.x;
+    for (int i = lane + 32; i < ns; i += 32) M = fmaxf(M, ml[2 * i]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -489,7 +497,7 @@ __device__ __forceinline__ float4 lse_merge_warp(const float *__restrict__ ml, c
             // weights of partitions i0 .. i0 + 31, one per lane
             float f = 0.f;
             if (i0 + lane < ns) {
-                const float2 e = *reinterpret_cast<const float2 *>(ml + 2 * (i0 + lane));
+                const float2 e = i0 == 0 ? e0 : *reinterpret_cast<const float2 *>(ml + 2 * (i0 + lane));
                 f = ex2(e.x - M);
                 lsum += f * e.y;
             }
@@ -499,8 +507,9 @@ __device__ __forceinline__ float4 lse_merge_warp(const float *__restrict__ ml, c
                 float4 v[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    v[u] = k0 + u < n ? reinterpret_cast<const float4 *>(o + (size_t)(i0 + k0 + u) * D)[lane]
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[u] = (i0 == 0 && k0 == 0) ? pre[u]
+                           : k0 + u < n ? reinterpret_cast<const float4 *>(o + (size_t)(i0 + k0 + u) * D)[lane]
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const float fk = __shfl_sync(0xffffffffu, f, (k0 + u) & 31);

@@ -574,7 +574,8 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
 // or per (row, q head) in the multi-row mode.
 __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p)
 {
-    griddep_wait();   // the partials come from the decode kernel just before
+    // (the lengths were written before the decode kernel began, so they are read
+    // before the wait for its partials)
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const bool per_row = p.col_groups > 0;
@@ -596,6 +597,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p)
     const int nblk = (L + BS - 1) / BS;
     const int ns = (nblk + p.part_blocks - 1) / p.part_blocks;
     if (ns <= 1) return;
+    griddep_wait();   // the partials come from the decode kernel just before
     const size_t base = ((size_t)wi * p.hq + h) * p.num_splits;
     const float4 r = lse_merge_warp(p.part_ml + base * 2, p.part_o + base * D, ns, lane);
     reinterpret_cast<float4 *>(p.out + ((size_t)row * p.hq + h) * D)[lane] = r;
