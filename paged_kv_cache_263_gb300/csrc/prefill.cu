@@ -442,7 +442,8 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         };
         const bool cut0 = c_mrows > 0.f;
         int pick = tps0, cut = cut0 ? 1 : 0;
-        if (cut0 && est(1, 0.f) <= est(0, c_mrows * per_row_split + merge_start)) {
+        // (uncut only while an item's tiles fit the entry's 16-bit field)
+        if (cut0 && c_tmax[1] < 65536 && est(1, 0.f) <= est(0, c_mrows * per_row_split + merge_start)) {
             pick = max(tps0, c_tmax[1]);             // uncut: every range in one partition
             cut = 0;
         }
@@ -573,8 +574,8 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
 //
 // Persistent: the grid holds one CTA per SM, and each CTA takes work items
 // (query item, KV head, partition) from the longest-first list that
-// tile_prefix_kernel wrote, one after another through an atomic counter, until
-// the list is used up.  The producer warp fetches an item and hands it to the
+// tile_prefix_kernel wrote, one after another (CTA c takes item c first, then
+// the next free one through an atomic counter), until the list is used up.  The producer warp fetches an item and hands it to the
 // other warps through a ring of NSLOT shared-memory slots; the K/V stage ring,
 // the S buffers and every barrier phase run on across items, so the next item's
 // Q and first K/V tiles load, and its first QK^T products run, while the
