@@ -559,8 +559,8 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         if (bk >= 0) {
             const int pos = (bstart[bk] + cnt[w][bk] + __popc(peers & ((1u << lane) - 1u))) * p.hkv;
             for (int g = 0; g < p.hkv; ++g) {
-                p.order[2 * (pos + g)] = e0;
-                p.order[2 * (pos + g) + 1] = make_int4(e1.x, e1.y, e1.z | g, e1.w);
+                p.order[2 * (size_t)(pos + g)] = e0;
+                p.order[2 * (size_t)(pos + g) + 1] = make_int4(e1.x, e1.y, e1.z | g, e1.w);
             }
         }
         __syncwarp();
@@ -735,7 +735,7 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
                         idx = __shfl_sync(0xffffffffu, idx, 0);
                     }
                     if (idx >= p.order_count[0]) break;
-                    const int4 e0 = p.order[2 * idx], e1 = p.order[2 * idx + 1];
+                    const int4 e0 = p.order[2 * (size_t)idx], e1 = p.order[2 * (size_t)idx + 1];
                     it.s = e0.x;
                     it.row0 = e0.y;
                     it.n = e0.z;
