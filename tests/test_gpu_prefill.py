@@ -272,3 +272,19 @@ def test_large_batches_take_the_global_memory_paths():
     _, _, ref = expected_full(wl)
     _, got = _run(wl)
     check_close(got, ref, "bf16", "9,000 sequences")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_many_ragged_chunks_in_the_pair_layout(kv_dtype):
+    """48 sequences with 40-row chunks over contexts of 300..6,000 keys.  With
+    G = 8 a chunk's rows x heads fill three 128-row tiles, so it takes the
+    64-key layout as one item of two query tiles and one item of a single tile
+    (the second issuer idle); the work-list kernel orders the ragged items
+    longest first and may leave their key ranges whole.  Every row matches the
+    oracle."""
+    rng = np.random.default_rng(1500)
+    lens = rng.integers(300, 6000, size=48).astype(np.int32)
+    wl = small_workload(1500, lens=lens, q_lens=np.full(48, 40, np.int32), hq=16, hkv=2, kv_dtype=kv_dtype)
+    _, _, ref = expected_full(wl)
+    _, got = _run(wl)
+    check_close(got, ref, kv_dtype, "48 ragged chunks")
