@@ -724,7 +724,7 @@ def run_ours(args):
                                "paged_attention_chunked_prefill (whole call)"),
                     "flops_per_launch": flops, "avg_launch_ms": kern_avg, "traffic": None,
                     "whole_call": {"avg_ms": attn_avg, "achieved": call_tflops, "frac": call_tflops / tpeak,
-                                   "includes": "chunk tiles + decode rows (side stream) + LSE merges"}}
+                                   "includes": "chunk tiles + decode rows (beside them) + LSE merges"}}
     launches_per_step = _launches_per_step(pkv, wl)
     kv_bytes = ab["kv_unique"]
     line = {

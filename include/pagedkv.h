@@ -338,12 +338,13 @@ PAGEDKV_API kv_status paged_attention_decode_static_scratch(
  * context_len-n_s .. context_len-1, row i attends keys 0 .. context_len-n_s+i
  * (causal inside the chunk, everything before it visible).  Rows with n_s = 1
  * are decode rows and take the decode kernel; with a bf16 cache, chunks
- * (n_s >= 2) take the tensor-core (tcgen05) kernel, and the decode rows run on
- * a stream the library owns (one per device), forked from `stream` with an
- * event and joined back into it before the call returns: work enqueued on
- * `stream` afterwards sees the whole output.  When total_q_tokens = num_seqs x
- * max_q_len every query is max_q_len rows long, so there are no decode rows and
- * no side stream (a query of 1 row is then flagged as out of range).  Short
+ * (n_s >= 2) take the tensor-core (tcgen05) kernel.  Every kernel of the call
+ * runs on `stream`: the decode kernel is launched programmatically right behind
+ * the chunk kernel and runs beside it, on a few SMs that the chunk kernel
+ * leaves free while it computes, then on all of them; work enqueued on `stream`
+ * afterwards sees the whole output.  When total_q_tokens = num_seqs x max_q_len
+ * every query is max_q_len rows long, so there are no decode rows (a query of 1
+ * row is then flagged as out of range).  Short
  * chunks -- max_q_len x (num_q_heads / num_kv_heads) <= 8, e.g. a speculative
  * draft of 2 tokens under a GQA group of 4 ([P3] speculative decoding) -- run
  * instead with the whole batch in the decode kernel, whose CTA then covers all
@@ -378,8 +379,8 @@ PAGEDKV_API size_t paged_attention_chunked_prefill_workspace_size(int32_t num_se
                                                       int32_t num_splits);
 
 /* Number of kernels one successful paged_attention_chunked_prefill call with
- * these sizes enqueues, on the caller's stream and the library's side stream
- * together (host-only; reads no device memory).  With max_q_len = 1 it is also
+ * these sizes enqueues on the caller's stream (host-only; reads no device
+ * memory).  With max_q_len = 1 it is also
  * the count of a paged_attention_decode call with the same num_seqs,
  * num_q_heads, max_blocks_per_seq and num_splits.  Returns 0 for sizes a call
  * would accept without launching anything (no sequences or no query rows) and

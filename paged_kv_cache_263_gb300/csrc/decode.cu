@@ -71,6 +71,11 @@ struct DecodeParams {
     int part_blocks;
     int num_splits;
     float scale_log2;          // softmax scale * log2(e)
+    // launched programmatically right after the chunk-prefill kernel of the same
+    // call, to run beside it: every input was written before that call's first
+    // kernel, so only the first CTA waits for the chunk kernel (the grid then
+    // completes after it, and the kernels behind it see both grids' results)
+    int corun;
 };
 
 // Ring depth per warp and CTAs per SM (compile-time).  Measured on GB300:
@@ -165,7 +170,7 @@ __global__ void __launch_bounds__(THREADS, PKV_DECODE_MIN_CTAS)
     const int gq = lane >> 2, cq = lane & 3;
     // launched with programmatic serialisation: the CTA may be resident before
     // the previous kernel on the stream (typically the cache write) finished
-    griddep_wait();
+    if (!p.corun || (blockIdx.x | blockIdx.y | blockIdx.z) == 0) griddep_wait();
 
     // s: sequence (block table); row: (first) row of q/out; wi: index of the
     // partials; nq: query rows of the sequence this CTA covers
@@ -706,7 +711,7 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
               const int32_t *cu_q_lens, int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t hkv,
               int32_t num_blocks, float scale, kv_dtype dt, const float *k_scale, const float *v_scale,
               int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st,
-              int32_t multi_q_len, bool pdl)
+              int32_t multi_q_len, bool pdl, bool corun = false)
 {
     const bool multi = multi_q_len > 0;
     if (multi && (!cu_q_lens || total_rows < 0)) return KV_ERR_INVALID;
@@ -740,6 +745,7 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
     p.group = G;
     p.num_blocks = num_blocks;
     p.scale_log2 = scale * LOG2E;
+    p.corun = corun && pdl ? 1 : 0;
     plan_splits(max_blocks, num_splits, num_seqs, hq, &p.part_blocks, &p.num_splits);
     // columns of one sequence and KV head: its rows x the group's heads
     const int64_t cols = multi ? (int64_t)multi_q_len * G : G;

@@ -45,8 +45,13 @@
 //  * Long contexts are cut into equal partitions of whole tiles (at most
 //    16,384 keys, less when the grid would be too small to fill the GPU),
 //    merged by a fixed-order log-sum-exp kernel (no atomics).
-//  * Decode rows (n = 1) of the batch run on a library-owned side stream in
-//    the decode kernel, concurrently with the chunk tiles.
+//  * Decode rows (n = 1) of the batch run in the decode kernel, launched
+//    programmatically right behind the chunk kernel on the caller's stream.  A
+//    chunk CTA's shared memory leaves no room for a decode CTA beside it, so the
+//    work-list kernel leaves a few SMs without a chunk CTA (a model of both
+//    kernels' rates), and the decode CTAs stream their K/V there while the
+//    chunk tiles compute on the others; once the chunk kernel is done they take
+//    every SM.
 //
 // fp8 cache: the same kernel with four more warps that widen each e4m3 K/V tile
 // (landed by TMA in a staging ring) to f16 operand tiles -- exact, as every
@@ -171,7 +176,8 @@ struct PrefillParams {
     int32_t *tile_off;   // [num_seqs + 1] pairs of query tiles per sequence, prefix sums
     int4 *order;         // work items, longest first: two int4 each (see tile_prefix_kernel)
     int32_t *row_info;   // [rows] key partitions of the row's query item (0: not a chunk row)
-    int32_t *order_count;  // [0] items listed, [1] items taken so far (the CTAs' counter), [2] any cut
+    int32_t *order_count;  // [0] items listed, [1] items taken so far (the CTAs' counter), [2] any cut,
+                           // [3] CTAs that take items (the others leave their SMs to the decode rows)
     int items_cap;       // query items the order array has room for (x 1 KV head x 1 partition)
     float *part_o;       // [rows][Hq][max_splits][128]
     float *part_ml;      // [rows][Hq][max_splits][2]
@@ -183,6 +189,9 @@ struct PrefillParams {
     int max_q_len;                     // the caller's bound on every query's rows (a longer one is flagged)
     int grid_ctas;                     // the chunk kernel's CTAs
     int q_box_bytes;                   // one 64-dim half of a query tile as loaded (rows x G x 128 B)
+    int corun;           // the decode rows run beside the chunk kernel, on SMs it leaves free
+    float decode_key_bytes;   // K and V bytes of one key of a decode row (all KV heads)
+    float decode_sm_bytes;    // bytes the decode CTAs of one SM read in one KV tile's time
     int item_tiles;      // query tiles per CTA: 2 (a pair), or 1 (the 128-key layout)
     int tile_keys;       // keys per KV tile: 64, or 128 (the 128-key layout)
     float scale_log2;
@@ -294,6 +303,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // to see as many keys as its last one.
 constexpr int PREFIX_SMAX = 2048;
 constexpr int PREFIX_XMAX = 8192;   // query items whose sequence is tabled in shared memory
+constexpr float ITEM_TILES = 0.5f;   // a work item's Q load and epilogue, in tile-times
 __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
 {
     __shared__ int32_t warp_sums[32];
@@ -305,8 +315,8 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     // warp at a time: shared-memory atomics on one word serialise a warp)
     __shared__ unsigned int c_items[2];
     __shared__ int c_tmax[2], c_tmin[2];
-    __shared__ float c_mrows, s_tiles;
-    __shared__ int s_tps, s_nsmax, s_cut;
+    __shared__ float c_mrows, s_tiles, s_dkeys, s_merge;
+    __shared__ int s_tps, s_nsmax, s_cut, s_ctas, s_tbest;
     constexpr int NBKT = 32;
     static_assert(NBKT == 32, "one warp scans the buckets");
     __shared__ int32_t cnt[32][NBKT];
@@ -330,6 +340,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
     if (threadIdx.x == 0) {
         carry = 0;
         s_tiles = 0.f;
+        s_dkeys = 0.f;
         c_mrows = 0.f;
         sh_toff[0] = 0;
     }
@@ -361,6 +372,8 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
             unsigned it0 = 0u, it1 = 0u;
             int mx0 = 0, mn0 = INT_MAX, mx1 = 0, mn1 = INT_MAX;
             float tl = 0.f, mr = 0.f;
+            // a decode row's keys (read by the decode kernel beside this one)
+            float dk = (n == 1 && L > 0) ? (float)min(L, p.max_blocks * BS) : 0.f;
             if (tiles > 0) {
                 const int KT = (L + tk - 1) / tk;
                 // the items' tiles: item x sees L - n + min(n, (x + 1) r) keys, r rows per item
@@ -373,6 +386,11 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
                 if (ns > 1) mr = (float)n * ns;
                 it1 = (unsigned)tiles;
                 mx1 = mn1 = KT;
+            }
+            if (p.corun && __any_sync(0xffffffffu, dk > 0.f)) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) dk += __shfl_xor_sync(0xffffffffu, dk, o);
+                if (lane == 0) atomicAdd(&s_dkeys, dk);
             }
             if (__any_sync(0xffffffffu, tiles > 0)) {
                 it0 = __reduce_add_sync(0xffffffffu, it0);
@@ -435,7 +453,6 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         // a partial result (130 floats per head) is written and read once
         const float per_row_split = (float)p.hq * 130.f * 4.f * 2.f / p.bytes_per_tile;
         const float merge_start = 3.f * 64.f / tk;   // the merge kernel's start, in tile-times
-        constexpr float ITEM_TILES = 0.5f;           // per item: its Q load and epilogue
         auto est = [&](int k, float merge) {
             return fmaxf((float)c_tmax[k], S / m + 0.5f * (float)c_tmin[k]) +
                    (float)c_items[k] * p.hkv * ITEM_TILES / m + merge;
@@ -451,8 +468,42 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
         s_nsmax = (max(c_tmax[1], 1) + pick - 1) / pick;   // the most partitions of any item
         s_cut = cut;
         p.order_count[2] = cut;                      // the merge kernel has work
+        s_merge = cut ? c_mrows * per_row_split + merge_start : 0.f;
+        s_tbest = __float_as_int(INFINITY);
+        s_ctas = p.corun && s_dkeys > 0.f ? 0 : p.grid_ctas;
     }
     __syncthreads();
+    // ---- 2b. The decode rows run beside this kernel on the SMs that its CTAs
+    // leave free (the decode kernel is launched right behind it, and a chunk CTA's
+    // shared memory leaves no room for a decode CTA): c CTAs take items, the other
+    // SMs read decode K/V at decode_sm_bytes per tile-time each, and what is left
+    // when the chunk work ends is read by every SM at the HBM rate.  c is the
+    // largest count whose modelled end of both is within 0.1 % of the least (one
+    // candidate per thread).
+    if (s_ctas == 0) {
+        const int c_lo = max(1, p.grid_ctas / 2);
+        const int ncand = min(p.grid_ctas - c_lo + 1, (int)blockDim.x);
+        int c = 0;
+        float t = INFINITY;
+        if ((int)threadIdx.x < ncand) {
+            c = p.grid_ctas - (int)threadIdx.x;
+            const int k = s_cut ? 0 : 1;
+            const float fc = (float)c, S = s_tiles * p.hkv;
+            const float chunk = fmaxf((float)c_tmax[k], S / fc + 0.5f * (float)c_tmin[k]) +
+                                (float)c_items[k] * p.hkv * ITEM_TILES / fc + s_merge;
+            const float beside = fminf((float)(p.num_sms - c) * p.decode_sm_bytes, p.bytes_per_tile);
+            t = chunk + fmaxf(0.f, s_dkeys * p.decode_key_bytes - chunk * beside) / p.bytes_per_tile;
+        }
+        float tm = t;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tm = fminf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+        if (lane == 0 && tm < INFINITY) atomicMin(&s_tbest, __float_as_int(tm));   // (t >= 0)
+        __syncthreads();
+        const int cm = __reduce_max_sync(0xffffffffu, t <= __int_as_float(s_tbest) * 1.001f ? c : 0);
+        if (lane == 0 && cm > 0) atomicMax(&s_ctas, cm);
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) p.order_count[3] = s_ctas;
     const int tps = s_tps;
     const int32_t *toff = staged ? sh_toff : p.tile_off;
     const int32_t *cu = staged ? sh_cu : p.cu_q_lens;
@@ -547,7 +598,7 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(PrefillParams p)
             p.order_count[0] = v * p.hkv;
             // the persistent CTAs' fetch counter: CTA c takes item c first, the
             // rest through the counter
-            p.order_count[1] = p.grid_ctas;
+            p.order_count[1] = s_ctas;
         }
     }
     __syncthreads();
@@ -728,7 +779,9 @@ __global__ void __launch_bounds__(FP8 ? 512 : Lay<FP8, BIG>::THREADS, 1)
                 // every listed partition is non-empty, but a CTA never trusts that
                 // to keep its pipelines in step
                 it.valid = 0;
-                for (int tries = 0;; ++tries) {
+                // CTAs past the work list's count leave their SMs to the decode rows
+                const bool idle = k == 0 && (int)blockIdx.x >= p.order_count[3];
+                for (int tries = 0; !idle; ++tries) {
                     int idx = (int)blockIdx.x;           // the first item: no round trip
                     if (k > 0 || tries > 0) {
                         if (lane == 0) idx = atomicAdd(p.order_count + 1, 1);
@@ -1295,6 +1348,14 @@ constexpr int64_t NUM_SMS = 152;               // a chunk CTA holds a whole SM: 
 constexpr double CTA_FIXED_TILES = 4.0;        // a CTA's Q load, set-up and epilogue, in tile-times
 // HBM bytes moved while a CTA works through one 64-key tile (~0.86 us at ~6.5 TB/s)
 constexpr double BYTES_PER_TILE_TIME = 5.6e6;
+// bytes the decode kernel's CTAs on one SM (three of them) read while a chunk CTA
+// works through one 64-key tile, with the chunk kernel on the other SMs.  Fitted
+// on GB300 to the mixed batch (1,024-row chunk + 255 decode rows): the best
+// whole call came with 140 chunk CTAs of 152 (bf16 cache), 3.098 ms, against
+// 3.157-3.353 ms at 124-136 and 3.150-3.263 ms at 144-148; this rate makes the
+// model take 139 (and 145 over an fp8 cache, whose decode rows read half the
+// bytes: 3.150-3.155 ms at 140-148)
+constexpr double DECODE_SM_BYTES_PER_TILE_TIME = 120.0 * 1024.0;
 
 struct Plan {
     size_t decode_bytes, part_o_off, part_ml_off, tile_off_off, order_off, row_info_off, total;
@@ -1310,7 +1371,7 @@ kv_status run(float *out, const void *q, const void *k_cache, const void *v_cach
               const int32_t *cu_q_lens, int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t hkv,
               int32_t num_blocks, float scale, kv_dtype dt, const float *k_scale, const float *v_scale,
               int32_t num_splits, void *workspace, size_t workspace_bytes_given, cudaStream_t st,
-              int32_t multi_q_len, bool pdl);
+              int32_t multi_q_len, bool pdl, bool corun);
 size_t workspace_bytes(int32_t num_seqs, int32_t hq, int32_t max_blocks, int32_t num_splits);
 size_t workspace_bytes_multi(int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t max_blocks,
                              int32_t num_splits);
@@ -1423,16 +1484,7 @@ bool use_big(kv_dtype dt, int32_t max_q_len, int32_t hq, int32_t hkv)
 }  // namespace
 
 namespace {
-// A library-owned stream per device on which the decode rows of a mixed batch
-// run next to the chunk tiles (memory-bound next to tensor-bound work), joined
-// back into the caller's stream with events.
-struct SideStream {
-    cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
 constexpr int MAX_DEVICES = 64;
-std::mutex g_side_mu;
-SideStream g_side[MAX_DEVICES];
 
 // SMs of the current device (the persistent chunk grid's size)
 int num_sms()
@@ -1444,19 +1496,6 @@ int num_sms()
     return n;
 }
 
-SideStream *side_stream()
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
-    SideStream &ss = g_side[dev];
-    if (!ss.stream) {
-        if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
-            return nullptr;
-    }
-    return &ss;
-}
 }  // namespace
 
 namespace {
@@ -1563,7 +1602,8 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
         // short chunks: the decode kernel's multi-row mode for the whole batch
         return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
-                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, max_q_len, true);
+                               k_scale, v_scale, num_splits, workspace, workspace_bytes, st, max_q_len, true,
+                               false);
     }
     if (dtype == KV_FP8_E4M3 && (!k_scale || !v_scale)) return KV_ERR_INVALID;
     const bool big = use_big(dtype, max_q_len, num_q_heads, num_kv_heads);
@@ -1572,40 +1612,16 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     if (pl.total && (!workspace || workspace_bytes < pl.total || !pkv_host::aligned(workspace, 256)))
         return KV_ERR_INVALID;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    auto decode_rows = [&](cudaStream_t on, bool pdl) {
+    auto decode_rows = [&](cudaStream_t on, bool pdl, bool beside) {
         return pkv_decode::run(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, cu_q_lens,
                                total_q_tokens, num_seqs, num_q_heads, num_kv_heads, num_blocks, scale, dtype,
                                k_scale, v_scale, num_splits, pl.decode_bytes ? ws : nullptr, pl.decode_bytes, on,
-                               0, pdl);
+                               0, pdl, beside);
     };
-    if (max_q_len < 2) return decode_rows(st, true);   // decode rows only
-    // decode rows (n = 1) on the side stream, forked from and joined into the
-    // caller's stream; the chunk tiles run on the caller's stream meanwhile.
-    // There are none when total_q_tokens = num_seqs x max_q_len (every query is
-    // max_q_len long; tile_prefix_kernel flags a row of 1 then).
+    if (max_q_len < 2) return decode_rows(st, true, false);   // decode rows only
+    // decode rows (n = 1): none when total_q_tokens = num_seqs x max_q_len (every
+    // query is max_q_len long; tile_prefix_kernel flags a row of 1 then)
     const bool rows1 = (int64_t)total_q_tokens != (int64_t)num_seqs * max_q_len;
-    std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
-    SideStream *side = nullptr;
-    kv_status rs = KV_OK;
-    if (rows1) {
-        side_lock.lock();
-        side = side_stream();
-        if (!side) return KV_ERR_CUDA;
-        if (cudaEventRecord(side->fork, st) != cudaSuccess ||
-            cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
-            return KV_ERR_CUDA;
-        rs = decode_rows(side->stream, false);   // fed by an event, not a kernel
-        if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return KV_ERR_CUDA;
-    }
-    struct Join {   // the caller's stream waits for the decode rows however this call ends
-        cudaStream_t st;
-        SideStream *side;
-        ~Join()
-        {
-            if (side) cudaStreamWaitEvent(st, side->join, 0);
-        }
-    } join{st, side};
-    if (rs != KV_OK) return rs;
     // prefill chunks (n >= 2)
     PrefillParams p{};
     p.out = out;
@@ -1639,6 +1655,11 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     p.rows1 = rows1 ? 1 : 0;
     p.max_q_len = max_q_len;
     p.bytes_per_tile = (float)(BYTES_PER_TILE_TIME * p.tile_keys / 64.0);
+    Trace *tr = trace_for_call();
+    // (a traced call times the chunk kernel alone: its decode rows run after it)
+    p.corun = rows1 && !tr ? 1 : 0;
+    p.decode_key_bytes = (float)num_kv_heads * D * 2 * (dtype == KV_FP8_E4M3 ? 1 : 2);
+    p.decode_sm_bytes = (float)(DECODE_SM_BYTES_PER_TILE_TIME * p.tile_keys / 64.0);
     CUtensorMap qm, km, vm;
     const int tpt = BM / G;
     // the 128-key layout holds one query tile per sequence (max_q_len x G <= 128):
@@ -1669,11 +1690,13 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     const int64_t ctas_ub = pl.items_ub * num_kv_heads * p.max_splits;
     if (ctas_ub > INT32_MAX || p.max_splits > 65535 || num_kv_heads > 65535) return KV_ERR_UNSUPPORTED;
     p.grid_ctas = (int)std::min<int64_t>(ctas_ub, p.num_sms);
+    // (a plain launch when there are decode rows: the decode CTAs, which start
+    // while the chunk kernel runs, read their inputs without waiting, so every
+    // kernel before this call must have finished)
     if (pkv_host::launch_ex(tile_prefix_kernel, dim3(1), dim3(1024), 0, st, !rows1, p) != cudaSuccess)
         return KV_ERR_CUDA;
     // persistent: one CTA per SM (a CTA holds a whole SM), at most one per work item
     dim3 grid((unsigned)p.grid_ctas);
-    Trace *tr = trace_for_call();
     if (tr) cudaEventRecord(tr->start, st);
     // programmatic serialisation: the CTAs' set-up overlaps tile_prefix_kernel
     // (trace events between the two only make the launch plain)
@@ -1694,6 +1717,14 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
         tr->recorded = true;
     }
     if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
+    if (rows1) {
+        // the decode rows, launched programmatically behind the chunk kernel: their
+        // CTAs start on the SMs the chunk kernel leaves free while it runs (a chunk
+        // CTA's shared memory leaves no room for one beside it), and on every SM
+        // once it is done
+        const kv_status r = decode_rows(st, true, p.corun != 0);
+        if (r != KV_OK) return r;
+    }
     if (p.max_splits > 1) {
         const int64_t warps = (int64_t)total_q_tokens * num_q_heads;
         if (pkv_host::launch_ex(prefill_reduce_kernel,

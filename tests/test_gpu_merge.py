@@ -102,7 +102,8 @@ def test_multi_row_merge_with_garbage_workspace(kv_dtype):
 
 
 def test_mixed_batch_decode_rows_merge():
-    """Decode rows of a mixed batch (side stream) merge their partitions too."""
+    """Decode rows of a mixed batch (run beside the chunk kernel) merge their
+    partitions too."""
     wl = small_workload(506, lens=[3000, 2100, 90, 5000], q_lens=[1, 200, 1, 1], hq=16, hkv=2, num_splits=6)
     dw = DeviceWorkload(wl)
     dw.workspace.fill_(0x77)

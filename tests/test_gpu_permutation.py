@@ -2,8 +2,8 @@
 section "PagedAttention": the kernel reads the same values through the table,
 wherever the blocks sit).  At the full sizes of every workload, in the launch
 configuration the benchmark times -- the partition plans chosen for those sizes,
-the multi-row mode, the tensor-core chunk kernel and the side-stream decode
-rows --, the same batch is placed by three different seeded permutations of
+the multi-row mode, the tensor-core chunk kernel and the decode rows that run
+beside it --, the same batch is placed by three different seeded permutations of
 the physical pool and the whole output must be bitwise identical.  The
 comparison is made on the device; no oracle is involved."""
 import numpy as np
