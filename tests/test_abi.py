@@ -263,9 +263,20 @@ class _FakeDeviceTensor:
 def test_static_scratch_decode_checks_the_caches_before_any_launch(bad, monkeypatch):
     """A CPU or non-contiguous cache is refused by the binding with ValueError
     before the library is called, as paged_attention_decode does."""
+    import gc
     import torch
+
+    # records which library entry points are reached (a host object of an
+    # earlier test, collected meanwhile, may reach its own destructor's call)
     called = []
-    monkeypatch.setattr(pkv, "lib", lambda: called.append(1))
+
+    class _Recorder:
+        def __getattr__(self, name):
+            called.append(name)
+            return lambda *a, **k: 0
+
+    gc.collect()
+    monkeypatch.setattr(pkv, "lib", lambda: _Recorder())
     out = _FakeDeviceTensor(torch.float32, (2, 8, 128))
     q = _FakeDeviceTensor(torch.bfloat16, (2, 8, 128))
     bt = _FakeDeviceTensor(torch.int32, (2, 4))
@@ -282,4 +293,4 @@ def test_static_scratch_decode_checks_the_caches_before_any_launch(bad, monkeypa
         k.is_contiguous = lambda: False
     with pytest.raises(ValueError, match="k_cache|v_cache"):
         pkv.paged_attention_decode_static_scratch(out, q, k, v, bt, cl)
-    assert not called
+    assert "paged_attention_decode_static_scratch" not in called
