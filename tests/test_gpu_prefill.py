@@ -288,3 +288,21 @@ def test_many_ragged_chunks_in_the_pair_layout(kv_dtype):
     _, _, ref = expected_full(wl)
     _, got = _run(wl)
     check_close(got, ref, kv_dtype, "48 ragged chunks")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_decode_heavy_mixed_batch(kv_dtype):
+    """One 32-row chunk over 16,384 keys (cut into partitions and merged) beside
+    100 decode rows of 200..700 keys: the decode rows' bytes outweigh the chunk's
+    work, so the work-list kernel leaves many SMs without a chunk CTA and the
+    decode kernel, launched right behind the chunk kernel, runs there.  Every
+    row matches the oracle, and a NaN-poisoned pool gives the same bits."""
+    rng = np.random.default_rng(1700)
+    lens = np.concatenate([[16384], rng.integers(200, 700, size=100)]).astype(np.int32)
+    qlens = np.concatenate([[32], np.ones(100, np.int32)]).astype(np.int32)
+    wl = small_workload(1700, lens=lens, q_lens=qlens, hq=16, hkv=4, kv_dtype=kv_dtype)
+    _, _, ref = expected_full(wl)
+    _, got = _run(wl)
+    check_close(got, ref, kv_dtype, "decode-heavy mixed batch")
+    _, dirty = _run(small_workload(1700, lens=lens, q_lens=qlens, hq=16, hkv=4, kv_dtype=kv_dtype), poison=True)
+    assert np.array_equal(got, dirty)
