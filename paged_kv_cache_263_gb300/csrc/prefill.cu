@@ -281,11 +281,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-// The chunk kernel's work list, one CTA of 1024 threads:
+// The chunk kernel's work list, one CTA of 128 to 1024 threads (sized by the
+// host to the batch; every phase is written for any whole number of warps):
 //  1. per sequence (a thread each): the chunk metadata validated, its query
 //     items counted (then a block-wide scan), and its share of the partition
 //     length estimates below;
-//  2. the partition length;
+//  2. the partition length; with decode rows in the batch, 2b. the number of
+//     chunk CTAs that take items;
 //  3. per query row, the number of key partitions its item is cut into (for
 //     the merge kernel); the work items' bucket counts;
 //  4. the work items in launch order.
@@ -1693,7 +1695,15 @@ kv_status paged_attention_chunked_prefill(float *out, const void *q, const int32
     // (a plain launch when there are decode rows: the decode CTAs, which start
     // while the chunk kernel runs, read their inputs without waiting, so every
     // kernel before this call must have finished)
-    if (pkv_host::launch_ex(tile_prefix_kernel, dim3(1), dim3(1024), 0, st, !rows1, p) != cudaSuccess)
+    // (its block: a thread per sequence or per four query rows, 128 to 1,024.
+    // The kernel is a chain of block-wide phases, so idle warps cost issue slots
+    // at every one of them -- 1,024 threads took 7.4 us for 32 sequences of 8
+    // rows -- while the per-row phase wants threads: 128 took 2.5 us longer than
+    // 1,024 for 1,087 rows)
+    const int64_t tp_want = std::max<int64_t>(num_seqs, ((int64_t)total_q_tokens + 3) / 4);
+    const int tp_threads = (int)std::min<int64_t>(1024, std::max<int64_t>(128, (tp_want + 31) / 32 * 32));
+    if (pkv_host::launch_ex(tile_prefix_kernel, dim3(1), dim3((unsigned)tp_threads), 0, st, !rows1, p) !=
+        cudaSuccess)
         return KV_ERR_CUDA;
     // persistent: one CTA per SM (a CTA holds a whole SM), at most one per work item
     dim3 grid((unsigned)p.grid_ctas);
