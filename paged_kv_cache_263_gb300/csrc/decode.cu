@@ -706,6 +706,9 @@ bool make_maps(const void *k_cache, const void *v_cache, int32_t num_blocks, int
 // launch when pdl is set (see pkv_host::launch_ex).  Needing cu_q_lens:
 //  multi_q_len > 0 multi-row mode: every sequence's rows (at most multi_q_len)
 //                  are covered by column groups of one CTA per KV tile stream.
+// corun (with pdl): launched right behind a mixed batch's chunk-prefill kernel,
+// whose inputs and these were all written before that call began; only the
+// grid's first CTA waits for the chunk kernel, the others start beside it.
 kv_status run(float *out, const void *q, const void *k_cache, const void *v_cache,
               const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
               const int32_t *cu_q_lens, int32_t total_rows, int32_t num_seqs, int32_t hq, int32_t hkv,
