@@ -16,7 +16,7 @@
 //    group; the two tiles of a pair share every K/V tile as well.  Both Q tiles
 //    land in shared memory with one 3-D TMA load each.
 //  * K/V tiles of 64 keys = 4 physical blocks, gathered through the block
-//    table by TMA loads (128-byte swizzle) into a 4-stage ring (warp 8): K as
+//    table by TMA loads (128-byte swizzle) into a 5-stage ring (warp 8): K as
 //    two 2-D boxes per block (each 64-dim half of the tile's keys contiguous, as
 //    the QK^T operand needs), V as one 3-D box per block holding both halves.
 //  * Chunks whose rows x heads fit one 128-row tile (speculative drafts) take a
@@ -93,6 +93,7 @@ constexpr uint32_t F8_STAGE_BYTES = 16384, F8_V_OFF = 8192;
 // product is N = 128: half the product instructions per key, which is what a
 // CTA with a single issuer waits on.  Three stages of 64 KiB keep the same
 // bytes in flight as four of 32 KiB.
+constexpr int MAX_KV_STAGES = 5;   // room in the barrier table
 template <bool FP8, bool BIG = false>
 struct Lay {
     static constexpr int BNK = BIG ? 128 : 64;               // keys per KV tile
@@ -109,7 +110,9 @@ struct Lay {
     // itself, between items that are long
     static constexpr int W_TAIL = BIG ? W_PROD2 + 1 : -1;
     static constexpr int THREADS = 32 * (W_WIDEN + (FP8 ? 4 : 0) + (BIG ? 2 : 0));
-    static constexpr int KV_STAGES = BIG ? 3 : (FP8 ? 3 : 4);
+    // (bf16 two-tile layout: five stages, 224 KiB with Q; measured on GB300 the
+    // fifth stage took 1.6-1.9 % off the long chunk's kernel time)
+    static constexpr int KV_STAGES = BIG ? 3 : (FP8 ? 3 : 5);
     static constexpr uint32_t KV_HALF = BNK * 128;           // one 64-dim half of a K or V tile
     static constexpr uint32_t V_OFF = 2 * KV_HALF;
     static constexpr uint32_t KV_STAGE_BYTES = 4 * KV_HALF;  // K and V
@@ -124,14 +127,15 @@ struct Lay {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(NG * (S_COLS + 128) <= 512, "tensor memory");
     static_assert(!(FP8 && BIG), "the 128-key layout is for the bf16 cache");
+    static_assert(KV_STAGES <= MAX_KV_STAGES && F8_STAGES <= 3, "barrier table");
 };
 // work items a CTA's producer may have fetched ahead of its slowest warp
 constexpr int NSLOT = 4;
 // barriers (room for the larger of the two layouts)
 enum {
     B_KVF = 0,                      // + stage: K and V operand tiles ready
-    B_KVE = B_KVF + 4,              // + stage: every MMA reading the stage is done
-    B_Q = B_KVE + 4,                // the item's Q tiles landed
+    B_KVE = B_KVF + MAX_KV_STAGES,              // + stage: every MMA reading the stage is done
+    B_Q = B_KVE + MAX_KV_STAGES,                // the item's Q tiles landed
     B_QFREE = B_Q + 1,              // every QK^T product of the item finished (one per issuer)
     B_QC = B_QFREE + 1,             // + group: fp8 cache: the group's Q tile is in f16
     B_S = B_QC + 2,                 // + 2*group + buffer: an S tile of the group is in TMEM
@@ -139,12 +143,12 @@ enum {
     B_PVD = B_P + 4,                // + group: the group's latest PV product finished
     B_DRAIN = B_PVD + 2,            // + group: every MMA of the group's item finished
     B_TAIL = B_DRAIN + 2,           // + stage: bf16 cache: the V rows past the context are zeroed
-    B_F8F = B_TAIL + 4,             // + staging stage: fp8 cache: e4m3 K and V landed
+    B_F8F = B_TAIL + MAX_KV_STAGES,             // + staging stage: fp8 cache: e4m3 K and V landed
     B_F8E = B_F8F + 3,              // + staging stage: fp8 cache: the stage was widened
     B_IFULL = B_F8E + 3,            // + slot: the producer wrote a work item into the slot
     B_IEMPTY = B_IFULL + NSLOT,     // + slot: every other warp has read it
     B_TGO = B_IEMPTY + NSLOT,       // + stage: bf16 cache: an item's last tile, past the context, landed
-    NBAR = B_TGO + 4
+    NBAR = B_TGO + MAX_KV_STAGES
 };
 // a work item as the producer hands it to the other warps (valid = 0: no more)
 struct ItemSlot {
