@@ -91,8 +91,8 @@ constexpr uint32_t F8_STAGE_BYTES = 16384, F8_V_OFF = 8192;
 // 4 producer of K, 5 issuer, 6 producer of V -- and tiles of 128 keys.  With one query tile the
 // tensor memory holds two S buffers of 128 columns next to O, so each QK^T
 // product is N = 128: half the product instructions per key, which is what a
-// CTA with a single issuer waits on.  Three stages of 64 KiB keep the same
-// bytes in flight as four of 32 KiB.
+// CTA with a single issuer waits on.  Three stages of 64 KiB (192 KiB) are as
+// many as fit beside the query tile.
 constexpr int MAX_KV_STAGES = 5;   // room in the barrier table
 template <bool FP8, bool BIG = false>
 struct Lay {
