@@ -30,7 +30,9 @@ verifying a 4-token draft: 4 causal query rows per sequence) and
 serving", speculative decoding: a draft of N = 4-8 tokens verified in one
 forward pass); ``mixed_prefill_small`` (the mixed batch scaled down for
 profiling); ``prefill_chunk`` (the mixed batch's chunk without its decode
-rows: the tensor-core kernel alone).
+rows: the tensor-core kernel alone); ``prefill_chunk_small`` (the chunk of
+``mixed_prefill_small`` alone, for full profiler captures of that kernel on
+every SM).
 
 fp8 workloads carry per-KV-head scales for K and for V (``fp8_scales``):
 amax / 448 over every value of that head and tensor in the workload.
@@ -346,12 +348,22 @@ def _make(name: str) -> Workload:
         return Workload("prefill_chunk", seed, 64, 8, pool, "bf16", lens, np.array([1024], np.int32),
                         rng.permutation(pool),
                         description="one 1,024-token chunk over 100,000 cached tokens, alone")
+    if name == "prefill_chunk_small":
+        # the chunk of the small mixed batch alone: about 0.3 GB of K/V (above
+        # L2), for multi-pass profiler captures of the tensor-core kernel
+        seed = 2647
+        rng = np.random.Generator(np.random.PCG64(seed))
+        lens = np.array([41024], dtype=np.int32)
+        pool = _pool_to_fit(lens, 0, -1)
+        return Workload("prefill_chunk_small", seed, 64, 8, pool, "bf16", lens, np.array([1024], np.int32),
+                        rng.permutation(pool),
+                        description="one 1,024-token chunk over 40,000 cached tokens, alone")
     raise KeyError(name)
 
 
 WORKLOADS = ("tiny", "llama8b", "llama70b_prefix", "mixed_prefill", "split_fp8")
 EXTRA_WORKLOADS = ("mixed_prefill_small", "mixed_prefill_small_fp8", "mixed_prefill_fp8", "spec_verify", "spec_verify8",
-                   "prefill_chunk")
+                   "prefill_chunk", "prefill_chunk_small")
 
 
 def small_workload(seed: int, lens, q_lens=None, hq=8, hkv=2, kv_dtype="bf16", num_blocks=None,
